@@ -1,0 +1,410 @@
+"""Benchmark of the KIVI quantized KV cache on GB300: one step = append one
+new K/V token to every sequence + decode attention over the whole cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  `value` is the effective HBM throughput of the
+step: the algorithmic bytes of append + decode (the bytes the method must
+move, not what the kernels happen to move) divided by the CUDA-event time of
+the K timed steps, summed over ranks.  Inputs are resident in HBM before the
+timed region; the caches rotate over replicas whose total footprint is well
+above the 129 MB L2, so every step streams from DRAM.
+
+Multi-GPU: the workload is replicated per GPU (independent sequences need no
+exchange); time is the max over ranks and `value` the sum of all ranks'
+bytes over it ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attn effective HBM GB/s & % of 8 TB/s; append tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mha7b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0 = enough for 4x L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def workload(name):
+    from kivi_quantized_kv_gb300.synth import WORKLOADS, sweep_workload
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    if name.startswith("sweep_"):   # sweep_B<batch>_T<tokens>_b<bits>
+        _, b, t, bits = name.split("_")
+        return sweep_workload(int(b[1:]), int(t[1:]), int(bits[1:]))
+    raise SystemExit(f"unknown workload {name}")
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "batch": w.batch, "h_q": w.h_q, "h_kv": w.h_kv, "head_dim": w.head_dim,
+           "tokens": w.tokens, "bits": w.bits, "group": w.group, "residual": w.residual, "sinks": w.sinks,
+           "window": w.window, "layers": 1}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for i, n in enumerate(names):
+                    if r[5 + i].lower().startswith("active"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- bytes
+def append_bytes(w, L_before, L_after, n=1):
+    """Algorithmic bytes of appending n tokens per sequence: read the new
+    fp16 K/V, write them to the ring (or fp32 sinks), and for every group the
+    append freezes read its G fp16 tokens and write its block."""
+    units = w.batch * w.h_kv
+    d = w.head_dim
+    new_groups = L_after["n_groups"] - L_before["n_groups"]
+    per_unit = n * 8 * d + new_groups * (4 * d * w.group + L_after["block_bytes"])
+    return units * per_unit
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, rank, world, device):
+    import torch
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
+    from kivi_quantized_kv_gb300.synth import KVStream, queries
+
+    w = workload(args.workload)
+    total_steps = args.steps + args.warmup
+    cap_extra = total_steps + 64
+    cfg = KiviConfig.from_workload(w)
+    if w.window == 0:
+        cfg = KiviConfig(**{**cfg.__dict__, "max_tokens": w.tokens + cap_extra})
+    from kivi_quantized_kv_gb300 import cache_bytes
+    per_cache = cache_bytes(cfg)
+    l2 = 129 * 1024 * 1024
+    n_rep = args.replicas or max(2, -(-4 * l2 // per_cache))
+    stream = torch.cuda.current_stream(device)
+
+    caches = []
+    for r in range(n_rep):
+        c = KiviCache(cfg, device=device)
+        kv = KVStream(w.with_(seed=w.seed + 100 * r), device=device)
+        t = 0
+        target = w.tokens - 1
+        while t < target:
+            n = min(4096, target - t)
+            k, v = kv.next(n)
+            c.append(k, v)
+            t += n
+        caches.append((c, kv))
+    # per-step inputs, resident before the timed region
+    new_kv = [caches[s % n_rep][1].next(1) for s in range(total_steps)]
+    qs = [queries(w, step=s, device=device) for s in range(min(total_steps, 64))]
+    out = torch.empty((w.batch, w.h_q, w.head_dim), dtype=torch.float16, device=device)
+    torch.cuda.synchronize(device)
+
+    def step(s, ev=None):
+        c = caches[s % n_rep][0]
+        k, v = new_kv[s]
+        Lb = c.layout()
+        if ev is not None:
+            ev[0].record(stream)
+        c.append(k, v)
+        if ev is not None:
+            ev[1].record(stream)
+        c.decode(qs[s % len(qs)], out=out)
+        if ev is not None:
+            ev[2].record(stream)
+        La = c.layout()
+        return Lb, La, c
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize(device)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t0.record(stream)
+    dec_bytes = app_bytes = launches = 0
+    for i in range(args.steps):
+        s = args.warmup + i
+        Lb, La, c = step(s, evs[i])
+        dec_bytes += c.decode_bytes()
+        app_bytes += append_bytes(w, Lb, La)
+        flush = La["n_groups"] > Lb["n_groups"]
+        launches += (2 if flush else 1) + 2     # append: write (+flush); decode: split + merge
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop() if clocks else None
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    app_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    ms_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    step_bytes = (dec_bytes + app_bytes) / args.steps
+    value = step_bytes * args.steps * world / (ms_max / 1e3) / 1e9
+    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    res = {
+        "w": w, "cfg": cfg, "n_rep": n_rep, "per_cache": per_cache, "ms": ms_max, "value": value,
+        "dec_gbs": dec_gbs, "dec_ms": dec_ms / args.steps, "app_ms": app_ms / args.steps,
+        "dec_bytes": dec_bytes / args.steps, "step_bytes": step_bytes, "launches": launches,
+        "clocks": clk, "app_tok_s": w.batch * args.steps / (app_ms / 1e3),
+    }
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, caches, new_kv, w, device, stream)
+    return res
+
+
+def run_e2e(args, caches, new_kv, w, device, stream):
+    """The same step through the public API with host buffers: pinned host
+    K/V and q copied in, out copied back, inside the timed region."""
+    import torch
+    n_rep = len(caches)
+    steps = min(args.steps, 100)
+    g = torch.Generator().manual_seed(7)
+    k_h = [torch.randn((w.batch, w.h_kv, 1, w.head_dim), generator=g).half().pin_memory() for _ in range(steps)]
+    v_h = [torch.randn((w.batch, w.h_kv, 1, w.head_dim), generator=g).half().pin_memory() for _ in range(steps)]
+    q_h = torch.randn((w.batch, w.h_q, w.head_dim), generator=g).half().pin_memory()
+    out_h = torch.empty_like(q_h).pin_memory()
+    k_d = torch.empty((w.batch, w.h_kv, 1, w.head_dim), dtype=torch.float16, device=device)
+    v_d = torch.empty_like(k_d)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    total = 0
+    for s in range(steps):
+        c = caches[s % n_rep][0]
+        Lb = c.layout()
+        k_d.copy_(k_h[s], non_blocking=True)
+        v_d.copy_(v_h[s], non_blocking=True)
+        c.append(k_d, v_d)
+        c.decode_host(q_h, out_h)
+        total += c.decode_bytes() + append_bytes(w, Lb, c.layout())
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1)
+    h2d = (2 * w.batch * w.h_kv + w.batch * w.h_q) * w.head_dim * 2
+    d2h = w.batch * w.h_q * w.head_dim * 2
+    return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+# --------------------------------------------------------------- oracle arm
+def oracle_sample(w, units_max, seed=0):
+    """An oracle cache holding a bounded sample of the workload: the first
+    `units` (sequence, kv head) units, built from the same generator."""
+    import numpy as np
+    import oracle
+    from kivi_quantized_kv_gb300.synth import KVStream
+    rep = w.h_q // w.h_kv
+    units = min(units_max, w.batch * w.h_kv)
+    hk = min(units, w.h_kv)
+    bs = max(1, units // hk)
+    ws = w.with_(batch=bs, h_kv=hk, h_q=hk * rep)
+    p = oracle.Params(bits=w.bits, group=w.group, residual=w.residual, sinks=w.sinks, h_q=ws.h_q, h_kv=ws.h_kv,
+                      head_dim=w.head_dim, batch=ws.batch, max_tokens=0 if w.window else w.tokens + 4096,
+                      window=w.window)
+    c = oracle.Cache(p)
+    kv = KVStream(ws, device="cpu")
+    t = 0
+    while t < w.tokens - 1:
+        n = min(4096, w.tokens - 1 - t)
+        k, v = kv.next(n)
+        c.append(k.numpy(), v.numpy())
+        t += n
+    return c, ws, kv
+
+
+def time_oracle(w, budget_s=12.0, units_max=None):
+    import numpy as np
+    import torch
+    from kivi_quantized_kv_gb300.synth import queries
+    cores = os.cpu_count() or 1
+    units_max = units_max or max(cores * 2, 8)
+    t_build = time.perf_counter()
+    c, ws, kv = oracle_sample(w, units_max)
+    t_build = time.perf_counter() - t_build
+    q = queries(ws).numpy()
+    steps = 0
+    total = 0
+    tt = 0.0
+    while tt < budget_s and steps < 50:
+        k, v = kv.next(1)
+        t0 = time.perf_counter()
+        c.append(k.numpy(), v.numpy())
+        c.decode_attn(q, threads=cores)
+        tt += time.perf_counter() - t0
+        total += c.decode_bytes() + ws.batch * ws.h_kv * 8 * w.head_dim
+        steps += 1
+    return {"value": round(total / tt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{ws.batch * ws.h_kv} of {w.batch * w.h_kv} (sequence, kv-head) units of {w.name}, "
+                      f"{steps} steps (append 1 token + fp64 decode), {cores} threads, build {t_build:.1f}s excluded",
+            "steps": steps, "seconds": round(tt, 2)}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workload(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        base = time_oracle(w, budget_s=min(20.0, 2.0 + 0.2 * args.steps))
+        line = {"metric": METRIC, "value": base["value"], "unit": "GB/s", "n_gpus": args.gpus, "steps": base["steps"],
+                "warmup": args.warmup, "ms_per_step": round(base["seconds"] * 1e3 / max(base["steps"], 1), 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "impl": "reference", "config": workload_config(w),
+                "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import __graft_entry__ as ge
+    ge.build()
+
+    r = run_ours(args, rank, world, device)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    traffic = load_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": round(r["value"], 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "config": workload_config(w, {"parallelism": f"replicas{world}",
+                                      "l2": f"{r['n_rep']} rotating cache replicas x {r['per_cache'] / 1e6:.0f} MB "
+                                            f"(> 4x 129 MB L2)"}),
+        "roofline": {"bound": "hbm", "achieved": round(r["dec_gbs"], 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(r["dec_gbs"] / peak, 4), "traffic": traffic,
+                     "kernel": "kivi_decode_attn (split-K + merge)", "peak_source": src,
+                     "bytes_per_launch": int(r["dec_bytes"])},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "decode_gbs": round(r["dec_gbs"], 1),
+        "decode_frac_of_8tbs": round(r["dec_gbs"] / NOMINAL_HBM_GBS, 4),
+        "decode_us": round(r["dec_ms"] * 1e3, 2),
+        "decode_steps_per_s": round(1e3 / r["dec_ms"], 1),
+        "append_us": round(r["app_ms"] * 1e3, 2),
+        "append_tokens_per_s": round(r["app_tok_s"], 1),
+    }
+    if "e2e" in r:
+        line["e2e"] = r["e2e"]
+    if not args.no_cpu_baseline:
+        base = time_oracle(w)
+        line["cpu_baseline"] = {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def load_traffic(name):
+    """DRAM bytes per decode launch from the committed ncu summary, if the
+    kernel has not changed since it was taken (profiles/traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(name)
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

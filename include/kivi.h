@@ -1,0 +1,184 @@
+/*
+ * kivi.h — C ABI of the GB300 (sm_103a) KIVI quantized KV cache.
+ *
+ * One library, libkivi.so, built from kivi_quantized_kv_gb300/csrc.  Plain
+ * pointers and sizes only; no C++ or framework types cross this boundary and no
+ * exception leaves it.
+ *
+ * What the cache computes (sources are the pages the method is described on):
+ *   - KV-cache quantization guide (pigeon), "How it works", steps 1-5: keys
+ *     quantized per channel with one scale and zero point per channel over a
+ *     group of G tokens, values per token, asymmetric
+ *     q = round((x - min) / Δ) with Δ = (max - min) / (2^b - 1); the most
+ *     recent R tokens stay in fp16 until a group fills; decode attention
+ *     softmax(q Kᵀ / sqrt(d)) V reads the packed groups and dequantizes them
+ *     on the fly, never materialising an fp16 copy.
+ *   - tract #2458 "quantized KV-cache storage op (int8/int4)": the first S
+ *     tokens (attention sinks) stay in f32 in both stores; key blocks keep
+ *     frozen scales once written.
+ *   - tract #2329 "KIVI-style KV-cache quantization", "What's in the PR": the
+ *     fused op takes [Q, K_new, V_new], handles GQA, and its output has Q's
+ *     shape; "Relationship to other PRs": a bounded sliding window composes
+ *     with the quantized storage.
+ *
+ * Memory ownership: the caller allocates every device buffer (the arena and
+ * all inputs/outputs).  The library allocates only the small host-side handle
+ * and never allocates, frees or synchronises device memory.
+ *
+ * Concurrency: every call is asynchronous on the given CUDA stream (NULL =
+ * the legacy default stream).  A handle must not be used from two streams or
+ * two host threads at the same time.
+ *
+ * Errors: each call returns a kivi_status.  All parameter checks run on the
+ * host before any launch, so a call that returns an error has changed no
+ * device or host state (except KIVI_ECUDA, raised when a launch itself
+ * fails; the handle's token count is then left at its pre-call value).
+ */
+#ifndef KIVI_H
+#define KIVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kivi_status {
+  KIVI_OK = 0,
+  KIVI_EINVAL = 1,     /* a parameter is outside the supported set */
+  KIVI_EALIGN = 2,     /* a pointer is not aligned as required */
+  KIVI_ECAPACITY = 3,  /* T + n would exceed max_tokens (window == 0) */
+  KIVI_ENOSPC = 4,     /* the arena is smaller than kivi_cache_bytes() */
+  KIVI_ECUDA = 5,      /* a CUDA launch or copy reported an error */
+  KIVI_ENULL = 6       /* a required pointer is NULL */
+} kivi_status;
+
+/* Cache parameters.
+ *   bits       b in {2, 4, 8}: code width.
+ *   group      G: tokens per frozen key group; a multiple of 16 in [16, 256].
+ *   residual   R: capacity of the fp16 residual ring; R >= G and R % G == 0.
+ *   sinks      S in [0, 1024]: leading tokens kept in fp32.
+ *   h_q, h_kv  query and key/value heads; h_q % h_kv == 0; query head h reads
+ *              kv head h / (h_q / h_kv) (contiguous GQA groups).
+ *   head_dim   d in {64, 128}.
+ *   batch      B >= 1 sequences, all of the same length.
+ *   max_tokens capacity in tokens per sequence when window == 0.
+ *   window     W: 0 = attend to every token; W > 0 (W >= R) = attend to the
+ *              sinks and to the most recent W tokens, the stream is unbounded
+ *              and frozen groups live in a ring of ceil(W/G) + 1 slots. */
+typedef struct kivi_params {
+  int32_t bits;
+  int32_t group;
+  int32_t residual;
+  int32_t sinks;
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t head_dim;
+  int32_t batch;
+  int64_t max_tokens;
+  int64_t window;
+} kivi_params;
+
+/* Byte layout of the arena and current state (all offsets in bytes).
+ *
+ * The arena is [cache region][workspace].  The cache region is B * h_kv
+ * units, unit (b, h) at (b * h_kv + h) * unit_bytes; inside a unit:
+ *   sink_k, sink_v  fp32 [S][d]        the sink tokens' keys / values
+ *   res_k, res_v    fp16 [R][d]        ring; token a (>= S) in slot (a-S) % R
+ *   groups          n_slots blocks of block_bytes; frozen group g (tokens
+ *                   S+gG .. S+gG+G-1) in slot g (window == 0) or
+ *                   g % n_slots (window > 0).  Inside a block:
+ *     blk_kq  key codes, token-major: G rows of d*b/8 bytes
+ *     blk_ks  fp16 key Δ[d] then key min[d] (one pair per channel)
+ *     blk_vq  value codes, channel-major: d rows of G*b/8 bytes
+ *     blk_vs  fp16 (Δ, min) per token, G pairs
+ *   A row of codes is cut into little-endian 32-bit words of 32/b codes;
+ *   element j of a word sits in the low 16-bit half when j is even, the high
+ *   half when j is odd, at bit b*floor(j/2) of its half.
+ * The workspace (workspace_offset, workspace_bytes) holds split-K partial
+ * results and per-unit counters; its contents are scratch. */
+typedef struct kivi_layout {
+  int64_t n_slots;
+  int64_t sink_k, sink_v, res_k, res_v, groups;
+  int64_t block_bytes, blk_kq, blk_ks, blk_vq, blk_vs;
+  int64_t unit_bytes, cache_bytes;
+  int64_t workspace_offset, workspace_bytes, arena_bytes;
+  int64_t tokens;     /* T: tokens appended per sequence */
+  int64_t n_sink;     /* min(T, S) */
+  int64_t n_groups;   /* frozen groups written so far */
+  int64_t n_res;      /* tokens live in the ring */
+  int32_t max_splits; /* split-K partitions the workspace holds per head */
+  int32_t reserved;
+} kivi_layout;
+
+typedef struct kivi_cache kivi_cache;
+
+/* Bytes of device memory the arena needs (cache region + workspace), or 0 if
+ * the parameters are invalid.  Host only; touches no device. */
+size_t kivi_cache_bytes(const kivi_params* params);
+
+/* Creates a handle over a caller-owned device arena of at least
+ * kivi_cache_bytes(params) bytes, 256-byte aligned, and zeroes the arena
+ * asynchronously on `stream`.  *out receives the handle (host memory owned by
+ * the library until kivi_cache_destroy).  Errors: ENULL, EINVAL, EALIGN,
+ * ENOSPC, ECUDA. */
+int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_bytes,
+                      void* cuda_stream, kivi_cache** out);
+
+/* Frees the host handle.  The arena stays the caller's. */
+void kivi_cache_destroy(kivi_cache* cache);
+
+/* Appends n_tokens (>= 1) new tokens to every sequence (KV-cache
+ * quantization guide, steps 1-4; tract #2458 sinks).
+ *   k_new, v_new  device fp16 [B][h_kv][n_tokens][d], contiguous, 16-byte
+ *                 aligned.
+ * Tokens below position S are widened to fp32 sink slots.  A token that
+ * reaches a full ring first pushes the ring's oldest G tokens out as one
+ * frozen group: keys quantized per channel over the G tokens, values per
+ * token, codes packed and (Δ, min) stored as fp16.  The ring then receives
+ * the token.  Bulk appends give the same bytes as token-by-token appends.
+ * Errors: ENULL, EALIGN, EINVAL (n_tokens < 1), ECAPACITY, ECUDA. */
+int kivi_append(kivi_cache* cache, const void* k_new, const void* v_new, int64_t n_tokens,
+                void* cuda_stream);
+
+/* Decode attention over everything appended so far (KV-cache quantization
+ * guide, step 5; tract #2329 GQA and output shape).
+ *   q    device fp16 [B][h_q][d], contiguous, 16-byte aligned.
+ *   out  device fp16 [B][h_q][d], contiguous, 16-byte aligned.
+ * out[b][h] = Σ_t softmax_t(q·k̂_t / sqrt(d)) v̂_t over the visible tokens of
+ * kv head h / (h_q / h_kv): the sinks (fp32), the frozen groups (dequantized
+ * in registers) and the ring (fp16); with a window, the sinks plus the most
+ * recent W tokens.  With T == 0 the output is all zeros.  The work is split
+ * over the sequence (split-K) and merged in the same call; the workspace is
+ * scratch.  Errors: ENULL, EALIGN, ECUDA. */
+int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_stream);
+
+/* Same as kivi_decode_attn with host-resident q and out (pinned host memory
+ * gives asynchronous copies): copies q into the arena's staging area, runs
+ * the decode, copies the result back to out_host, all on `stream`.  The call
+ * returns once the work is queued; synchronise the stream before reading
+ * out_host.  Errors: as kivi_decode_attn. */
+int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host, void* cuda_stream);
+
+/* Forces the number of split-K partitions of later decode calls (0 = the
+ * library's own choice, the default; values above max_splits are clamped).
+ * Errors: ENULL, EINVAL (negative). */
+int kivi_set_num_splits(kivi_cache* cache, int32_t num_splits);
+
+/* Layout, counters and sizes of the handle.  Errors: ENULL. */
+int kivi_cache_layout(const kivi_cache* cache, kivi_layout* out);
+
+/* Algorithmic bytes one decode call must move at the current state: packed
+ * codes of the visible quantized tokens, key (Δ, min) rows of the groups they
+ * touch, value (Δ, min) pairs, fp16 ring tokens, fp32 sinks, q and out.
+ * Returns -1 for a NULL handle. */
+int64_t kivi_decode_bytes(const kivi_cache* cache);
+
+/* Static text for a status code. */
+const char* kivi_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KIVI_H */

@@ -1,0 +1,232 @@
+// append.cu — the write side of the KIVI cache on sm_103a.
+//
+// flush_kernel: one CTA per (new frozen group, kv head, sequence).  It stages
+// the group's G fp16 tokens (keys and values) in shared memory, quantizes
+//   keys   per channel over the G tokens  (KV-cache quantization guide
+//          (pigeon), "How it works", step 1),
+//   values per token over the d channels  (same page, step 2),
+// with q = round((x - min) / Δ), Δ = (max - min) / (2^b - 1) (step 3), and
+// writes the packed codes and fp16 (Δ, min) pairs of the group block.  Once a
+// block is written it never changes (tract #2458: frozen block scales).
+//
+// Bit-exactness: every fp32 operation of the quantizer is an explicit
+// round-to-nearest-even intrinsic (__fsub_rn, __fdiv_rn, __fadd_rn), so the
+// compiler cannot contract or reorder it; fp16 conversion is
+// __float2half_rn; "round" is rintf (half to even).  min and max are
+// canonicalised with + 0.0f so -0 and +0 give the same bytes.
+//
+// write_kernel: widens new sink tokens to fp32 (tract #2458, sink commit) and
+// copies new tokens into the fp16 ring at slot (a - S) mod R (pigeon guide,
+// step 4).  It runs after flush_kernel on the same stream, because a flush can
+// read ring slots that the write then overwrites.
+#include "kivi_internal.cuh"
+
+namespace kivi {
+namespace {
+
+constexpr int kFlushThreads = 256;
+
+// Shared memory: keys [G][d] fp16, values [G][d] fp16, key codes [G][d] u8,
+// value codes [G][d] u8.
+__global__ void __launch_bounds__(kFlushThreads)
+flush_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
+             const __half* __restrict__ v_new, int64_t T_old, int64_t n_new, int64_t g_begin) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int G = g.G, d = g.d, b = g.bits;
+  const int64_t grp = g_begin + blockIdx.x;
+  const int h = blockIdx.y, bb = blockIdx.z;
+  __half* kx = reinterpret_cast<__half*>(smem);
+  __half* vx = kx + G * d;
+  uint8_t* kc = reinterpret_cast<uint8_t*>(vx + G * d);
+  uint8_t* vc = kc + G * d;
+
+  uint8_t* unit = arena + (static_cast<int64_t>(bb) * g.hkv + h) * g.unit_bytes;
+  const int64_t in_off = (static_cast<int64_t>(bb) * g.hkv + h) * n_new * d;
+  const int64_t a0 = g.S + grp * G;
+
+  // stage the group's tokens: 16-byte chunks of each d-wide row
+  const int chunks = d / 8;
+  for (int i = threadIdx.x; i < G * chunks; i += blockDim.x) {
+    const int t = i / chunks, c8 = (i % chunks) * 8;
+    const int64_t a = a0 + t;
+    const __half* ks;
+    const __half* vs;
+    if (a < T_old) {
+      const int64_t slot = (a - g.S) % g.R;
+      ks = reinterpret_cast<const __half*>(unit + g.res_k) + slot * d;
+      vs = reinterpret_cast<const __half*>(unit + g.res_v) + slot * d;
+    } else {
+      ks = k_new + in_off + (a - T_old) * d;
+      vs = v_new + in_off + (a - T_old) * d;
+    }
+    *reinterpret_cast<uint4*>(kx + t * d + c8) = *reinterpret_cast<const uint4*>(ks + c8);
+    *reinterpret_cast<uint4*>(vx + t * d + c8) = *reinterpret_cast<const uint4*>(vs + c8);
+  }
+  __syncthreads();
+
+  const float top = static_cast<float>((1 << b) - 1);
+  uint8_t* blk = unit + g.groups + (grp % g.n_slots) * g.block_bytes;
+  __half* ks_out = reinterpret_cast<__half*>(blk + g.blk_ks);
+  __half* vs_out = reinterpret_cast<__half*>(blk + g.blk_vs);
+
+  // keys: one (Δ, min) per channel over the group's tokens
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float mn = __half2float(kx[c]), mx = mn;
+    for (int t = 1; t < G; ++t) {
+      const float v = __half2float(kx[t * d + c]);
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+    }
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), top));
+    const float dq = __half2float(d16);
+    for (int t = 0; t < G; ++t) {
+      int code = 0;
+      if (dq != 0.0f) {
+        const float r = rintf(__fdiv_rn(__fsub_rn(__half2float(kx[t * d + c]), mn), dq));
+        code = static_cast<int>(fminf(fmaxf(r, 0.0f), top));
+      }
+      kc[t * d + c] = static_cast<uint8_t>(code);
+    }
+    ks_out[c] = d16;
+    ks_out[d + c] = __float2half_rn(mn);
+  }
+
+  // values: one (Δ, min) per token over the channels; one warp per token
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int t = warp; t < G; t += nwarps) {
+    float mn = __half2float(vx[t * d + lane]), mx = mn;
+    for (int c = lane + 32; c < d; c += 32) {
+      const float v = __half2float(vx[t * d + c]);
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), top));
+    const float dq = __half2float(d16);
+    for (int c = lane; c < d; c += 32) {
+      int code = 0;
+      if (dq != 0.0f) {
+        const float r = rintf(__fdiv_rn(__fsub_rn(__half2float(vx[t * d + c]), mn), dq));
+        code = static_cast<int>(fminf(fmaxf(r, 0.0f), top));
+      }
+      vc[t * d + c] = static_cast<uint8_t>(code);
+    }
+    if (lane == 0) {
+      vs_out[2 * t] = d16;
+      vs_out[2 * t + 1] = __float2half_rn(mn);
+    }
+  }
+  __syncthreads();
+
+  // pack: element j of a 32-bit word goes to half (j & 1), bit b * (j >> 1)
+  const int per = 32 / b;
+  uint32_t* kq = reinterpret_cast<uint32_t*>(blk + g.blk_kq);
+  const int kwords = G * (d / per);            // key rows: G tokens x d channels
+  for (int i = threadIdx.x; i < kwords; i += blockDim.x) {
+    const int t = i / (d / per), w = i % (d / per);
+    uint32_t word = 0;
+    for (int j = 0; j < per; ++j)
+      word |= static_cast<uint32_t>(kc[t * d + w * per + j]) << (16 * (j & 1) + b * (j >> 1));
+    kq[i] = word;
+  }
+  uint32_t* vq = reinterpret_cast<uint32_t*>(blk + g.blk_vq);
+  const int vwords = d * (G / per);            // value rows: d channels x G tokens
+  for (int i = threadIdx.x; i < vwords; i += blockDim.x) {
+    const int c = i / (G / per), w = i % (G / per);
+    uint32_t word = 0;
+    for (int j = 0; j < per; ++j)
+      word |= static_cast<uint32_t>(vc[(w * per + j) * d + c]) << (16 * (j & 1) + b * (j >> 1));
+    vq[i] = word;
+  }
+}
+
+// One thread per 8 channels of one token of one unit.
+__global__ void write_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
+                             const __half* __restrict__ v_new, int64_t T_old, int64_t n_new,
+                             int64_t sink_end, int64_t ring_begin) {
+  const int d = g.d, chunks = d / 8;
+  const int64_t n_sink_new = sink_end > T_old ? sink_end - T_old : 0;
+  const int64_t n_ring_new = T_old + n_new - ring_begin;
+  const int64_t per_unit = (n_sink_new + n_ring_new) * chunks;
+  const int64_t total = per_unit * g.B * g.hkv;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t u = i / per_unit, r = i % per_unit;
+    const int64_t k = r / chunks;
+    const int c8 = static_cast<int>(r % chunks) * 8;
+    const int64_t a = (k < n_sink_new) ? T_old + k : ring_begin + (k - n_sink_new);
+    const int64_t src = (u * n_new + (a - T_old)) * d + c8;
+    uint8_t* unit = arena + u * g.unit_bytes;
+    const uint4 kv = *reinterpret_cast<const uint4*>(k_new + src);
+    const uint4 vv = *reinterpret_cast<const uint4*>(v_new + src);
+    if (a < g.S) {
+      const __half2* kh = reinterpret_cast<const __half2*>(&kv);
+      const __half2* vh = reinterpret_cast<const __half2*>(&vv);
+      float* sk = reinterpret_cast<float*>(unit + g.sink_k) + a * d + c8;
+      float* sv = reinterpret_cast<float*>(unit + g.sink_v) + a * d + c8;
+      float2 f[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] = __half22float2(kh[j]);
+      reinterpret_cast<float4*>(sk)[0] = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+      reinterpret_cast<float4*>(sk)[1] = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] = __half22float2(vh[j]);
+      reinterpret_cast<float4*>(sv)[0] = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+      reinterpret_cast<float4*>(sv)[1] = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+    } else {
+      const int64_t slot = (a - g.S) % g.R;
+      *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(unit + g.res_k) + slot * d + c8) = kv;
+      *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(unit + g.res_v) + slot * d + c8) = vv;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
+                         int64_t T_old, int64_t n_new, int64_t g_begin, int64_t g_end,
+                         cudaStream_t stream) {
+  if (g_end <= g_begin) return cudaSuccess;
+  const size_t smem = static_cast<size_t>(g.G) * g.d * (2 * sizeof(__half) + 2);
+  cudaError_t e = cudaFuncSetAttribute(flush_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int64_t left = g_end - g_begin;
+  int64_t start = g_begin;
+  while (left > 0) {   // grid.x is limited to 2^31-1; chunk for safety
+    const int64_t n = left < 65535 * 256 ? left : 65535 * 256;
+    dim3 grid(static_cast<unsigned>(n), g.hkv, g.B);
+    flush_kernel<<<grid, kFlushThreads, smem, stream>>>(g, arena, k_new, v_new, T_old, n_new, start);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    start += n;
+    left -= n;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
+                         int64_t T_old, int64_t n_new, int64_t ring_begin, cudaStream_t stream) {
+  const int64_t T_new = T_old + n_new;
+  const int64_t sink_end = T_new < g.S ? T_new : g.S;
+  const int64_t n_sink_new = sink_end > T_old ? sink_end - T_old : 0;
+  const int64_t n_ring_new = T_new - ring_begin;
+  const int64_t total = (n_sink_new + n_ring_new) * (g.d / 8) * g.B * g.hkv;
+  if (total <= 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(g, arena, k_new, v_new, T_old, n_new,
+                                                                       sink_end, ring_begin);
+  return cudaGetLastError();
+}
+
+}  // namespace kivi

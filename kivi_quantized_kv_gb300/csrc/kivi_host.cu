@@ -1,0 +1,279 @@
+// kivi_host.cu — the C ABI of libkivi.so (declared in include/kivi.h).
+//
+// Host-side work only: parameter checks, the arena layout, the token counters
+// (the cache state is a pure function of the token count T), the choice of
+// split-K partitions, and kernel launches.  No device memory is allocated,
+// freed or synchronised here.
+#include "kivi_internal.cuh"
+
+#include <new>
+
+struct kivi_cache {
+  kivi_params p;
+  kivi::Geo g;
+  uint8_t* arena;
+  size_t arena_bytes;
+  int64_t T;
+  int32_t forced_splits;
+  int32_t num_sms;
+};
+
+namespace {
+
+using kivi::Geo;
+using kivi::State;
+
+constexpr int64_t kAlign = 256;
+constexpr int kMaxRep = 8;
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int validate(const kivi_params* p) {
+  if (!p) return KIVI_ENULL;
+  if (!(p->bits == 2 || p->bits == 4 || p->bits == 8)) return KIVI_EINVAL;
+  if (!(p->head_dim == 64 || p->head_dim == 128)) return KIVI_EINVAL;
+  if (p->group < 16 || p->group > 256 || p->group % 16 != 0) return KIVI_EINVAL;
+  if (p->residual < p->group || p->residual % p->group != 0) return KIVI_EINVAL;
+  if (p->residual > (1 << 20)) return KIVI_EINVAL;
+  if (p->sinks < 0 || p->sinks > 1024) return KIVI_EINVAL;
+  if (p->h_kv < 1 || p->h_q < 1 || p->h_q % p->h_kv != 0) return KIVI_EINVAL;
+  if (p->h_q / p->h_kv > kMaxRep) return KIVI_EINVAL;
+  if (p->batch < 1 || p->h_kv > 65535 || p->batch > 65535) return KIVI_EINVAL;
+  if (p->window < 0 || p->max_tokens < 0) return KIVI_EINVAL;
+  if (p->window > 0 && p->window < p->residual) return KIVI_EINVAL;
+  return KIVI_OK;
+}
+
+// Split-K partitions the workspace is sized for: enough (sequence, kv head,
+// split) work items to fill the GPU several times over when B * h_kv is
+// small; one split per unit when the batch alone fills it.
+int32_t max_splits_for(const kivi_params& p) {
+  const int64_t units = static_cast<int64_t>(p.batch) * p.h_kv;
+  int64_t s = (4096 + units - 1) / units;
+  if (s < 1) s = 1;
+  if (s > 256) s = 256;
+  return static_cast<int32_t>(s);
+}
+
+Geo geometry(const kivi_params& p) {
+  Geo g{};
+  g.bits = p.bits; g.G = p.group; g.R = p.residual; g.S = p.sinks;
+  g.hq = p.h_q; g.hkv = p.h_kv; g.d = p.head_dim; g.B = p.batch; g.rep = p.h_q / p.h_kv;
+  g.window = p.window;
+  const int64_t d = p.head_dim, G = p.group, b = p.bits;
+  if (p.window > 0) {
+    g.n_slots = (p.window + G - 1) / G + 1;
+  } else {
+    g.n_slots = kivi::state_at(g, p.max_tokens).n_groups;
+  }
+  g.sink_k = 0;
+  g.sink_v = g.sink_k + p.sinks * d * 4;
+  g.res_k = g.sink_v + p.sinks * d * 4;
+  g.res_v = g.res_k + p.residual * d * 2;
+  g.groups = g.res_v + p.residual * d * 2;
+  g.blk_kq = 0;
+  g.blk_ks = g.blk_kq + G * d * b / 8;
+  g.blk_vq = g.blk_ks + 2 * d * 2;
+  g.blk_vs = g.blk_vq + d * G * b / 8;
+  g.block_bytes = g.blk_vs + G * 2 * 2;
+  g.unit_bytes = g.groups + g.n_slots * g.block_bytes;
+  g.cache_bytes = static_cast<int64_t>(p.batch) * p.h_kv * g.unit_bytes;
+  g.max_splits = max_splits_for(p);
+  const int64_t bhq = static_cast<int64_t>(p.batch) * p.h_q;
+  g.ws_partials = round_up(g.cache_bytes, kAlign);
+  g.ws_counters = round_up(g.ws_partials + bhq * g.max_splits * (d + 2) * 4, kAlign);
+  g.ws_q = round_up(g.ws_counters + static_cast<int64_t>(p.batch) * p.h_kv * 4, kAlign);
+  g.ws_out = round_up(g.ws_q + bhq * d * 2, kAlign);
+  return g;
+}
+
+int64_t arena_bytes_of(const Geo& g) {
+  return round_up(g.ws_out + static_cast<int64_t>(g.B) * g.hq * g.d * 2, kAlign);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ECUDA; }
+
+// First frozen group that can hold a visible token, and the plan of splits.
+kivi::DecodePlan plan_for(const kivi_cache& c) {
+  kivi::DecodePlan pl{};
+  pl.st = kivi::state_at(c.g, c.T);
+  int64_t first = pl.st.n_groups - c.g.n_slots;
+  if (first < 0) first = 0;
+  if (c.g.window > 0) {
+    const int64_t lo = c.T - c.g.window;                 // first visible position
+    if (lo > c.g.S) {
+      const int64_t gl = (lo - c.g.S) / c.g.G;            // group holding position lo
+      if (gl > first) first = gl;
+    }
+  }
+  if (first > pl.st.n_groups) first = pl.st.n_groups;
+  pl.g_first = first;
+  pl.n_vis_groups = pl.st.n_groups - first;
+  int64_t splits;
+  if (c.forced_splits > 0) {
+    splits = c.forced_splits;
+  } else {
+    const int64_t units = static_cast<int64_t>(c.g.B) * c.g.hkv;
+    const int64_t target = static_cast<int64_t>(c.num_sms) * 8;   // work items in flight
+    splits = (target + units - 1) / units;
+    // at least a few groups per split, so the partials stay a small overhead
+    const int64_t by_work = (pl.n_vis_groups + 3) / 4;
+    if (splits > by_work) splits = by_work;
+  }
+  if (splits > c.g.max_splits) splits = c.g.max_splits;
+  if (splits > pl.n_vis_groups) splits = pl.n_vis_groups;
+  if (splits < 1) splits = 1;
+  int64_t gps = (pl.n_vis_groups + splits - 1) / splits;
+  if (gps < 1) gps = 1;
+  splits = pl.n_vis_groups > 0 ? (pl.n_vis_groups + gps - 1) / gps : 1;
+  pl.splits = static_cast<int32_t>(splits);
+  pl.groups_per_split = static_cast<int32_t>(gps);
+  return pl;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kivi_cache_bytes(const kivi_params* params) {
+  if (validate(params) != KIVI_OK) return 0;
+  return static_cast<size_t>(arena_bytes_of(geometry(*params)));
+}
+
+int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_bytes, void* cuda_stream,
+                      kivi_cache** out) {
+  if (!out || !d_arena) return KIVI_ENULL;
+  const int v = validate(params);
+  if (v != KIVI_OK) return v;
+  if (!aligned(d_arena, kAlign)) return KIVI_EALIGN;
+  const Geo g = geometry(*params);
+  if (static_cast<int64_t>(arena_bytes) < arena_bytes_of(g)) return KIVI_ENOSPC;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KIVI_ECUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KIVI_ECUDA;
+  kivi_cache* c = new (std::nothrow) kivi_cache();
+  if (!c) return KIVI_ENULL;
+  c->p = *params;
+  c->g = g;
+  c->arena = static_cast<uint8_t*>(d_arena);
+  c->arena_bytes = arena_bytes;
+  c->T = 0;
+  c->forced_splits = 0;
+  c->num_sms = sms > 0 ? sms : 1;
+  const cudaError_t e = cudaMemsetAsync(d_arena, 0, static_cast<size_t>(arena_bytes_of(g)),
+                                        static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) { delete c; return KIVI_ECUDA; }
+  *out = c;
+  return KIVI_OK;
+}
+
+void kivi_cache_destroy(kivi_cache* cache) { delete cache; }
+
+int kivi_append(kivi_cache* c, const void* k_new, const void* v_new, int64_t n, void* cuda_stream) {
+  if (!c || !k_new || !v_new) return KIVI_ENULL;
+  if (n < 1) return KIVI_EINVAL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return KIVI_EALIGN;
+  const Geo& g = c->g;
+  const int64_t T_old = c->T, T_new = c->T + n;
+  if (g.window == 0 && T_new > c->p.max_tokens) return KIVI_ECAPACITY;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const State s0 = kivi::state_at(g, T_old), s1 = kivi::state_at(g, T_new);
+  // groups created by this append; with a window only the last n_slots survive
+  int64_t g_begin = s0.n_groups;
+  if (s1.n_groups - g.n_slots > g_begin) g_begin = s1.n_groups - g.n_slots;
+  const auto* kh = static_cast<const __half*>(k_new);
+  const auto* vh = static_cast<const __half*>(v_new);
+  cudaError_t e = kivi::launch_flush(g, c->arena, kh, vh, T_old, n, g_begin, s1.n_groups, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  // the ring keeps the last R tokens of the stream (flushed or not)
+  int64_t ring_begin = T_old;
+  if (ring_begin < g.S) ring_begin = g.S;
+  if (T_new - g.R > ring_begin) ring_begin = T_new - g.R;
+  if (ring_begin > T_new) ring_begin = T_new;
+  e = kivi::launch_write(g, c->arena, kh, vh, T_old, n, ring_begin, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  c->T = T_new;
+  return KIVI_OK;
+}
+
+int kivi_decode_attn(kivi_cache* c, const void* q, void* out, void* cuda_stream) {
+  if (!c || !q || !out) return KIVI_ENULL;
+  if (!aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
+  const kivi::DecodePlan pl = plan_for(*c);
+  return cuda_status(kivi::launch_decode(c->g, c->arena, static_cast<const __half*>(q),
+                                         static_cast<__half*>(out), pl, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int kivi_decode_attn_host(kivi_cache* c, const void* q_host, void* out_host, void* cuda_stream) {
+  if (!c || !q_host || !out_host) return KIVI_ENULL;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const size_t bytes = static_cast<size_t>(c->g.B) * c->g.hq * c->g.d * 2;
+  void* dq = c->arena + c->g.ws_q;
+  void* dout = c->arena + c->g.ws_out;
+  cudaError_t e = cudaMemcpyAsync(dq, q_host, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return KIVI_ECUDA;
+  const int st = kivi_decode_attn(c, dq, dout, cuda_stream);
+  if (st != KIVI_OK) return st;
+  e = cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, s);
+  return cuda_status(e);
+}
+
+int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {
+  if (!c) return KIVI_ENULL;
+  if (num_splits < 0) return KIVI_EINVAL;
+  c->forced_splits = num_splits;
+  return KIVI_OK;
+}
+
+int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
+  if (!c || !out) return KIVI_ENULL;
+  const Geo& g = c->g;
+  const State st = kivi::state_at(g, c->T);
+  kivi_layout L{};
+  L.n_slots = g.n_slots;
+  L.sink_k = g.sink_k; L.sink_v = g.sink_v; L.res_k = g.res_k; L.res_v = g.res_v; L.groups = g.groups;
+  L.block_bytes = g.block_bytes; L.blk_kq = g.blk_kq; L.blk_ks = g.blk_ks; L.blk_vq = g.blk_vq; L.blk_vs = g.blk_vs;
+  L.unit_bytes = g.unit_bytes; L.cache_bytes = g.cache_bytes;
+  L.workspace_offset = g.ws_partials;
+  L.arena_bytes = arena_bytes_of(g);
+  L.workspace_bytes = L.arena_bytes - g.ws_partials;
+  L.tokens = c->T; L.n_sink = st.n_sink; L.n_groups = st.n_groups; L.n_res = st.n_res;
+  L.max_splits = g.max_splits;
+  *out = L;
+  return KIVI_OK;
+}
+
+int64_t kivi_decode_bytes(const kivi_cache* c) {
+  if (!c) return -1;
+  const Geo& g = c->g;
+  const kivi::DecodePlan pl = plan_for(*c);
+  const int64_t T = c->T, d = g.d;
+  const int64_t lo = g.window > 0 ? T - g.window : 0;
+  int64_t tq = 0, touched = 0;
+  for (int64_t grp = pl.g_first; grp < pl.st.n_groups; ++grp) {
+    const int64_t a0 = g.S + grp * g.G, a1 = a0 + g.G;
+    const int64_t start = a0 > lo ? a0 : lo;
+    const int64_t vis = a1 - start;
+    if (vis > 0) { tq += vis; touched += 1; }
+  }
+  const int64_t per_unit = 2 * tq * d * g.bits / 8 + 4 * d * touched + 4 * tq + 4 * d * pl.st.n_res +
+                           8 * d * pl.st.n_sink;
+  return per_unit * g.B * g.hkv + 4 * d * static_cast<int64_t>(g.B) * g.hq;
+}
+
+const char* kivi_status_string(int status) {
+  switch (status) {
+    case KIVI_OK: return "ok";
+    case KIVI_EINVAL: return "invalid parameter";
+    case KIVI_EALIGN: return "pointer not aligned (arena: 256 bytes; tensors: 16 bytes)";
+    case KIVI_ECAPACITY: return "append would exceed max_tokens";
+    case KIVI_ENOSPC: return "arena smaller than kivi_cache_bytes()";
+    case KIVI_ECUDA: return "CUDA launch or copy failed";
+    case KIVI_ENULL: return "NULL pointer";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every entry
+point include/kivi.h declares, sizes arenas, and rejects bad arguments on the
+host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def abi():
+    from kivi_quantized_kv_gb300.build import build
+    build()
+    from kivi_quantized_kv_gb300 import _abi
+    _abi.lib()
+    return _abi
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "kivi.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(kivi_\w+)\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(abi):
+    names = header_functions()
+    assert len(names) >= 10, names
+    lib = ctypes.CDLL(abi.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(abi.EXPORTS) == names
+
+
+def params(**kw):
+    from kivi_quantized_kv_gb300 import KiviConfig
+    base = dict(bits=4, group=32, residual=32, sinks=4, h_q=4, h_kv=4, head_dim=64, batch=1, max_tokens=256)
+    base.update(kw)
+    return KiviConfig(**base)
+
+
+def test_cache_bytes_covers_the_oracle_layout(abi, oracle_lib):
+    from kivi_quantized_kv_gb300 import cache_bytes
+    for kw in (dict(), dict(bits=2, head_dim=128, batch=8, h_q=32, h_kv=32, max_tokens=4096),
+               dict(bits=8, group=64, residual=64, window=4096, max_tokens=0, h_q=32, h_kv=8, batch=32,
+                    head_dim=128)):
+        cfg = params(**kw)
+        lay = oracle_lib.layout(oracle_lib.Params(**cfg.__dict__))
+        nb = cache_bytes(cfg)
+        assert nb >= lay["cache_bytes"]
+        # the workspace is small next to the cache: partials, counters, staging
+        assert nb - lay["cache_bytes"] <= 8 * 1024 * 1024 + lay["cache_bytes"] // 100
+
+
+@pytest.mark.parametrize("kw", [dict(bits=3), dict(bits=16), dict(head_dim=96), dict(group=8), dict(group=40),
+                                dict(residual=16), dict(residual=48), dict(sinks=-1), dict(h_q=6),
+                                dict(h_q=36, h_kv=4), dict(window=16, max_tokens=0), dict(window=-1),
+                                dict(batch=0), dict(max_tokens=-1)])
+def test_invalid_parameters_are_rejected(abi, kw):
+    from kivi_quantized_kv_gb300 import cache_bytes
+    cfg = params(**kw)
+    assert cache_bytes(cfg) == 0
+    p = cfg.c()
+    h = ctypes.c_void_p()
+    buf = ctypes.create_string_buffer(1 << 16)
+    st = abi.lib().kivi_cache_create(ctypes.byref(p), ctypes.c_void_p(ctypes.addressof(buf)), 1 << 16, None,
+                                     ctypes.byref(h))
+    assert st == abi.KIVI_EINVAL
+
+
+def test_host_side_errors_before_any_device_call(abi):
+    L = abi.lib()
+    p = params().c()
+    need = L.kivi_cache_bytes(ctypes.byref(p))
+    h = ctypes.c_void_p()
+    assert L.kivi_cache_create(ctypes.byref(p), None, need, None, ctypes.byref(h)) == abi.KIVI_ENULL
+    assert L.kivi_cache_create(None, ctypes.c_void_p(4096), need, None, ctypes.byref(h)) == abi.KIVI_ENULL
+    assert L.kivi_cache_create(ctypes.byref(p), ctypes.c_void_p(4096 + 16), need, None,
+                               ctypes.byref(h)) == abi.KIVI_EALIGN
+    assert L.kivi_cache_create(ctypes.byref(p), ctypes.c_void_p(4096), need - 1, None,
+                               ctypes.byref(h)) == abi.KIVI_ENOSPC
+    assert L.kivi_append(None, None, None, 1, None) == abi.KIVI_ENULL
+    assert L.kivi_decode_attn(None, None, None, None) == abi.KIVI_ENULL
+    assert L.kivi_decode_attn_host(None, None, None, None) == abi.KIVI_ENULL
+    assert L.kivi_set_num_splits(None, 2) == abi.KIVI_ENULL
+    assert L.kivi_cache_layout(None, None) == abi.KIVI_ENULL
+    assert L.kivi_decode_bytes(None) == -1
+    for s in range(7):
+        assert abi.status_string(s)
+    assert abi.status_string(99) == "unknown status"
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch):
+    from kivi_quantized_kv_gb300 import _abi
+    monkeypatch.setattr(_abi, "_lib", None)
+    monkeypatch.setattr(_abi, "LIB_PATH", "/nonexistent/libkivi.so")
+    with pytest.raises(ImportError):
+        _abi.lib()

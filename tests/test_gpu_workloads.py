@@ -1,0 +1,82 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times (automatic split count).
+
+The CUDA cache is filled with the whole workload (every sequence and kv
+head) from the seeded generator on the GPU.  The oracle cannot afford every
+unit, so it rebuilds a few sampled (sequence, kv head) units from the same
+input chunks: units never interact, so each sampled unit's bytes and its
+query heads' attention rows must match exactly / within 2e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
+from kivi_quantized_kv_gb300.synth import KVStream, WORKLOADS, queries, sweep_workload
+from gpu_util import TOL, oparams, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as ge
+    ge.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_sampled(w, units, chunk=2048, layer=0):
+    dev = torch.device("cuda")
+    cfg = KiviConfig.from_workload(w)
+    cache = KiviCache(cfg, device=dev)
+    stream = KVStream(w, layer=layer, device=dev)
+    ks = {u: [] for u in units}
+    vs = {u: [] for u in units}
+    t = 0
+    while t < w.tokens:
+        n = min(chunk, w.tokens - t)
+        k, v = stream.next(n)
+        cache.append(k, v)
+        for (b, h) in units:
+            ks[(b, h)].append(k[b, h].cpu())
+            vs[(b, h)].append(v[b, h].cpu())
+        t += n
+    q = queries(w, layer=layer, device=dev)
+    out = cache.decode(q).float().cpu().numpy()
+    torch.cuda.synchronize()
+    arena = cache.cache_region()
+    L = cache.layout()
+    rep = w.h_q // w.h_kv
+    worst = 0.0
+    for (b, h) in units:
+        p1 = oparams(cfg, batch=1, h_kv=1, h_q=rep)
+        ref = oracle.Cache(p1)
+        kk = torch.cat(ks[(b, h)], dim=0)[None, None].numpy()
+        vv = torch.cat(vs[(b, h)], dim=0)[None, None].numpy()
+        assert ref.append(kk, vv) == 0
+        u = b * w.h_kv + h
+        got = arena[u * L["unit_bytes"]:(u + 1) * L["unit_bytes"]].cpu().numpy()
+        assert np.array_equal(got, ref.arena()), (w.name, b, h)
+        qq = q[b, h * rep:(h + 1) * rep].cpu()[None].numpy()
+        exp = ref.decode_attn(qq)
+        err = row_rel_err(out[b, h * rep:(h + 1) * rep][None], exp)
+        assert err <= TOL, (w.name, b, h, err)
+        worst = max(worst, err)
+    return worst
+
+
+@pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa8b_b4", "gqa8b_b2", "swa_mistral"])
+def test_workload_full_size_sampled_units(name):
+    w = WORKLOADS[name]
+    units = sorted({(0, 0), (w.batch - 1, w.h_kv - 1), (w.batch // 2, w.h_kv // 2)})
+    err = run_sampled(w, units)
+    print(f"{name}: worst row error {err:.2e}")
+
+
+@pytest.mark.parametrize("batch,tokens,bits,layer", [(16, 16384, 4, 0), (1, 131072, 2, 31), (128, 1024, 8, 5)])
+def test_sweep_cells_sampled(batch, tokens, bits, layer):
+    w = sweep_workload(batch, tokens, bits)
+    units = sorted({(0, 0), (batch - 1, 7), (batch // 2, 3)})
+    run_sampled(w, units, chunk=4096, layer=layer)
