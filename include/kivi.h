@@ -51,7 +51,8 @@ typedef enum kivi_status {
   KIVI_ECAPACITY = 3,  /* T + n would exceed max_tokens (window == 0) */
   KIVI_ENOSPC = 4,     /* the arena is smaller than kivi_cache_bytes() */
   KIVI_ECUDA = 5,      /* a CUDA launch or copy reported an error */
-  KIVI_ENULL = 6       /* a required pointer is NULL */
+  KIVI_ENULL = 6,      /* a required pointer is NULL */
+  KIVI_ESCRATCH = 7    /* too large for the fixed scratch of kivi_decode_attn_noalloc */
 } kivi_status;
 
 /* Cache parameters.
@@ -160,6 +161,28 @@ int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_str
  * returns once the work is queued; synchronise the stream before reading
  * out_host.  Errors: as kivi_decode_attn. */
 int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host, void* cuda_stream);
+
+/* Decode attention that allocates nothing (the method's pages have no
+ * counterpart: this is a deployment variant of kivi_decode_attn).  For callers
+ * that can pass only their inputs and outputs and cannot obtain device memory
+ * while decoding, for instance a plugin inside a host runtime that owns all
+ * device memory and forbids allocation during execution.  Same arguments,
+ * layouts and result as kivi_decode_attn (within its rounding: the split
+ * count may be lower); the split-K scratch is a fixed 4 MiB device array
+ * inside the library instead of the arena workspace.  It calls no cudaMalloc
+ * or cudaFree.
+ *   - Every GPU that loads the library holds the 4 MiB until process exit;
+ *     the CUDA driver materialises it when it loads the library's device
+ *     variables (with lazy module loading, at the latest on the first call).
+ *   - The first call on a device looks up the array's device address on the
+ *     current device; make that first call before any stream capture.
+ *   - All calls share the array: calls whose GPU work overlaps (concurrent
+ *     streams or host threads) race on it.  The merge counters in it are
+ *     cleared by every call.
+ *   - B * h_q * (head_dim + 2) * 4 bytes (one split's partial results) plus
+ *     the counters must fit in 4 MiB, else KIVI_ESCRATCH and nothing runs.
+ * Errors: ENULL, EALIGN, ESCRATCH, ECUDA. */
+int kivi_decode_attn_noalloc(kivi_cache* cache, const void* q, void* out, void* cuda_stream);
 
 /* Forces the number of split-K partitions of later decode calls (0 = the
  * library's own choice, the default; values above max_splits are clamped).

@@ -11,12 +11,12 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkivi.so")
 
-KIVI_OK, KIVI_EINVAL, KIVI_EALIGN, KIVI_ECAPACITY, KIVI_ENOSPC, KIVI_ECUDA, KIVI_ENULL = range(7)
+KIVI_OK, KIVI_EINVAL, KIVI_EALIGN, KIVI_ECAPACITY, KIVI_ENOSPC, KIVI_ECUDA, KIVI_ENULL, KIVI_ESCRATCH = range(8)
 
 # every entry point include/kivi.h declares
 EXPORTS = (
     "kivi_cache_bytes", "kivi_cache_create", "kivi_cache_destroy", "kivi_append",
-    "kivi_decode_attn", "kivi_decode_attn_host", "kivi_set_num_splits", "kivi_cache_layout",
+    "kivi_decode_attn", "kivi_decode_attn_host", "kivi_decode_attn_noalloc", "kivi_set_num_splits", "kivi_cache_layout",
     "kivi_decode_bytes", "kivi_status_string",
 )
 
@@ -65,6 +65,7 @@ def lib():
         "kivi_append": (ctypes.c_int, [vp, vp, vp, i64, vp]),
         "kivi_decode_attn": (ctypes.c_int, [vp, vp, vp, vp]),
         "kivi_decode_attn_host": (ctypes.c_int, [vp, vp, vp, vp]),
+        "kivi_decode_attn_noalloc": (ctypes.c_int, [vp, vp, vp, vp]),
         "kivi_set_num_splits": (ctypes.c_int, [vp, i32]),
         "kivi_cache_layout": (ctypes.c_int, [vp, P(KiviLayout)]),
         "kivi_decode_bytes": (i64, [vp]),

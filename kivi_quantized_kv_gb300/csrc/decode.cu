@@ -54,8 +54,8 @@ struct WarpSmem {
 
 template <int D, int BITS>
 __global__ void __launch_bounds__(kWarps * 32)
-decode_v0_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ q,
-                 DecodePlan plan) {
+decode_v0_kernel(Geo g, const uint8_t* __restrict__ arena, const __half* __restrict__ q,
+                 float* __restrict__ part, DecodePlan plan) {
   constexpr int NC = D / 32;            // channels per lane
   constexpr int PER = 32 / BITS;        // codes per 32-bit word
   __shared__ float qs[kMaxRep][D];      // q (log2 e / sqrt(d) folded)
@@ -226,7 +226,6 @@ decode_v0_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ 
     for (int j = 0; j < NC; ++j) red_o[warp][r][lane + 32 * j] = o[r][j] + mnt;
   }
   __syncthreads();
-  float* part = reinterpret_cast<float*>(arena + g.ws_partials);
   for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
     const int r = i / D, c = i % D;
     float M = -INFINITY;
@@ -249,10 +248,9 @@ decode_v0_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ 
 // Combines the splits of one (sequence, query head): M = max m_i,
 // L = Σ l_i 2^(m_i - M), out = Σ o_i 2^(m_i - M) / L (m in log2 units).
 template <int D>
-__global__ void merge_kernel(Geo g, const uint8_t* __restrict__ arena, __half* __restrict__ out, int splits) {
+__global__ void merge_kernel(Geo g, const float* __restrict__ partials, __half* __restrict__ out, int splits) {
   const int hq = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-  const float* part = reinterpret_cast<const float*>(arena + g.ws_partials) +
-                      (static_cast<int64_t>(b) * g.hq + hq) * g.max_splits * (D + 2);
+  const float* part = partials + (static_cast<int64_t>(b) * g.hq + hq) * g.max_splits * (D + 2);
   float M = -INFINITY;
   for (int s = 0; s < splits; ++s) M = fmaxf(M, part[s * (D + 2) + D]);
   float L = 0.f, O = 0.f;
@@ -269,29 +267,37 @@ __global__ void merge_kernel(Geo g, const uint8_t* __restrict__ arena, __half* _
 }
 
 template <int D, int BITS>
-cudaError_t launch_v0(const Geo& g, uint8_t* arena, const __half* q, __half* out, const DecodePlan& plan,
-                      cudaStream_t stream) {
+cudaError_t launch_v0(const Geo& g, const uint8_t* arena, const __half* q, __half* out, const DecodePlan& plan,
+                      float* partials, cudaStream_t stream) {
   dim3 grid(plan.splits, g.hkv, g.B);
-  decode_v0_kernel<D, BITS><<<grid, kWarps * 32, 0, stream>>>(g, arena, q, plan);
+  decode_v0_kernel<D, BITS><<<grid, kWarps * 32, 0, stream>>>(g, arena, q, partials, plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  merge_kernel<D><<<dim3(g.hq, g.B), D, 0, stream>>>(g, arena, out, plan.splits);
+  merge_kernel<D><<<dim3(g.hq, g.B), D, 0, stream>>>(g, partials, out, plan.splits);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,
-                          const DecodePlan& plan, cudaStream_t stream) {
+cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
+                                  const DecodePlan& plan, float* partials, unsigned* counters,
+                                  cudaStream_t stream) {
+  (void)counters;   // the separate merge pass needs no counters
   if (g.rep > kMaxRep) return cudaErrorInvalidValue;
   if (g.d == 64) {
-    if (g.bits == 2) return launch_v0<64, 2>(g, arena, q, out, plan, stream);
-    if (g.bits == 4) return launch_v0<64, 4>(g, arena, q, out, plan, stream);
-    return launch_v0<64, 8>(g, arena, q, out, plan, stream);
+    if (g.bits == 2) return launch_v0<64, 2>(g, arena, q, out, plan, partials, stream);
+    if (g.bits == 4) return launch_v0<64, 4>(g, arena, q, out, plan, partials, stream);
+    return launch_v0<64, 8>(g, arena, q, out, plan, partials, stream);
   }
-  if (g.bits == 2) return launch_v0<128, 2>(g, arena, q, out, plan, stream);
-  if (g.bits == 4) return launch_v0<128, 4>(g, arena, q, out, plan, stream);
-  return launch_v0<128, 8>(g, arena, q, out, plan, stream);
+  if (g.bits == 2) return launch_v0<128, 2>(g, arena, q, out, plan, partials, stream);
+  if (g.bits == 4) return launch_v0<128, 4>(g, arena, q, out, plan, partials, stream);
+  return launch_v0<128, 8>(g, arena, q, out, plan, partials, stream);
+}
+
+cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,
+                          const DecodePlan& plan, cudaStream_t stream) {
+  return launch_decode_scratch(g, arena, q, out, plan, reinterpret_cast<float*>(arena + g.ws_partials),
+                               reinterpret_cast<unsigned*>(arena + g.ws_counters), stream);
 }
 
 }  // namespace kivi

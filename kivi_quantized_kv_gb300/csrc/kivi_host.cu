@@ -6,6 +6,7 @@
 // freed or synchronised here.
 #include "kivi_internal.cuh"
 
+#include <mutex>
 #include <new>
 
 struct kivi_cache {
@@ -220,6 +221,80 @@ int kivi_decode_attn_host(kivi_cache* c, const void* q_host, void* out_host, voi
   return cuda_status(e);
 }
 
+// ---------------------------------------------------------------------------
+// Decode without any device allocation by anyone: the split-K scratch lives in
+// a fixed, library-owned device array instead of the caller's arena
+// workspace.  For callers that hand this library only their input and output
+// buffers and cannot obtain more device memory while decoding, e.g. a plugin
+// running inside a host runtime that owns all device memory and forbids
+// allocation during execution, or a latency-critical loop where cudaMalloc's
+// implicit device synchronisation is unacceptable.
+//
+// The array is a module-scope __device__ variable: every GPU that loads this
+// library holds kNoAllocScratchBytes of it until the process exits (the CUDA
+// driver materialises it when it loads the variable, which with lazy module
+// loading happens at the latest on the first call on that device).  In host
+// code the symbol is only a host-side stand-in, never a device address, so its
+// device address is looked up once per device with cudaGetSymbolAddress, with
+// that device current, on the first call made on that device (make that first
+// call before any stream capture).  All calls share the array and it keeps the
+// previous call's contents: the merge counters are cleared on every call, and
+// calls whose work overlaps on the GPU (other streams, other host threads)
+// race on it.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KIVI_ECUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return KIVI_EINVAL;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return KIVI_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KIVI_OK;
+}
+
+}  // namespace
+
+int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda_stream) {
+  if (!c || !q || !out) return KIVI_ENULL;
+  if (!aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
+  // scratch: [counters, one word per (sequence, kv head)][partials]
+  const int64_t counter_bytes = round_up(static_cast<int64_t>(c->g.B) * c->g.hkv * 4, kAlign);
+  const int64_t record = static_cast<int64_t>(c->g.B) * c->g.hq * (c->g.d + 2) * 4;   // one split
+  const int64_t fit = (static_cast<int64_t>(kNoAllocScratchBytes) - counter_bytes) / record;
+  if (fit < 1) return KIVI_ESCRATCH;
+  kivi::DecodePlan pl = plan_for(*c);
+  if (pl.splits > fit) {
+    const int64_t gps = (pl.n_vis_groups + fit - 1) / fit;
+    pl.groups_per_split = static_cast<int32_t>(gps);
+    pl.splits = static_cast<int32_t>((pl.n_vis_groups + gps - 1) / gps);
+  }
+  Geo g = c->g;
+  g.max_splits = pl.splits;   // partial records are strided by this split count
+  void* base = nullptr;
+  const int st = noalloc_scratch(&base);
+  if (st != KIVI_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  unsigned* counters = static_cast<unsigned*>(base);
+  float* partials = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + counter_bytes);
+  if (cudaMemsetAsync(counters, 0, static_cast<size_t>(counter_bytes), s) != cudaSuccess) return KIVI_ECUDA;
+  return cuda_status(kivi::launch_decode_scratch(g, c->arena, static_cast<const __half*>(q),
+                                                 static_cast<__half*>(out), pl, partials, counters, s));
+}
+
 int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {
   if (!c) return KIVI_ENULL;
   if (num_splits < 0) return KIVI_EINVAL;
@@ -272,6 +347,7 @@ const char* kivi_status_string(int status) {
     case KIVI_ENOSPC: return "arena smaller than kivi_cache_bytes()";
     case KIVI_ECUDA: return "CUDA launch or copy failed";
     case KIVI_ENULL: return "NULL pointer";
+    case KIVI_ESCRATCH: return "problem too large for the library's fixed no-allocation scratch (4 MiB)";
     default: return "unknown status";
   }
 }

@@ -59,7 +59,13 @@ struct DecodePlan {
   int32_t groups_per_split;
 };
 
+// Decode with the arena's own workspace for the split-K partials.
 cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,
                           const DecodePlan& plan, cudaStream_t stream);
+// Decode with caller-chosen scratch: `partials` holds B * h_q * max_splits
+// records of (d + 2) floats, `counters` one word per (sequence, kv head).
+cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
+                                  const DecodePlan& plan, float* partials, unsigned* counters,
+                                  cudaStream_t stream);
 
 }  // namespace kivi
