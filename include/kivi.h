@@ -109,7 +109,7 @@ typedef struct kivi_layout {
   int64_t n_sink;     /* min(T, S) */
   int64_t n_groups;   /* frozen groups written so far */
   int64_t n_res;      /* tokens live in the ring */
-  int32_t max_splits; /* split-K partitions the workspace holds per head */
+  int32_t max_splits; /* CTAs that may share one unit's work */
   int32_t reserved;
 } kivi_layout;
 
@@ -179,13 +179,15 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  *   - All calls share the array: calls whose GPU work overlaps (concurrent
  *     streams or host threads) race on it.  The merge counters in it are
  *     cleared by every call.
- *   - B * h_q * (head_dim + 2) * 4 bytes (one split's partial results) plus
- *     the counters must fit in 4 MiB, else KIVI_ESCRATCH and nothing runs.
+ *   - Three partial records per query head, 3 * B * h_q * (head_dim + 2) * 4
+ *     bytes, plus the merge counters must fit in 4 MiB, else KIVI_ESCRATCH and
+ *     nothing runs; the work is spread over fewer CTAs when fewer records fit.
  * Errors: ENULL, EALIGN, ESCRATCH, ECUDA. */
 int kivi_decode_attn_noalloc(kivi_cache* cache, const void* q, void* out, void* cuda_stream);
 
-/* Forces the number of split-K partitions of later decode calls (0 = the
- * library's own choice, the default; values above max_splits are clamped).
+/* Forces the number of CTAs per (sequence, kv head) unit that later decode
+ * calls spread the work over (0 = the library's own choice: one wave of
+ * resident CTAs; larger values are clamped to what the workspace holds).
  * Errors: ENULL, EINVAL (negative). */
 int kivi_set_num_splits(kivi_cache* cache, int32_t num_splits);
 

@@ -1,0 +1,14 @@
+// decode_b4.cu — the 4-bit instantiations of the tensor-core decode kernel.
+#include "decode_launch.cuh"
+
+namespace kivi {
+namespace mma {
+
+cudaError_t launch_b4(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+  return launch_bits<4>(a, grid, threads, smem, s);
+}
+
+int occupancy_b4(const Geo& g, int threads, int smem) { return occupancy_bits<4>(g, threads, smem); }
+
+}  // namespace mma
+}  // namespace kivi

@@ -1,0 +1,73 @@
+// decode_launch.cuh — per-instantiation launch and occupancy helpers of the
+// tensor-core decode kernel; each decode_b*.cu instantiates one bit width.
+#pragma once
+
+#include <atomic>
+
+#include "decode_mma.cuh"
+
+namespace kivi {
+namespace mma {
+
+template <int D, int BITS, int CH>
+cudaError_t prepare() {
+  // opt in to the largest dynamic shared memory once per instantiation
+  static std::atomic<int> done{0};
+  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, decode_mma_kernel<D, BITS, CH>);
+  if (e != cudaSuccess) return e;
+  // the opt-in limit covers static + dynamic shared memory
+  e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           optin - static_cast<int>(fa.sharedSizeBytes));
+  if (e == cudaSuccess) done.store(1, std::memory_order_release);
+  return e;
+}
+
+template <int D, int BITS, int CH>
+cudaError_t launch_one(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+  cudaError_t e = prepare<D, BITS, CH>();
+  if (e != cudaSuccess) return e;
+  decode_mma_kernel<D, BITS, CH><<<grid, threads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, int BITS, int CH>
+int occupancy_one(int threads, int smem) {
+  if (prepare<D, BITS, CH>() != cudaSuccess) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, BITS, CH>, threads, smem) != cudaSuccess)
+    return 1;
+  return n > 0 ? n : 1;
+}
+
+template <int BITS>
+cudaError_t launch_bits(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+  const bool ch32 = (a.g.G % 32) == 0;
+  if (a.g.d == 64)
+    return ch32 ? launch_one<64, BITS, 32>(a, grid, threads, smem, s) : launch_one<64, BITS, 16>(a, grid, threads, smem, s);
+  return ch32 ? launch_one<128, BITS, 32>(a, grid, threads, smem, s) : launch_one<128, BITS, 16>(a, grid, threads, smem, s);
+}
+
+template <int BITS>
+int occupancy_bits(const Geo& g, int threads, int smem) {
+  const bool ch32 = (g.G % 32) == 0;
+  if (g.d == 64) return ch32 ? occupancy_one<64, BITS, 32>(threads, smem) : occupancy_one<64, BITS, 16>(threads, smem);
+  return ch32 ? occupancy_one<128, BITS, 32>(threads, smem) : occupancy_one<128, BITS, 16>(threads, smem);
+}
+
+// defined in decode_b2.cu, decode_b4.cu, decode_b8.cu
+cudaError_t launch_b2(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_b4(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_b8(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
+int occupancy_b2(const Geo& g, int threads, int smem);
+int occupancy_b4(const Geo& g, int threads, int smem);
+int occupancy_b8(const Geo& g, int threads, int smem);
+
+}  // namespace mma
+}  // namespace kivi

@@ -17,6 +17,7 @@ struct kivi_cache {
   int64_t T;
   int32_t forced_splits;
   int32_t num_sms;
+  int32_t ctas_per_sm;   // resident decode CTAs per SM for this geometry
 };
 
 namespace {
@@ -41,21 +42,21 @@ int validate(const kivi_params* p) {
   if (p->sinks < 0 || p->sinks > 1024) return KIVI_EINVAL;
   if (p->h_kv < 1 || p->h_q < 1 || p->h_q % p->h_kv != 0) return KIVI_EINVAL;
   if (p->h_q / p->h_kv > kMaxRep) return KIVI_EINVAL;
-  if (p->batch < 1 || p->h_kv > 65535 || p->batch > 65535) return KIVI_EINVAL;
+  if (p->batch < 1 || p->batch > 65535) return KIVI_EINVAL;
+  if (static_cast<int64_t>(p->h_kv) * ((p->h_q / p->h_kv + 3) / 4) > 65535) return KIVI_EINVAL;
   if (p->window < 0 || p->max_tokens < 0) return KIVI_EINVAL;
   if (p->window > 0 && p->window < p->residual) return KIVI_EINVAL;
   return KIVI_OK;
 }
 
-// Split-K partitions the workspace is sized for: enough (sequence, kv head,
-// split) work items to fill the GPU several times over when B * h_kv is
-// small; one split per unit when the batch alone fills it.
+// CTAs that may share one (sequence, kv head, head pass) unit: the decode
+// launches at most kMaxDecodeCtas CTAs (one wave on any GPU with up to 256
+// SMs at 4 CTAs each), cut into equal ranges over the units' work, so a unit
+// meets at most ceil(kMaxDecodeCtas / units) + 1 of them.
+constexpr int64_t kMaxDecodeCtas = 1024;
 int32_t max_splits_for(const kivi_params& p) {
-  const int64_t units = static_cast<int64_t>(p.batch) * p.h_kv;
-  int64_t s = (4096 + units - 1) / units;
-  if (s < 1) s = 1;
-  if (s > 256) s = 256;
-  return static_cast<int32_t>(s);
+  const int64_t units = static_cast<int64_t>(p.batch) * p.h_kv * ((p.h_q / p.h_kv + 3) / 4);
+  return static_cast<int32_t>((kMaxDecodeCtas + units - 1) / units + 1);
 }
 
 Geo geometry(const kivi_params& p) {
@@ -82,10 +83,13 @@ Geo geometry(const kivi_params& p) {
   g.unit_bytes = g.groups + g.n_slots * g.block_bytes;
   g.cache_bytes = static_cast<int64_t>(p.batch) * p.h_kv * g.unit_bytes;
   g.max_splits = max_splits_for(p);
+  g.split_stride = g.max_splits + 2;
   const int64_t bhq = static_cast<int64_t>(p.batch) * p.h_q;
+  const int64_t npass = (g.rep + 3) / 4;
   g.ws_partials = round_up(g.cache_bytes, kAlign);
-  g.ws_counters = round_up(g.ws_partials + bhq * g.max_splits * (d + 2) * 4, kAlign);
-  g.ws_q = round_up(g.ws_counters + static_cast<int64_t>(p.batch) * p.h_kv * 4, kAlign);
+  g.ws_counters = round_up(g.ws_partials + bhq * g.split_stride * (d + 2) * 4, kAlign);
+  g.ws_error = round_up(g.ws_counters + static_cast<int64_t>(p.batch) * p.h_kv * npass * 4, kAlign);
+  g.ws_q = round_up(g.ws_error + 4, kAlign);
   g.ws_out = round_up(g.ws_q + bhq * d * 2, kAlign);
   return g;
 }
@@ -112,25 +116,18 @@ kivi::DecodePlan plan_for(const kivi_cache& c) {
   if (first > pl.st.n_groups) first = pl.st.n_groups;
   pl.g_first = first;
   pl.n_vis_groups = pl.st.n_groups - first;
-  int64_t splits;
-  if (c.forced_splits > 0) {
-    splits = c.forced_splits;
-  } else {
-    const int64_t units = static_cast<int64_t>(c.g.B) * c.g.hkv;
-    const int64_t target = static_cast<int64_t>(c.num_sms) * 8;   // work items in flight
-    splits = (target + units - 1) / units;
-    // at least a few groups per split, so the partials stay a small overhead
-    const int64_t by_work = (pl.n_vis_groups + 3) / 4;
-    if (splits > by_work) splits = by_work;
+  // one wave of resident CTAs; the sinks are cut into chunks of 4 tokens and
+  // the ring into chunks of 8, one work position each (at least one position,
+  // empty when the cache is)
+  int64_t ctas = static_cast<int64_t>(c.num_sms) * c.ctas_per_sm;
+  if (ctas > kMaxDecodeCtas) ctas = kMaxDecodeCtas;
+  if (c.forced_splits > 0) {   // a fixed number of CTAs per unit
+    const int64_t units = static_cast<int64_t>(c.g.B) * c.g.hkv * ((c.g.rep + 3) / 4);
+    ctas = units * c.forced_splits;
   }
-  if (splits > c.g.max_splits) splits = c.g.max_splits;
-  if (splits > pl.n_vis_groups) splits = pl.n_vis_groups;
-  if (splits < 1) splits = 1;
-  int64_t gps = (pl.n_vis_groups + splits - 1) / splits;
-  if (gps < 1) gps = 1;
-  splits = pl.n_vis_groups > 0 ? (pl.n_vis_groups + gps - 1) / gps : 1;
-  pl.splits = static_cast<int32_t>(splits);
-  pl.groups_per_split = static_cast<int32_t>(gps);
+  pl.ctas = static_cast<int32_t>(ctas > 0 ? ctas : 1);
+  const int64_t tc = (pl.st.n_sink + 3) / 4 + (pl.st.n_res + 7) / 8;
+  pl.tc = static_cast<int32_t>(tc < 1 ? 1 : tc);
   return pl;
 }
 
@@ -163,6 +160,7 @@ int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_byt
   c->T = 0;
   c->forced_splits = 0;
   c->num_sms = sms > 0 ? sms : 1;
+  c->ctas_per_sm = kivi::decode_ctas_per_sm(g);
   const cudaError_t e = cudaMemsetAsync(d_arena, 0, static_cast<size_t>(arena_bytes_of(g)),
                                         static_cast<cudaStream_t>(cuda_stream));
   if (e != cudaSuccess) { delete c; return KIVI_ECUDA; }
@@ -271,28 +269,25 @@ int noalloc_scratch(void** out) {
 int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda_stream) {
   if (!c || !q || !out) return KIVI_ENULL;
   if (!aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
-  // scratch: [counters, one word per (sequence, kv head)][partials]
-  const int64_t counter_bytes = round_up(static_cast<int64_t>(c->g.B) * c->g.hkv * 4, kAlign);
-  const int64_t record = static_cast<int64_t>(c->g.B) * c->g.hq * (c->g.d + 2) * 4;   // one split
-  const int64_t fit = (static_cast<int64_t>(kNoAllocScratchBytes) - counter_bytes) / record;
-  if (fit < 1) return KIVI_ESCRATCH;
-  kivi::DecodePlan pl = plan_for(*c);
-  if (pl.splits > fit) {
-    const int64_t gps = (pl.n_vis_groups + fit - 1) / fit;
-    pl.groups_per_split = static_cast<int32_t>(gps);
-    pl.splits = static_cast<int32_t>((pl.n_vis_groups + gps - 1) / gps);
-  }
-  Geo g = c->g;
-  g.max_splits = pl.splits;   // partial records are strided by this split count
+  // scratch: [error word][merge counters, npass per (sequence, kv head)][partials]
+  const int64_t npass = (c->g.rep + 3) / 4;
+  const int64_t head_bytes = kAlign + round_up(static_cast<int64_t>(c->g.B) * c->g.hkv * npass * 4, kAlign);
+  const int64_t record = static_cast<int64_t>(c->g.B) * c->g.hq * (c->g.d + 2) * 4;   // one CTA per unit
+  const int64_t fit = (static_cast<int64_t>(kNoAllocScratchBytes) - head_bytes) / record;
+  if (fit < 3) return KIVI_ESCRATCH;   // at least two CTAs per unit
+  const kivi::DecodePlan pl = plan_for(*c);   // the launch caps the CTAs so a unit's partials fit
   void* base = nullptr;
   const int st = noalloc_scratch(&base);
   if (st != KIVI_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  unsigned* counters = static_cast<unsigned*>(base);
-  float* partials = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + counter_bytes);
-  if (cudaMemsetAsync(counters, 0, static_cast<size_t>(counter_bytes), s) != cudaSuccess) return KIVI_ECUDA;
-  return cuda_status(kivi::launch_decode_scratch(g, c->arena, static_cast<const __half*>(q),
-                                                 static_cast<__half*>(out), pl, partials, counters, s));
+  unsigned char* bytes = static_cast<unsigned char*>(base);
+  unsigned* error = reinterpret_cast<unsigned*>(bytes);
+  unsigned* counters = reinterpret_cast<unsigned*>(bytes + kAlign);
+  float* partials = reinterpret_cast<float*>(bytes + head_bytes);
+  if (cudaMemsetAsync(bytes, 0, static_cast<size_t>(head_bytes), s) != cudaSuccess) return KIVI_ECUDA;
+  return cuda_status(kivi::launch_decode_scratch(c->g, c->arena, static_cast<const __half*>(q),
+                                                 static_cast<__half*>(out), pl, partials,
+                                                 static_cast<int32_t>(fit), counters, error, s));
 }
 
 int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {

@@ -19,8 +19,10 @@ struct Geo {
   int64_t cache_bytes;
   int64_t ws_partials;   // arena offset of the split-K partials
   int64_t ws_counters;   // arena offset of the per-unit merge counters
+  int64_t ws_error;      // arena offset of the device error word
   int64_t ws_q, ws_out;  // arena offsets of the host-call staging buffers
-  int32_t max_splits;
+  int32_t max_splits;    // CTAs that may share one unit (partial records - 2)
+  int32_t split_stride;  // partial records per query head
 };
 
 // Cache state after T tokens (lazy flush: a token that reaches a full ring
@@ -55,17 +57,33 @@ struct DecodePlan {
   State st;
   int64_t g_first;        // first frozen group that can hold a visible token
   int64_t n_vis_groups;   // groups [g_first, n_groups)
-  int32_t splits;         // split-K partitions per unit
-  int32_t groups_per_split;
+  int32_t tc;             // work positions (in groups) that stand for one unit's tail
+  int32_t ctas;           // CTAs of the wave (the launch clamps it further)
 };
+
+// Launch shape of the decode kernel for a geometry (host side, no device work).
+struct DecodeShape {
+  int32_t nw;             // warps per CTA
+  int32_t ns;             // copy stages per warp
+  int32_t stage_bytes;
+  int32_t smem_base;      // dynamic shared memory per CTA without the merge weights
+  int32_t npass;          // head passes (4 query heads each) per kv head
+};
+DecodeShape decode_shape(const Geo& g);
+// Dynamic shared memory of one CTA when partial records are strided by `stride`.
+inline int32_t decode_smem(const DecodeShape& sh, int32_t stride) { return sh.smem_base + 16 * stride; }
+// Resident decode CTAs per SM for this geometry (queries the device).
+int decode_ctas_per_sm(const Geo& g);
 
 // Decode with the arena's own workspace for the split-K partials.
 cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,
                           const DecodePlan& plan, cudaStream_t stream);
-// Decode with caller-chosen scratch: `partials` holds B * h_q * max_splits
-// records of (d + 2) floats, `counters` one word per (sequence, kv head).
+// Decode with caller-chosen scratch: `partials` holds B * h_q * stride
+// records of (d + 2) floats, `counters` npass words per (sequence, kv head),
+// zero on entry and left zero on exit, `error` one word that the kernel ORs
+// with 1 if a copy never arrived.
 cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
-                                  const DecodePlan& plan, float* partials, unsigned* counters,
-                                  cudaStream_t stream);
+                                  const DecodePlan& plan, float* partials, int32_t stride,
+                                  unsigned* counters, unsigned* error, cudaStream_t stream);
 
 }  // namespace kivi
