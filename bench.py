@@ -35,7 +35,7 @@ NOMINAL_HBM_GBS = 8000.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="mha7b")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -75,55 +75,115 @@ def workload_config(w, extra=None):
 
 # --------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """SM clock and throttle reasons sampled while the timed region runs.
 
+    Reads NVML (libnvidia-ml, the driver's management library) through ctypes
+    every 2 ms from a thread, so that even a timed region of a few tens of
+    milliseconds gets samples; falls back to `nvidia-smi -lms 200` when NVML
+    cannot be loaded.  Only samples taken between mark_begin() and mark_end()
+    count.  Nothing here changes a GPU setting."""
+
+    # NVML clock-event reason bits (nvml.h: nvmlClocksEventReason*)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
-        self.rows = []
+    def __init__(self, device):
+        self.device = device
+        self.rows = []          # (t, sm_mhz, max_mhz, set of reasons)
         self.proc = None
+        self.nvml = None
+        self.running = False
+        self.t_begin = self.t_end = None
+
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if nv.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        idx = self.device.index if self.device.index is not None else 0
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.device).uuid)
+            ok = nv.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid.encode()), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) != 0:
+            return None
+        self.index = idx
+        return nv, h
 
     def start(self):
+        self.nvml = self._nvml_handle()
+        self.running = True
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.thread.start()
+            return
         try:
+            idx = self.device.index if self.device.index is not None else 0
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.index)],
+                                          "-lms", "200", "-i", str(idx)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.rows.append([c.strip() for c in line.split(",")])
+    def _poll_nvml(self):
+        import ctypes
+        nv, h = self.nvml
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while self.running:
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and \
+                    get_reasons(h, ctypes.byref(rs)) == 0:
+                reasons = {n for bit, n in self.REASONS.items() if rs.value & bit}
+                self.rows.append((time.perf_counter(), float(clk.value), float(mx.value), reasons))
+            time.sleep(0.002)
 
-    def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.thread.join(timeout=2)
-        sm, mx, reasons = [], None, set()
+    def _read_smi(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in self.rows:
+        for line in self.proc.stdout:
+            r = [c.strip() for c in line.split(",")]
             try:
-                sm.append(float(r[1]))
-                mx = float(r[2])
-                for i, n in enumerate(names):
-                    if r[5 + i].lower().startswith("active"):
-                        reasons.add(n)
+                reasons = {n for i, n in enumerate(names) if r[5 + i].lower().startswith("active")}
+                self.rows.append((time.perf_counter(), float(r[1]), float(r[2]), reasons))
             except (ValueError, IndexError):
                 continue
-        if not sm:
+
+    def mark_begin(self):
+        self.t_begin = time.perf_counter()
+
+    def mark_end(self):
+        self.t_end = time.perf_counter()
+
+    def stop(self):
+        self.running = False
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if getattr(self, "thread", None) is not None:
+            self.thread.join(timeout=2)
+        rows = [r for r in self.rows if self.t_begin is None or self.t_begin <= r[0] <= self.t_end]
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = set().union(*(r[3] for r in rows))
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": rows[-1][2],
+                "reasons": sorted(reasons), "samples": len(rows),
+                "source": "nvml 2 ms" if self.nvml is not None else "nvidia-smi 200 ms"}
 
 
 # --------------------------------------------------------------- bytes
@@ -153,7 +213,9 @@ def run_ours(args, rank, world, device):
     from kivi_quantized_kv_gb300 import cache_bytes
     per_cache = cache_bytes(cfg)
     l2 = 129 * 1024 * 1024
-    n_rep = args.replicas or max(2, -(-4 * l2 // per_cache))
+    # enough replicas for 4x L2, and for each sequence to grow by at most 64
+    # tokens over the run
+    n_rep = args.replicas or max(2, -(-4 * l2 // per_cache), -(-total_steps // 64))
     stream = torch.cuda.current_stream(device)
 
     caches = []
@@ -196,13 +258,14 @@ def run_ours(args, rank, world, device):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(device.index if device.index is not None else 0) if rank == 0 else None
+    clocks = ClockSampler(device) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
     if clocks:
         clocks.start()
-        time.sleep(0.3)
+        time.sleep(0.05)
+        clocks.mark_begin()
     t0.record(stream)
     dec_bytes = app_bytes = launches = 0
     for i in range(args.steps):
@@ -211,9 +274,11 @@ def run_ours(args, rank, world, device):
         dec_bytes += c.decode_bytes()
         app_bytes += append_bytes(w, Lb, La)
         flush = La["n_groups"] > Lb["n_groups"]
-        launches += (2 if flush else 1) + 2     # append: write (+flush); decode: split + merge
+        launches += (2 if flush else 1) + 1     # append: write (+ flush); decode: one launch, merge inside
     t1.record(stream)
     torch.cuda.synchronize(device)
+    if clocks:
+        clocks.mark_end()
     clk = clocks.stop() if clocks else None
     if world > 1:
         torch.distributed.barrier()
@@ -367,13 +432,14 @@ def main():
     line = {
         "metric": METRIC, "value": round(r["value"], 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32", "data": "synthetic",
         "config": workload_config(w, {"parallelism": f"replicas{world}",
                                       "l2": f"{r['n_rep']} rotating cache replicas x {r['per_cache'] / 1e6:.0f} MB "
-                                            f"(> 4x 129 MB L2)"}),
+                                            f"(> 4x 129 MB L2)",
+                                      "appended_per_sequence": -(-(args.steps + args.warmup) // r["n_rep"])}),
         "roofline": {"bound": "hbm", "achieved": round(r["dec_gbs"], 1), "peak": peak, "unit": "GB/s",
                      "frac": round(r["dec_gbs"] / peak, 4), "traffic": traffic,
-                     "kernel": "kivi_decode_attn (split-K + merge)", "peak_source": src,
+                     "kernel": "decode_mma_kernel (stream-K split-K, merge in the same launch)", "peak_source": src,
                      "bytes_per_launch": int(r["dec_bytes"])},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
@@ -394,14 +460,32 @@ def main():
         torch.distributed.destroy_process_group()
 
 
+DECODE_SOURCES = ("kivi_internal.cuh", "decode_mma.cuh", "decode_launch.cuh", "decode.cu",
+                  "decode_b2.cu", "decode_b4.cu", "decode_b8.cu")
+
+
+def decode_sources_sha():
+    """sha256 over the decode kernel's sources, in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "kivi_quantized_kv_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def load_traffic(name):
-    """DRAM bytes per decode launch from the committed ncu summary, if the
-    kernel has not changed since it was taken (profiles/traffic.json)."""
+    """DRAM bytes (read + write) per decode launch from the committed ncu
+    summary profiles/traffic.json, or None when that capture does not cover
+    this workload or was taken on other decode sources than the ones built."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        return t.get(name)
+        if t.get("decode_sources_sha256") != decode_sources_sha():
+            return None
+        e = t["workloads"][name]
+        return int(e["dram_bytes_read"] + e["dram_bytes_write"])
     except Exception:
         return None
 

@@ -12,28 +12,30 @@ int32_t round_up32(int64_t x, int64_t a) { return static_cast<int32_t>((x + a - 
 DecodeShape decode_shape(const Geo& g) {
   DecodeShape sh{};
   const int64_t ch = (g.G % 32) == 0 ? 32 : 16;
-  // a stage holds one group block or one tail chunk (4 fp32 or 8 fp16 tokens, K and V)
+  // a stage holds one group block, one tail chunk (4 fp32 or 8 fp16 tokens,
+  // K and V) or the query rows of one head pass
   const int64_t chunk = 32 * static_cast<int64_t>(g.d);
   sh.stage_bytes = round_up32(g.block_bytes > chunk ? g.block_bytes : chunk, 128);
+  // per warp besides its stages (mma::WarpSmem): query rows with padded
+  // quarters, the combine slot, the P' exchange
+  const int64_t q_bytes = 16 * (g.d / 2 + 16);
+  const int64_t slot_bytes = 16 * (g.d + 4);
+  const int64_t xch_bytes = ch == 32 ? 512 : 256;
   // 2 copy stages per warp (3 for small blocks); as many warps (2..8) as fit
-  // in about 110 KB, so that two CTAs share an SM
+  // in about 112 KB, so that two CTAs share an SM
   int ns = sh.stage_bytes <= 3072 ? 3 : 2;
-  const int64_t fixed = 4 * (g.d + 4) * 4 + 4 * g.d * 2 + 16 * 64;     // q (fp32, fp16), typical merge weights
   int64_t per_warp = 0, nw = 0;
   for (;; --ns) {
-    per_warp = static_cast<int64_t>(ns) * sh.stage_bytes   // stages
-               + (8 + 4 * g.d) * 4                          // red_m, red_l, red_o
-               + 8 * ch * 2                                 // P' exchange
-               + 8 * ns;                                    // barriers
-    nw = (110 * 1024 - fixed) / per_warp;
+    per_warp = static_cast<int64_t>(ns) * sh.stage_bytes + q_bytes + slot_bytes + xch_bytes + 8 * ns;
+    nw = (112 * 1024) / per_warp;
     if (nw > 8) nw = 8;
     if (nw < 2) nw = 2;
     // very large group blocks: fewer stages rather than more than ~190 KB
-    if (nw * per_warp + fixed <= 190 * 1024 || ns == 1) break;
+    if (nw * per_warp <= 190 * 1024 || ns == 1) break;
   }
   sh.ns = ns;
   sh.nw = static_cast<int32_t>(nw);
-  sh.smem_base = round_up32(nw * per_warp + 4 * (g.d + 4) * 4 + 4 * g.d * 2, 16);
+  sh.smem_base = round_up32(nw * per_warp, 16);
   sh.npass = (g.rep + 3) / 4;
   return sh;
 }

@@ -66,12 +66,12 @@ struct DecodeShape {
   int32_t nw;             // warps per CTA
   int32_t ns;             // copy stages per warp
   int32_t stage_bytes;
-  int32_t smem_base;      // dynamic shared memory per CTA without the merge weights
+  int32_t smem_base;      // dynamic shared memory per CTA
   int32_t npass;          // head passes (4 query heads each) per kv head
 };
 DecodeShape decode_shape(const Geo& g);
-// Dynamic shared memory of one CTA when partial records are strided by `stride`.
-inline int32_t decode_smem(const DecodeShape& sh, int32_t stride) { return sh.smem_base + 16 * stride; }
+// Dynamic shared memory of one CTA (independent of the partial-record stride).
+inline int32_t decode_smem(const DecodeShape& sh, int32_t /*stride*/) { return sh.smem_base; }
 // Resident decode CTAs per SM for this geometry (queries the device).
 int decode_ctas_per_sm(const Geo& g);
 
