@@ -179,7 +179,7 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  *   - All calls share the array: calls whose GPU work overlaps (concurrent
  *     streams or host threads) race on it.  The merge counters in it are
  *     cleared by every call.
- *   - Three partial records per query head, 3 * B * h_q * (head_dim + 2) * 4
+ *   - Three partial records per query head, 3 * B * h_q * (head_dim + 4) * 4
  *     bytes, plus the merge counters must fit in 4 MiB, else KIVI_ESCRATCH and
  *     nothing runs; the work is spread over fewer CTAs when fewer records fit.
  * Errors: ENULL, EALIGN, ESCRATCH, ECUDA. */

@@ -21,18 +21,24 @@ DecodeShape decode_shape(const Geo& g) {
   const int64_t q_bytes = 16 * (g.d / 2 + 16);
   const int64_t slot_bytes = 16 * (g.d + 4);
   const int64_t xch_bytes = ch == 32 ? 512 : 256;
-  // 2 copy stages per warp (3 for small blocks); as many warps (2..8) as fit
-  // in about 112 KB, so that two CTAs share an SM
-  int ns = sh.stage_bytes <= 3072 ? 3 : 2;
-  int64_t per_warp = 0, nw = 0;
-  for (;; --ns) {
-    per_warp = static_cast<int64_t>(ns) * sh.stage_bytes + q_bytes + slot_bytes + xch_bytes + 8 * ns;
-    nw = (112 * 1024) / per_warp;
-    if (nw > 8) nw = 8;
-    if (nw < 2) nw = 2;
-    // very large group blocks: fewer stages rather than more than ~190 KB
-    if (nw * per_warp <= 190 * 1024 || ns == 1) break;
-  }
+  // shared memory of one CTA: the SM's 228 KB shared by kDecodeCtasPerSm
+  // CTAs, less the 1 KB the driver reserves per CTA and room for the static
+  // shared memory, and at most the 227 KB one CTA may have
+  int64_t budget = (228 * 1024) / kDecodeCtasPerSm - 1024 - 512;
+  if (budget > 227 * 1024 - 512) budget = 227 * 1024 - 512;
+  auto per_warp_of = [&](int stages) {
+    return static_cast<int64_t>(stages) * sh.stage_bytes + q_bytes + slot_bytes + xch_bytes + 8 * stages;
+  };
+  // as many warps (up to kDecodeWarps) as fit with two copy stages each, then
+  // more stages (up to four) while they fit; very large group blocks get a
+  // single stage rather than fewer than two warps
+  int ns = 2;
+  int64_t nw = budget / per_warp_of(ns);
+  if (nw < 2) { ns = 1; nw = budget / per_warp_of(ns); }
+  if (nw > kDecodeWarps) nw = kDecodeWarps;
+  if (nw < 1) nw = 1;
+  while (ns < 4 && nw * per_warp_of(ns + 1) <= budget) ++ns;
+  const int64_t per_warp = per_warp_of(ns);
   sh.ns = ns;
   sh.nw = static_cast<int32_t>(nw);
   sh.smem_base = round_up32(nw * per_warp, 16);

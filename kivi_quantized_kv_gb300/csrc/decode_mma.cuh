@@ -71,7 +71,7 @@ struct Args {
   const uint8_t* arena;
   const __half* q;
   __half* out;
-  float* partials;      // [B][h_q][stride][d + 2]
+  float* partials;      // [B][h_q][stride][d + 4]: o[d], m, l, 2 pad
   unsigned* counters;   // [units]: CTAs finished per unit
   unsigned* error;      // kErrCopy | kErrSlot
   DecodePlan plan;
@@ -307,8 +307,160 @@ struct WarpSmem {
   static constexpr int kXch = CH == 32 ? 512 : 256;
 };
 
+// First query head of unit u (sequence, kv head, head pass).
+__device__ __forceinline__ int64_t unit_head0(const Args& a, int u) {
+  const int per_b = a.g.hkv * a.npass;
+  return static_cast<int64_t>(u / per_b) * a.g.hq + ((u % per_b) / a.npass) * a.g.rep + 4 * (u % a.npass);
+}
+
+// Merge of the `total` partial records (o[D], m, l, pad, pad) of one query
+// head for channel ch: M = max m_s, w_s = 2^(m_s - M), L = Σ l_s w_s,
+// O = Σ o_s[ch] w_s.  Eight records' loads go out at a time.
+template <int D>
+__device__ __forceinline__ void merge_partials(const float* base, int total, int ch, float& O, float& L) {
+  float m = -INFINITY;
+  O = 0.f;
+  L = 0.f;
+  for (int s0 = 0; s0 < total; s0 += 8) {
+    float2 ml[8];
+    float o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (s0 + k < total) {
+        const float* ps = base + (s0 + k) * (D + 4);
+        ml[k] = __ldcg(reinterpret_cast<const float2*>(ps + D));
+        o[k] = __ldcg(ps + ch);
+      } else {
+        ml[k] = make_float2(-INFINITY, 0.f);
+        o[k] = 0.f;
+      }
+    }
+    float mb = m;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mb = fmaxf(mb, ml[k].x);
+    if (mb == -INFINITY) continue;
+    const float sc = (m == -INFINITY) ? 0.f : ex2(m - mb);
+    O *= sc;
+    L *= sc;
+    m = mb;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float f = (ml[k].x == -INFINITY) ? 0.f : ex2(ml[k].x - m);
+      O = fmaf(o[k], f, O);
+      L = fmaf(ml[k].y, f, L);
+    }
+  }
+}
+
+// Combines head hh of the nw warp slots (o[D], m, l, pad, pad) for channel ch.
+template <int D>
+__device__ __forceinline__ void combine_slots(const float* slots, int slot_floats, int nw, int hh, int ch,
+                                              float& M, float& L, float& O) {
+  M = -INFINITY;
+  for (int w = 0; w < nw; ++w) M = fmaxf(M, slots[w * slot_floats + hh * (D + 4) + D]);
+  L = 0.f;
+  O = 0.f;
+  if (M == -INFINITY) return;
+  for (int w = 0; w < nw; ++w) {
+    const float* so = slots + w * slot_floats + hh * (D + 4);
+    const float mw = so[D];
+    const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+    L = fmaf(so[D + 1], f, L);
+    O = fmaf(so[ch], f, O);
+  }
+}
+
+// A combined (M, L, O) of channel ch of query head `head`: the output when
+// the unit lies inside one CTA, else this CTA's partial record.
+template <int D>
+__device__ __forceinline__ void publish(const Args& a, int64_t head, int ch, int total, int cslot, float M,
+                                        float L, float O) {
+  if (total == 1) {
+    a.out[head * D + ch] = __float2half_rn(L > 0.f ? O / L : 0.f);
+  } else {
+    float* dst = a.partials + (head * a.stride + cslot) * (D + 4);
+    dst[ch] = O;
+    if (ch == 0) { dst[D] = M; dst[D + 1] = L; }
+  }
+}
+
+// Epilogue of a unit that is not the CTA's last, run by the last warp to sign
+// in: combines the slots, publishes, releases the slots (s_done) and, in the
+// unit's last CTA, merges the partials.
+template <int D>
+__device__ __forceinline__ void warp_epilogue(const Args& a, const float* slots, int slot_floats, int nw, int u,
+                                           int nh, int total, int cslot, int useq, unsigned* s_done) {
+  const int lane = threadIdx.x & 31;
+  const int64_t head0 = unit_head0(a, u);
+  for (int hh = 0; hh < nh; ++hh) {
+    // per head: the max and the slot weights once, channels lane + 32 j
+    float M = -INFINITY;
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, slots[w * slot_floats + hh * (D + 4) + D]);
+    float L = 0.f, O[D / 32];
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) O[j] = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < nw; ++w) {
+        const float* so = slots + w * slot_floats + hh * (D + 4);
+        const float mw = so[D];
+        const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        L = fmaf(so[D + 1], f, L);
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) O[j] = fmaf(so[lane + 32 * j], f, O[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) publish<D>(a, head0 + hh, lane + 32 * j, total, cslot, M, L, O[j]);
+  }
+  __syncwarp();
+  __threadfence_block();
+  if (lane == 0) *reinterpret_cast<volatile unsigned*>(s_done) = static_cast<unsigned>(useq + 1);
+  if (total == 1) return;
+  __threadfence();
+  __syncwarp();
+  unsigned last_cta = 0;
+  if (lane == 0) last_cta = (atomicAdd(a.counters + u, 1u) == static_cast<unsigned>(total - 1)) ? 1u : 0u;
+  last_cta = __shfl_sync(0xffffffffu, last_cta, 0);
+  if (!last_cta) return;
+  __threadfence();
+  for (int i = lane; i < nh * D; i += 32) {
+    const int hh = i / D, ch = i % D;
+    float O, L;
+    merge_partials<D>(a.partials + (head0 + hh) * a.stride * (D + 4), total, ch, O, L);
+    a.out[(head0 + hh) * D + ch] = __float2half_rn(L > 0.f ? O / L : 0.f);
+  }
+  if (lane == 0) a.counters[u] = 0u;
+}
+
+// Epilogue of the CTA's last unit, run by every thread of the CTA.
+template <int D>
+__device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, int slot_floats, int nw, int u,
+                                          int nh, int total, int cslot, unsigned* s_flag) {
+  const int64_t head0 = unit_head0(a, u);
+  for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
+    const int hh = i / D, ch = i % D;
+    float M, L, O;
+    combine_slots<D>(slots, slot_floats, nw, hh, ch, M, L, O);
+    publish<D>(a, head0 + hh, ch, total, cslot, M, L, O);
+  }
+  if (total == 1) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *s_flag = (atomicAdd(a.counters + u, 1u) == static_cast<unsigned>(total - 1)) ? 1u : 0u;
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
+    const int hh = i / D, ch = i % D;
+    float O, L;
+    merge_partials<D>(a.partials + (head0 + hh) * a.stride * (D + 4), total, ch, O, L);
+    a.out[(head0 + hh) * D + ch] = __float2half_rn(L > 0.f ? O / L : 0.f);
+  }
+  if (threadIdx.x == 0) a.counters[u] = 0u;
+}
+
 template <int D, int BITS, int CH>
-__global__ void __launch_bounds__(256, 2) decode_mma_kernel(const Args a) {
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mma_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   using WS = WarpSmem<D, CH>;
   constexpr int RK = D * BITS / 8;          // key row bytes
@@ -348,6 +500,7 @@ __global__ void __launch_bounds__(256, 2) decode_mma_kernel(const Args a) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(xch_all + nw * WS::kXch);
   __shared__ unsigned s_arrive;   // warps signed in for the current combine
   __shared__ unsigned s_done;     // combines completed
+  __shared__ unsigned s_flag;     // this CTA merges its last unit
 
   uint8_t* my_stages = stages + static_cast<size_t>(warp) * a.ns * a.stage_bytes;
   uint8_t* qw = q_all + warp * WS::kQ;
@@ -844,87 +997,23 @@ __global__ void __launch_bounds__(256, 2) decode_mma_kernel(const Args a) {
         so[16 * ct + r + 8] = fmaf(oacc[ct][2] + oacc[ct][3], osc, mh);
       }
     }
-    __threadfence_block();
-    __syncwarp();
-    unsigned last = 0;
-    if (lane == 0) last = (atomicAdd(&s_arrive, 1u) == static_cast<unsigned>(nw - 1)) ? 1u : 0u;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) continue;
-
-    // ------------------------------------------------------ combine (last warp)
-    __threadfence_block();
-    if (lane == 0) s_arrive = 0u;
-    const int64_t head0 = static_cast<int64_t>(u / (g.hkv * a.npass)) * g.hq +
-                          ((u % (g.hkv * a.npass)) / a.npass) * rep + 4 * (u % a.npass);
-    for (int hh = 0; hh < nh; ++hh) {
-      float M = -INFINITY;
-      for (int w = 0; w < nw; ++w) M = fmaxf(M, slots[w * (WS::kSlot / 4) + hh * (D + 4) + D]);
-      float L = 0.f, O[D / 32];
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) O[j] = 0.f;
-      if (M != -INFINITY) {
-        for (int w = 0; w < nw; ++w) {
-          const float* so = slots + w * (WS::kSlot / 4) + hh * (D + 4);
-          const float mw = so[D];
-          const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-          L = fmaf(so[D + 1], f, L);
-#pragma unroll
-          for (int j = 0; j < D / 32; ++j) O[j] = fmaf(so[lane + 32 * j], f, O[j]);
-        }
-      }
-      if (total == 1) {
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) a.out[(head0 + hh) * D + lane + 32 * j] = __float2half_rn(O[j] * inv);
-      } else {
-        float* dst = a.partials + ((head0 + hh) * a.stride + cslot) * (D + 2);
-#pragma unroll
-        for (int j = 0; j < D / 32; ++j) dst[lane + 32 * j] = O[j];
-        if (lane == 0) { dst[D] = M; dst[D + 1] = L; }
-      }
+    if (u != u_last) {
+      __threadfence_block();
+      __syncwarp();
+      unsigned last = 0;
+      if (lane == 0) last = (atomicAdd(&s_arrive, 1u) == static_cast<unsigned>(nw - 1)) ? 1u : 0u;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+      // the last warp to sign in combines the unit while the others stream on
+      __threadfence_block();
+      if (lane == 0) s_arrive = 0u;
+      warp_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, useq, &s_done);
+      continue;
     }
-    __syncwarp();
-    __threadfence_block();
-    if (lane == 0) *reinterpret_cast<volatile unsigned*>(&s_done) = static_cast<unsigned>(useq + 1);
-    if (total == 1) continue;
-
-    // ------------------------------------------------------ cross-CTA merge
-    __threadfence();
-    __syncwarp();
-    unsigned last_cta = 0;
-    if (lane == 0) last_cta = (atomicAdd(a.counters + u, 1u) == static_cast<unsigned>(total - 1)) ? 1u : 0u;
-    last_cta = __shfl_sync(0xffffffffu, last_cta, 0);
-    if (!last_cta) continue;
-    __threadfence();
-    // M = max m_s, w_s = 2^(m_s - M), L = Σ l_s w_s, out = Σ o_s w_s / L
-    for (int hh = 0; hh < nh; ++hh) {
-      const float* base = a.partials + (head0 + hh) * a.stride * (D + 2);
-      float M = -INFINITY;
-      for (int s = lane; s < total; s += 32) M = fmaxf(M, __ldcg(base + s * (D + 2) + D));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float L = 0.f, O[D / 32];
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) O[j] = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll 2
-        for (int s = 0; s < total; ++s) {
-          const float* ps = base + s * (D + 2);
-          const float ms = __ldcg(ps + D), ls = __ldcg(ps + D + 1);
-          float x[D / 32];
-#pragma unroll
-          for (int j = 0; j < D / 32; ++j) x[j] = __ldcg(ps + lane + 32 * j);
-          const float f = (ms == -INFINITY) ? 0.f : ex2(ms - M);
-          L = fmaf(ls, f, L);
-#pragma unroll
-          for (int j = 0; j < D / 32; ++j) O[j] = fmaf(x[j], f, O[j]);
-        }
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) a.out[(head0 + hh) * D + lane + 32 * j] = __float2half_rn(O[j] * inv);
-    }
-    if (lane == 0) a.counters[u] = 0u;
+    // the CTA's last unit: nothing is left to stream, so every thread takes part
+    __syncthreads();
+    cta_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, &s_flag);
+    break;
   }
 
   // drain this warp's copies still in flight (only after an abort), bounded

@@ -87,7 +87,7 @@ Geo geometry(const kivi_params& p) {
   const int64_t bhq = static_cast<int64_t>(p.batch) * p.h_q;
   const int64_t npass = (g.rep + 3) / 4;
   g.ws_partials = round_up(g.cache_bytes, kAlign);
-  g.ws_counters = round_up(g.ws_partials + bhq * g.split_stride * (d + 2) * 4, kAlign);
+  g.ws_counters = round_up(g.ws_partials + bhq * g.split_stride * (d + 4) * 4, kAlign);
   g.ws_error = round_up(g.ws_counters + static_cast<int64_t>(p.batch) * p.h_kv * npass * 4, kAlign);
   g.ws_q = round_up(g.ws_error + 4, kAlign);
   g.ws_out = round_up(g.ws_q + bhq * d * 2, kAlign);
@@ -272,7 +272,7 @@ int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda
   // scratch: [error word][merge counters, npass per (sequence, kv head)][partials]
   const int64_t npass = (c->g.rep + 3) / 4;
   const int64_t head_bytes = kAlign + round_up(static_cast<int64_t>(c->g.B) * c->g.hkv * npass * 4, kAlign);
-  const int64_t record = static_cast<int64_t>(c->g.B) * c->g.hq * (c->g.d + 2) * 4;   // one CTA per unit
+  const int64_t record = static_cast<int64_t>(c->g.B) * c->g.hq * (c->g.d + 4) * 4;   // one CTA per unit
   const int64_t fit = (static_cast<int64_t>(kNoAllocScratchBytes) - head_bytes) / record;
   if (fit < 3) return KIVI_ESCRATCH;   // at least two CTAs per unit
   const kivi::DecodePlan pl = plan_for(*c);   // the launch caps the CTAs so a unit's partials fit

@@ -61,6 +61,11 @@ struct DecodePlan {
   int32_t ctas;           // CTAs of the wave (the launch clamps it further)
 };
 
+// Decode launch shape: up to kDecodeWarps warps per CTA and kDecodeCtasPerSm
+// CTAs per SM (the kernel's launch bounds; registers per thread follow).
+constexpr int kDecodeWarps = 8;
+constexpr int kDecodeCtasPerSm = 2;
+
 // Launch shape of the decode kernel for a geometry (host side, no device work).
 struct DecodeShape {
   int32_t nw;             // warps per CTA
@@ -79,7 +84,7 @@ int decode_ctas_per_sm(const Geo& g);
 cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,
                           const DecodePlan& plan, cudaStream_t stream);
 // Decode with caller-chosen scratch: `partials` holds B * h_q * stride
-// records of (d + 2) floats, `counters` npass words per (sequence, kv head),
+// records of (d + 4) floats, `counters` npass words per (sequence, kv head),
 // zero on entry and left zero on exit, `error` one word that the kernel ORs
 // with 1 if a copy never arrived.
 cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __half* q, __half* out,

@@ -78,7 +78,7 @@ def test_noalloc_matches_workspace_decode_twice(shape):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    """3 * B * h_q * (d + 2) * 4 bytes must fit in 4 MiB: 3 * 128 * 64 * 130 * 4 does not."""
+    """3 * B * h_q * (d + 4) * 4 bytes must fit in 4 MiB: 3 * 128 * 64 * 132 * 4 does not."""
     from kivi_quantized_kv_gb300 import KiviCache, KiviConfig, _abi
     L = _abi.lib()
     cfg = KiviConfig(bits=4, group=32, residual=128, sinks=4, h_q=64, h_kv=8, head_dim=128, batch=128,
