@@ -27,7 +27,7 @@ DecodeShape decode_shape(const Geo& g) {
   int64_t budget = (228 * 1024) / kDecodeCtasPerSm - 1024 - 512;
   if (budget > 227 * 1024 - 512) budget = 227 * 1024 - 512;
   auto per_warp_of = [&](int stages) {
-    return static_cast<int64_t>(stages) * sh.stage_bytes + q_bytes + slot_bytes + xch_bytes + 8 * stages;
+    return static_cast<int64_t>(stages) * sh.stage_bytes + q_bytes + slot_bytes + xch_bytes + 12 * stages;
   };
   // as many warps (up to kDecodeWarps) as fit with two copy stages each, then
   // more stages (up to four) while they fit; very large group blocks get a

@@ -10,16 +10,17 @@
 // its visible frozen groups, then `tc` positions for its tail (the fp32 sinks
 // in chunks of 4 tokens, then the fp16 ring in chunks of 8).  The units'
 // positions, laid end to end, are cut into one equal contiguous range per CTA,
-// and the grid is one wave of resident CTAs.  Inside a CTA, warp w takes the
-// positions lo + w, lo + w + nw, ... of every unit its CTA's range touches.
+// and the grid is one wave of resident CTAs.  Inside a CTA the warps claim
+// the range's positions one at a time from a shared counter, so a warp that
+// is held up (say, by combining a unit) simply takes fewer.
 //
 // Warps never wait for one another while they stream:
-//  * each warp runs its own copy pipeline: lane 0 issues one 1-D
-//    cp.async.bulk per item into the warp's next stage (completing on that
-//    stage's mbarrier) and keeps `ns` items in flight, walking on into the
-//    next unit while the warp still computes the current one.  The items of
-//    a unit are the unit's query rows (so no CTA barrier is needed to share
-//    them), then the warp's group blocks and tail chunks;
+//  * each warp runs its own copy pipeline: lane 0 claims a position, issues
+//    one 1-D cp.async.bulk per item into the warp's next stage (completing on
+//    that stage's mbarrier) and keeps `ns` items in flight, walking on into
+//    the next unit while the warp still computes the current one.  Before
+//    its first position of a unit a warp copies the unit's query rows (so no
+//    CTA barrier is needed to share them);
 //  * a warp that finishes a unit leaves its (m, l, o) in its shared-memory
 //    slot and signs in; the last warp of the CTA to sign in combines the
 //    slots, writes the output (unit inside one CTA) or the CTA's partial, and
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const int u_first = static_cast<int>(c_start / a.uw);
   const int u_last = static_cast<int>((c_end - 1) / a.uw);
 
-  // shared memory: stages | q | slots | exchange | barriers (per warp, warp-major within each)
+  // shared memory: stages | q | slots | exchange | barriers | item rings (per warp, warp-major within each)
   uint8_t* stages = smem_raw;
   uint8_t* q_all = stages + static_cast<size_t>(nw) * a.ns * a.stage_bytes;
   float* slots = reinterpret_cast<float*>(q_all + nw * WS::kQ);
@@ -501,29 +502,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   __shared__ unsigned s_arrive;   // warps signed in for the current combine
   __shared__ unsigned s_done;     // combines completed
   __shared__ unsigned s_flag;     // this CTA merges its last unit
+  __shared__ unsigned s_next;     // positions of the CTA's range claimed so far
 
   uint8_t* my_stages = stages + static_cast<size_t>(warp) * a.ns * a.stage_bytes;
   uint8_t* qw = q_all + warp * WS::kQ;
   uint8_t* xw = xch_all + warp * WS::kXch;
   const uint32_t xw_s = smem_addr(xw);
   const uint32_t bar0 = smem_addr(bars + warp * a.ns);
+  int* ring_w = reinterpret_cast<int*>(bars + nw * a.ns) + warp * a.ns;   // this warp's item ring
   const uint32_t blk_bytes = static_cast<uint32_t>(g.block_bytes);
 
-  if (threadIdx.x == 0) { s_arrive = 0u; s_done = 0u; }
+  if (threadIdx.x == 0) { s_arrive = 0u; s_done = 0u; s_next = 0u; }
   if (lane == 0) {
     for (int s = 0; s < a.ns; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
   __syncthreads();
 
-  auto warp_count = [&](int64_t lo, int64_t hi) -> int {
-    return (lo + warp < hi) ? static_cast<int>((hi - lo - warp + nw - 1) / nw) : 0;
-  };
-  auto unit_range = [&](int u, int64_t& lo, int64_t& hi) {
-    const int64_t base = static_cast<int64_t>(u) * a.uw;
-    lo = (c_start > base ? c_start : base) - base;
-    hi = (c_end < base + a.uw ? c_end : base + a.uw) - base;
-  };
   auto unit_base = [&](int u) -> const uint8_t* {
     const int per_b = g.hkv * a.npass;
     const int bb = u / per_b, hk = (u % per_b) / a.npass;
@@ -537,74 +532,85 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   };
 
   // ------------------------------------------------------------ producer
-  // per-warp copy pipeline over the warp's items of the whole range: per unit
-  // with work, the query rows, then the group blocks and tail chunks
+  // per-warp copy pipeline.  Lane 0 claims the CTA's positions one at a time
+  // from a shared counter (so a warp that is held up takes fewer), and before
+  // the first position of a unit it issues that unit's query rows; each item
+  // is noted in the warp's ring (one int per stage: 2 * rel for a position
+  // rel of the CTA's range, 2 * k + 1 for the query rows of unit u_first + k)
   const uint32_t n_slots = static_cast<uint32_t>(g.n_slots);
   const bool ring_slots = g.window > 0;
   const int t_sink = static_cast<int>(a.plan.st.n_sink), t_res = static_cast<int>(a.plan.st.n_res);
   const int rs0 = static_cast<int>((a.plan.st.n_groups * g.G) % g.R);   // ring slot of the oldest ring token
+  const int range = static_cast<int>(c_end - c_start);
   int c_st = 0;                 // consumer: stage, phase parity
   uint32_t c_ph = 0;
   int inflight = 0;             // items issued and not yet consumed (lane 0)
   int p_st = 0;                 // producer: next stage
-  int pu = u_first;             // producer: unit being issued
-  int p_left = -1;              // positions of unit pu still to issue (-1: unit not entered)
-  bool p_q = false;             // the query rows of unit pu are still to issue
-  int64_t p_pos = 0;            // next position (unit-local)
+  int p_u = -1;                 // unit (from u_first) of the last claimed position
+  bool p_have = false;          // a claimed position waits for a stage
+  bool p_q = false;             // the query rows of unit p_u wait for a stage
+  bool p_done = false;          // the CTA's positions are all claimed
+  int p_rel = 0;
+  int64_t p_end = static_cast<int64_t>(u_first) * a.uw;   // end of unit p_u's positions
   const uint8_t* p_unit = nullptr;
   bool aborted = false;
   auto produce = [&]() {
     if (lane != 0 || aborted) return;
     while (inflight < a.ns) {
-      if (!p_q && p_left <= 0) {
-        if (p_left == 0) ++pu;
-        if (pu > u_last) return;
-        int64_t lo, hi;
-        unit_range(pu, lo, hi);
-        p_left = warp_count(lo, hi);
-        p_pos = lo + warp;
-        p_unit = unit_base(pu);
-        if (p_left == 0) continue;
-        p_q = true;
+      if (!p_have) {
+        if (p_done) return;
+        const int rel = static_cast<int>(atomicAdd(&s_next, 1u));
+        if (rel >= range) { p_done = true; return; }
+        p_rel = rel;
+        p_have = true;
+        if (c_start + rel >= p_end) {   // the claim lies in a later unit (claims only grow)
+          do { ++p_u; p_end += a.uw; } while (c_start + rel >= p_end);
+          p_unit = unit_base(u_first + p_u);
+          p_q = true;
+        }
       }
       const uint32_t dst = smem_addr(my_stages + p_st * a.stage_bytes);
       const uint32_t bar = bar0 + 8 * p_st;
-      bool issued = true;
       if (p_q) {
-        int nh;
-        const __half* qsrc = unit_q(pu, nh);
-        bulk_load(dst, qsrc, static_cast<uint32_t>(nh) * D * 2, bar);
+        int nh_q;
+        const __half* qsrc = unit_q(u_first + p_u, nh_q);
+        ring_w[p_st] = 2 * p_u + 1;
+        bulk_load(dst, qsrc, static_cast<uint32_t>(nh_q) * D * 2, bar);
         p_q = false;
-      } else {
-        if (p_pos < n_vis) {   // a frozen group block
-          const uint32_t grp = static_cast<uint32_t>(a.plan.g_first + p_pos);
-          const uint32_t slot = ring_slots ? grp % n_slots : grp;
-          bulk_load(dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
-        } else {                // a tail chunk: key rows then value rows
-          const TailChunk tk = tail_chunk(static_cast<int>(p_pos - n_vis), t_sink, t_res);
-          if (tk.n == 0) {
-            issued = false;
-          } else if (tk.sink) {
-            const uint32_t bytes = static_cast<uint32_t>(tk.n) * D * 4;
-            bulk_arm(bar, 2 * bytes);
-            bulk_copy(dst, p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
-            bulk_copy(dst + 16 * D, p_unit + g.sink_v + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
-          } else {
-            int s0 = rs0 + tk.first;
-            if (s0 >= g.R) s0 -= g.R;
-            const int n1 = min(tk.n, g.R - s0), n2 = tk.n - n1;   // the ring may wrap
-            bulk_arm(bar, static_cast<uint32_t>(tk.n) * D * 4);
-            bulk_copy(dst, p_unit + g.res_k + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
-            bulk_copy(dst + 16 * D, p_unit + g.res_v + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
-            if (n2 > 0) {
-              bulk_copy(dst + n1 * D * 2, p_unit + g.res_k, n2 * D * 2, bar);
-              bulk_copy(dst + 16 * D + n1 * D * 2, p_unit + g.res_v, n2 * D * 2, bar);
-            }
+        if (++p_st == a.ns) p_st = 0;
+        ++inflight;
+        continue;
+      }
+      const int64_t pos = c_start + p_rel - static_cast<int64_t>(u_first + p_u) * a.uw;
+      bool issued = true;
+      ring_w[p_st] = 2 * p_rel;
+      if (pos < n_vis) {   // a frozen group block
+        const uint32_t grp = static_cast<uint32_t>(a.plan.g_first + pos);
+        const uint32_t slot = ring_slots ? grp % n_slots : grp;
+        bulk_load(dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
+      } else {                // a tail chunk: key rows then value rows
+        const TailChunk tk = tail_chunk(static_cast<int>(pos - n_vis), t_sink, t_res);
+        if (tk.n == 0) {
+          issued = false;     // nothing to copy or to attend to
+        } else if (tk.sink) {
+          const uint32_t bytes = static_cast<uint32_t>(tk.n) * D * 4;
+          bulk_arm(bar, 2 * bytes);
+          bulk_copy(dst, p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
+          bulk_copy(dst + 16 * D, p_unit + g.sink_v + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
+        } else {
+          int s0 = rs0 + tk.first;
+          if (s0 >= g.R) s0 -= g.R;
+          const int n1 = min(tk.n, g.R - s0), n2 = tk.n - n1;   // the ring may wrap
+          bulk_arm(bar, static_cast<uint32_t>(tk.n) * D * 4);
+          bulk_copy(dst, p_unit + g.res_k + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
+          bulk_copy(dst + 16 * D, p_unit + g.res_v + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
+          if (n2 > 0) {
+            bulk_copy(dst + n1 * D * 2, p_unit + g.res_k, n2 * D * 2, bar);
+            bulk_copy(dst + 16 * D + n1 * D * 2, p_unit + g.res_v, n2 * D * 2, bar);
           }
         }
-        p_pos += nw;
-        --p_left;
       }
+      p_have = false;
       if (issued) {
         if (++p_st == a.ns) p_st = 0;
         ++inflight;
@@ -641,344 +647,42 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   }
   const float sc_scale = qscale * kTwo24;
 
-  int useq = 0;   // units this CTA has combined so far (per warp, in step)
-  for (int u = u_first; u <= u_last; ++u, ++useq) {
-    int nh;
-    const __half* qsrc = unit_q(u, nh);
-    (void)qsrc;
-    int64_t lo_full, hi_full;
-    unit_range(u, lo_full, hi_full);
-    const int n_mine = warp_count(lo_full, hi_full);
-    const int64_t ubase = static_cast<int64_t>(u) * a.uw;
-    const int first = owner_of(ubase, W, P);
-    const int total = owner_of(ubase + a.uw - 1, W, P) - first + 1;
-    const int cslot = static_cast<int>(blockIdx.x) - first;
+  // ------------------------------------------------------------ consumer
+  const int nunits = u_last - u_first + 1;
+  int cu = -1;                  // open unit (from u_first); -1 before the first
+  int nh = 0, total = 1, cslot = 0;
+  int64_t u_base = 0;           // first position of the open unit
+  float res_m = -INFINITY, res_l = 0.f, res_mn = 0.f;
+  bool o_real = false;          // oacc holds real-scale values (after a tail chunk)
+  float oacc[NCT][4];
+#pragma unroll
+  for (int i = 0; i < NCT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  const uint8_t* qlane = qw + hh_col * WS::kQRow + c * WS::kQS;
 
-    float res_m = -INFINITY, res_l = 0.f, res_mn = 0.f;
-    bool o_real = false;   // oacc holds real-scale values (after a tail chunk)
-    float oacc[NCT][4];
+  auto open_unit = [&](int k) {
+    const int u = u_first + k;
+    (void)unit_q(u, nh);
+    u_base = static_cast<int64_t>(u) * a.uw;
+    const int first = owner_of(u_base, W, P);
+    total = owner_of(u_base + a.uw - 1, W, P) - first + 1;
+    cslot = static_cast<int>(blockIdx.x) - first;
+    res_m = -INFINITY; res_l = 0.f; res_mn = 0.f;
+    o_real = false;
 #pragma unroll
     for (int i = 0; i < NCT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
-
-    if (n_mine > 0) {
-      // ------------------------------------------------------ query rows
-      // copied to this warp's q area: quarter rows padded by 16 bytes, heads
-      // past nh zero
-      produce();
-      __syncwarp();
-      if (acquire()) {
-        const uint8_t* src = my_stages + c_st * a.stage_bytes;
-#pragma unroll
-        for (int k = lane; k < 4 * D / 8; k += 32) {
-          const int hh = k / (D / 8), idx = k % (D / 8);
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (hh < nh) v = *reinterpret_cast<const uint4*>(src + hh * D * 2 + idx * 16);
-          *reinterpret_cast<uint4*>(qw + hh * WS::kQRow + (idx / (QD / 8)) * WS::kQS + (idx % (QD / 8)) * 16) = v;
-        }
-        release();
-      }
-      __syncwarp();
-      const uint8_t* qlane = qw + hh_col * WS::kQRow + c * WS::kQS;
-
-      for (int t = 0; t < n_mine; ++t) {
-        const int64_t pos = lo_full + warp + static_cast<int64_t>(t) * nw;
-        produce();
-        __syncwarp();
-        if (pos < n_vis) {
-          // ------------------------------------------------ a frozen group
-          if (!acquire()) continue;
-          const int64_t grp = a.plan.g_first + pos;
-          const uint8_t* blk = my_stages + c_st * a.stage_bytes;
-
-          // (1) the query (natural pair order) and the folded B fragments:
-          // hi = fp16(q Δ) in even columns, lo = q Δ - hi in odd ones
-          uint32_t q2[NP];
-#pragma unroll
-          for (int i = 0; i < NP / 4; ++i) {
-            const uint4 v = reinterpret_cast<const uint4*>(qlane)[i];
-            q2[4 * i] = v.x; q2[4 * i + 1] = v.y; q2[4 * i + 2] = v.z; q2[4 * i + 3] = v.w;
-          }
-          const uint8_t* ks = blk + g.blk_ks;
-          uint32_t bq[NP];
-#pragma unroll
-          for (int i = 0; i < NP / 4; ++i) {
-            const uint4 dv = *reinterpret_cast<const uint4*>(ks + c * (D / 2) + 16 * i);
-            const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t hi = hmul2_u(q2[4 * i + j], dw[j]);
-              bq[4 * i + j] = hfma2_u(q2[4 * i + j], dw[j], (hi ^ 0x80008000u) & partmask);
-            }
-          }
-          // (2) Σ_c q_c min_c for every head, one MMA per k-chunk (column 2c = head c)
-          float cst[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < NP / 4; ++i) {
-            const uint4 mv = *reinterpret_cast<const uint4*>(ks + 2 * D + c * (D / 2) + 16 * i);
-            mma16816(cst, mv.x, mv.x, mv.y, mv.y, q2[4 * i], q2[4 * i + 1]);
-            mma16816(cst, mv.z, mv.z, mv.w, mv.w, q2[4 * i + 2], q2[4 * i + 3]);
-          }
-          const float cst_h = cst[0] * qscale;
-          const uint8_t* vsc = blk + g.blk_vs;
-          const int64_t a_grp = g.S + grp * g.G;
-
-          for (int s0 = 0; s0 < g.G; s0 += CH) {
-            // (3) scores: lane (r, c) gets head c's scores of tokens s0 + TPL*r + i
-            float sv[TPL];
-#pragma unroll
-            for (int v2 = 0; v2 < TPL / 2; ++v2) {
-              uint32_t w0[KW], w1[KW];
-              // 64-byte rows: odd r takes the pair's rows in swapped order so the
-              // two rows of a shared-memory phase fall in different bank halves
-              constexpr bool kSwap = (RK == 64);
-              const int sw = kSwap ? (r & 1) : 0;
-              const uint8_t* row0 = blk + g.blk_kq + (s0 + TPL * r + 2 * v2 + sw) * RK + c * (RK / 4);
-              const uint8_t* row1 = blk + g.blk_kq + (s0 + TPL * r + 2 * v2 + 1 - sw) * RK + c * (RK / 4);
-              if constexpr (KW >= 4) {
-#pragma unroll
-                for (int i = 0; i < KW; i += 4) {
-                  const uint4 x = *reinterpret_cast<const uint4*>(row0 + 4 * i);
-                  const uint4 y = *reinterpret_cast<const uint4*>(row1 + 4 * i);
-                  w0[i] = x.x; w0[i + 1] = x.y; w0[i + 2] = x.z; w0[i + 3] = x.w;
-                  w1[i] = y.x; w1[i + 1] = y.y; w1[i + 2] = y.z; w1[i + 3] = y.w;
-                }
-              } else if constexpr (KW == 2) {
-                const uint2 x = *reinterpret_cast<const uint2*>(row0);
-                const uint2 y = *reinterpret_cast<const uint2*>(row1);
-                w0[0] = x.x; w0[1] = x.y; w1[0] = y.x; w1[1] = y.y;
-              } else {
-                w0[0] = *reinterpret_cast<const uint32_t*>(row0);
-                w1[0] = *reinterpret_cast<const uint32_t*>(row1);
-              }
-              float acc[NA][4];
-#pragma unroll
-              for (int i = 0; i < NA; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-              for (int j = 0; j < NKC; ++j) {
-                const int pa = ord_pair<BITS, NP>(2 * j), pb = ord_pair<BITS, NP>(2 * j + 1);
-                mma16816(acc[acc_of<BITS, NP>(j)], code_pair<BITS>(w0, pa), code_pair<BITS>(w1, pa),
-                         code_pair<BITS>(w0, pb), code_pair<BITS>(w1, pb), bq[pa], bq[pb]);
-              }
-              float s_a = (acc[0][0] + acc[0][1]) * acc_scale<BITS>(0);
-              float s_b = (acc[0][2] + acc[0][3]) * acc_scale<BITS>(0);
-#pragma unroll
-              for (int i = 1; i < NA; ++i) {
-                s_a = fmaf(acc[i][0] + acc[i][1], acc_scale<BITS>(i), s_a);
-                s_b = fmaf(acc[i][2] + acc[i][3], acc_scale<BITS>(i), s_b);
-              }
-              s_a = fmaf(s_a, sc_scale, cst_h);
-              s_b = fmaf(s_b, sc_scale, cst_h);
-              sv[2 * v2] = sw ? s_b : s_a;
-              sv[2 * v2 + 1] = sw ? s_a : s_b;
-            }
-            if (g.window > 0) {   // tokens before T - W are invisible
-#pragma unroll
-              for (int i = 0; i < TPL; ++i)
-                if (a_grp + s0 + TPL * r + i < lo_pos) sv[i] = -INFINITY;
-            }
-            // (4) online softmax for head c, lazy rescale
-            float mx = sv[0];
-#pragma unroll
-            for (int i = 1; i < TPL; ++i) mx = fmaxf(mx, sv[i]);
-            mx = warp_max_rows(mx);
-            if (mx > res_m + kRescale) {   // uniform over the 8 lanes of head c
-              const float corr = (res_m == -INFINITY) ? 0.f : ex2(res_m - mx);
-              res_m = mx;
-              res_l *= corr;
-              res_mn *= corr;
-#pragma unroll
-              for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
-            }
-            const float mref = (res_m == -INFINITY) ? 0.f : res_m;   // every score so far -inf: p = 0
-            float pd[TPL];
-            {
-              float dm[2 * TPL];   // (Δ, min) of the lane's tokens
-              const __half2* vp = reinterpret_cast<const __half2*>(vsc) + s0 + TPL * r;
-              if constexpr (TPL == 4) {
-                const uint4 x = *reinterpret_cast<const uint4*>(vp);
-                const uint32_t xw4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw4[i]));
-                  dm[2 * i] = f.x; dm[2 * i + 1] = f.y;
-                }
-              } else {
-                const uint2 x = *reinterpret_cast<const uint2*>(vp);
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
-                dm[0] = f0.x; dm[1] = f0.y; dm[2] = f1.x; dm[3] = f1.y;
-              }
-#pragma unroll
-              for (int i = 0; i < TPL; ++i) {
-                const float p = ex2(sv[i] - mref);
-                res_l += p;
-                res_mn = fmaf(p, dm[2 * i + 1], res_mn);
-                pd[i] = p * dm[2 * i] * vscl[i];
-              }
-            }
-            // (5) P' hi/lo into the exchange buffer (head c, tokens TPL*r ..)
-            {
-              uint32_t hw[TPL / 2], lw[TPL / 2];
-#pragma unroll
-              for (int i = 0; i < TPL / 2; ++i) {
-                const float a0 = pd[2 * i], a1 = pd[2 * i + 1];
-                const float h0f = __uint_as_float(__float_as_uint(a0) & 0xFFFFE000u);
-                const float h1f = __uint_as_float(__float_as_uint(a1) & 0xFFFFE000u);
-                hw[i] = pack_half2(h0f, h1f);
-                lw[i] = pack_half2(a0 - h0f, a1 - h1f);
-              }
-              if constexpr (TPL == 4) {
-                *reinterpret_cast<uint2*>(xw + xch_off<CH>(c, 0, 4 * r)) = make_uint2(hw[0], hw[1]);
-                *reinterpret_cast<uint2*>(xw + xch_off<CH>(c, 1, 4 * r)) = make_uint2(lw[0], lw[1]);
-              } else {
-                *reinterpret_cast<uint32_t*>(xw + xch_off<CH>(c, 0, 2 * r)) = hw[0];
-                *reinterpret_cast<uint32_t*>(xw + xch_off<CH>(c, 1, 2 * r)) = lw[0];
-              }
-            }
-            __syncwarp();
-            // (6) Oᵀ += Vᵀ P': B = P' of tokens c*CH/4 + 4kcn + {0,1 | 2,3} in column r
-            uint32_t bp[NKT][2];
-            if constexpr (NKT == 2) {
-              const uint4 x = *reinterpret_cast<const uint4*>(xw + xch_off<CH>(hh_col, r & 1, 8 * c));
-              bp[0][0] = x.x; bp[0][1] = x.y; bp[1][0] = x.z; bp[1][1] = x.w;
-            } else {
-              const uint2 x = *reinterpret_cast<const uint2*>(xw + xch_off<CH>(hh_col, r & 1, 4 * c));
-              bp[0][0] = x.x; bp[0][1] = x.y;
-            }
-            const uint8_t* vq = blk + g.blk_vq + s0 * BITS / 8;
-            const int vrow = g.G * BITS / 8;
-#pragma unroll
-            for (int ct = 0; ct < NCT; ++ct) {
-              uint32_t v0[VW], v1[VW];
-              const uint8_t* rowa = vq + (16 * ct + r) * vrow;
-              const uint8_t* rowb = rowa + 8 * vrow;
-              if constexpr (QV >= 32) {
-#pragma unroll
-                for (int i = 0; i < VW; ++i) {
-                  v0[i] = reinterpret_cast<const uint32_t*>(rowa + c * (QV / 8))[i];
-                  v1[i] = reinterpret_cast<const uint32_t*>(rowb + c * (QV / 8))[i];
-                }
-              } else {
-                const int bitpos = c * QV;
-                const int sh = (bitpos % 32) / 2;
-                v0[0] = reinterpret_cast<const uint32_t*>(rowa)[bitpos / 32] >> sh;
-                v1[0] = reinterpret_cast<const uint32_t*>(rowb)[bitpos / 32] >> sh;
-              }
-#pragma unroll
-              for (int kcn = 0; kcn < NKT; ++kcn) {
-                mma16816(oacc[ct], code_pair<BITS>(v0, 2 * kcn), code_pair<BITS>(v1, 2 * kcn),
-                         code_pair<BITS>(v0, 2 * kcn + 1), code_pair<BITS>(v1, 2 * kcn + 1), bp[kcn][0], bp[kcn][1]);
-              }
-            }
-            __syncwarp();
-          }
-          release();
-        } else {
-          // ------------------------------------------------ a tail chunk
-          const TailChunk tk = tail_chunk(static_cast<int>(pos - n_vis), t_sink, t_res);
-          if (tk.n == 0) continue;
-          if (!acquire()) continue;
-          const uint8_t* kst = my_stages + c_st * a.stage_bytes;
-          const uint8_t* vst = kst + 16 * D;
-          if (!o_real) {   // from here on oacc holds real-scale values
-#pragma unroll
-            for (int i = 0; i < NCT; ++i) { oacc[i][0] *= kTwo24; oacc[i][1] *= kTwo24; oacc[i][2] *= kTwo24; oacc[i][3] *= kTwo24; }
-            o_real = true;
-          }
-          uint32_t q2[NP];
-#pragma unroll
-          for (int i = 0; i < NP / 4; ++i) {
-            const uint4 v = reinterpret_cast<const uint4*>(qlane)[i];
-            q2[4 * i] = v.x; q2[4 * i + 1] = v.y; q2[4 * i + 2] = v.z; q2[4 * i + 3] = v.w;
-          }
-          // keys of token r (zero past the chunk), natural pair order of quarter c
-          uint32_t ka[NP];
-          if (r < tk.n) {
-            if (tk.sink) {
-              const float* kr = reinterpret_cast<const float*>(kst) + r * D + c * QD;
-#pragma unroll
-              for (int i = 0; i < NP / 2; ++i) {
-                const float4 f = reinterpret_cast<const float4*>(kr)[i];
-                ka[2 * i] = pack_half2(f.x, f.y);
-                ka[2 * i + 1] = pack_half2(f.z, f.w);
-              }
-            } else {
-              const uint8_t* kr = kst + (r * D + c * QD) * 2;
-#pragma unroll
-              for (int i = 0; i < NP / 4; ++i) {
-                const uint4 v = reinterpret_cast<const uint4*>(kr)[i];
-                ka[4 * i] = v.x; ka[4 * i + 1] = v.y; ka[4 * i + 2] = v.z; ka[4 * i + 3] = v.w;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < NP; ++i) ka[i] = 0u;
-          }
-          // scores: rows r = tokens, column 2c = head c (every column holds its head's q)
-          float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < NKC; ++j) {
-            if (j & 1) mma16816(acc1, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
-            else       mma16816(acc0, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
-          }
-          const float s = (r < tk.n) ? (acc0[0] + acc1[0]) * qscale : -INFINITY;
-          const float mx = warp_max_rows(s);   // finite: the chunk holds a token
-          if (mx > res_m + kRescale) {
-            const float corr = (res_m == -INFINITY) ? 0.f : ex2(res_m - mx);
-            res_m = mx;
-            res_l *= corr;
-            res_mn *= corr;
-#pragma unroll
-            for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
-          }
-          const float p = ex2(s - res_m);
-          res_l += p;
-          {
-            const float h = __uint_as_float(__float_as_uint(p) & 0xFFFFE000u);
-            const __half hh = __float2half_rn(h), ll = __float2half_rn(p - h);
-            *reinterpret_cast<__half*>(xw + xch_off<CH>(c, 0, r)) = hh;
-            *reinterpret_cast<__half*>(xw + xch_off<CH>(c, 1, r)) = ll;
-          }
-          __syncwarp();
-          // Oᵀ += Vᵀ P': B = P' of tokens 2c, 2c + 1 in column r (tokens 8.. are absent)
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xw + xch_off<CH>(hh_col, r & 1, 2 * c));
-          const uint32_t tmask = (2 * c < tk.n ? 0x0000FFFFu : 0u) | (2 * c + 1 < tk.n ? 0xFFFF0000u : 0u);
-          if (tk.sink) {
-            const float* vr = reinterpret_cast<const float*>(vst);
-#pragma unroll
-            for (int ct = 0; ct < NCT; ++ct) {
-              uint32_t a0 = 0u, a1 = 0u;
-              if (2 * c < tk.n) {
-                const float* v0r = vr + (2 * c) * D + 16 * ct + r;
-                const float x0 = v0r[0], y0 = (2 * c + 1 < tk.n) ? v0r[D] : 0.f;
-                const float x1 = v0r[8], y1 = (2 * c + 1 < tk.n) ? v0r[D + 8] : 0.f;
-                a0 = pack_half2(x0, y0);
-                a1 = pack_half2(x1, y1);
-              }
-              mma16816(oacc[ct], a0, a1, 0u, 0u, b0, 0u);
-            }
-          } else {
-            const uint32_t vbase = smem_addr(vst) + (lane & 7) * D * 2 + ((lane >> 3) & 1) * 16;
-#pragma unroll
-            for (int ct = 0; ct < NCT; ++ct) {
-              uint32_t a0, a1;
-              ldsm_x2_trans(a0, a1, vbase + 32 * ct);
-              mma16816(oacc[ct], a0 & tmask, a1 & tmask, 0u, 0u, b0, 0u);
-            }
-          }
-          release();
-        }
-      }
-    }
-
-    // ------------------------------------------------------ warp -> slot
+  };
+  // the warp's state of unit cu into its slot, then the sign-in: the last warp
+  // combines a unit that is not the CTA's last while the others stream on; the
+  // CTA's last unit is combined by every thread once all streaming is over
+  auto close_unit = [&]() {
+    const int u = u_first + cu;
     float lh = warp_sum_rows(res_l), mh = warp_sum_rows(res_mn);
     // the slot may be rewritten once the combine of the previous unit is done
     if (lane == 0) {
       const volatile unsigned* done = &s_done;
-      if (*done < static_cast<unsigned>(useq)) {
+      if (*done < static_cast<unsigned>(cu)) {
         const unsigned long long t0 = global_ns();
-        while (*done < static_cast<unsigned>(useq)) {
+        while (*done < static_cast<unsigned>(cu)) {
           __nanosleep(64);
           if (global_ns() - t0 > kWaitNs) { atomicOr(a.error, kErrSlot); break; }
         }
@@ -997,23 +701,340 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         so[16 * ct + r + 8] = fmaf(oacc[ct][2] + oacc[ct][3], osc, mh);
       }
     }
-    if (u != u_last) {
+    if (cu != nunits - 1) {
       __threadfence_block();
       __syncwarp();
       unsigned last = 0;
       if (lane == 0) last = (atomicAdd(&s_arrive, 1u) == static_cast<unsigned>(nw - 1)) ? 1u : 0u;
       last = __shfl_sync(0xffffffffu, last, 0);
-      if (!last) continue;
-      // the last warp to sign in combines the unit while the others stream on
-      __threadfence_block();
-      if (lane == 0) s_arrive = 0u;
-      warp_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, useq, &s_done);
+      if (last) {
+        __threadfence_block();
+        if (lane == 0) s_arrive = 0u;
+        warp_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, cu, &s_done);
+      }
+    } else {
+      __syncthreads();
+      cta_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, &s_flag);
+    }
+  };
+
+  for (;;) {
+    produce();
+    __syncwarp();
+    if (__shfl_sync(0xffffffffu, inflight, 0) == 0) break;   // every claim issued and consumed
+    if (!acquire()) break;
+    const int item = *reinterpret_cast<volatile int*>(ring_w + c_st);
+    if (item & 1) {
+      // ------------------------------------------------------ query rows
+      // of the next unit this warp works on; units passed on the way are closed
+      const int k = item >> 1;
+      while (cu < k) {
+        if (cu >= 0) close_unit();
+        ++cu;
+        open_unit(cu);
+      }
+      // copied to this warp's q area: quarter rows padded by 16 bytes, heads
+      // past nh zero
+      const uint8_t* src = my_stages + c_st * a.stage_bytes;
+#pragma unroll
+      for (int kk = lane; kk < 4 * D / 8; kk += 32) {
+        const int hh = kk / (D / 8), idx = kk % (D / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (hh < nh) v = *reinterpret_cast<const uint4*>(src + hh * D * 2 + idx * 16);
+        *reinterpret_cast<uint4*>(qw + hh * WS::kQRow + (idx / (QD / 8)) * WS::kQS + (idx % (QD / 8)) * 16) = v;
+      }
+      release();
+      __syncwarp();
       continue;
     }
-    // the CTA's last unit: nothing is left to stream, so every thread takes part
-    __syncthreads();
-    cta_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, &s_flag);
-    break;
+    const int64_t pos = c_start + (item >> 1) - u_base;   // position inside the open unit
+    if (pos < n_vis) {
+      // ------------------------------------------------------ a frozen group
+      const int64_t grp = a.plan.g_first + pos;
+      const uint8_t* blk = my_stages + c_st * a.stage_bytes;
+
+      // (1) the query (natural pair order) and the folded B fragments:
+      // hi = fp16(q Δ) in even columns, lo = q Δ - hi in odd ones
+      uint32_t q2[NP];
+#pragma unroll
+      for (int i = 0; i < NP / 4; ++i) {
+        const uint4 v = reinterpret_cast<const uint4*>(qlane)[i];
+        q2[4 * i] = v.x; q2[4 * i + 1] = v.y; q2[4 * i + 2] = v.z; q2[4 * i + 3] = v.w;
+      }
+      const uint8_t* ks = blk + g.blk_ks;
+      uint32_t bq[NP];
+#pragma unroll
+      for (int i = 0; i < NP / 4; ++i) {
+        const uint4 dv = *reinterpret_cast<const uint4*>(ks + c * (D / 2) + 16 * i);
+        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t hi = hmul2_u(q2[4 * i + j], dw[j]);
+          bq[4 * i + j] = hfma2_u(q2[4 * i + j], dw[j], (hi ^ 0x80008000u) & partmask);
+        }
+      }
+      // (2) Σ_c q_c min_c for every head, one MMA per k-chunk (column 2c = head c)
+      float cst[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < NP / 4; ++i) {
+        const uint4 mv = *reinterpret_cast<const uint4*>(ks + 2 * D + c * (D / 2) + 16 * i);
+        mma16816(cst, mv.x, mv.x, mv.y, mv.y, q2[4 * i], q2[4 * i + 1]);
+        mma16816(cst, mv.z, mv.z, mv.w, mv.w, q2[4 * i + 2], q2[4 * i + 3]);
+      }
+      const float cst_h = cst[0] * qscale;
+      const uint8_t* vsc = blk + g.blk_vs;
+      const int64_t a_grp = g.S + grp * g.G;
+
+      for (int s0 = 0; s0 < g.G; s0 += CH) {
+        // (3) scores: lane (r, c) gets head c's scores of tokens s0 + TPL*r + i
+        float sv[TPL];
+#pragma unroll
+        for (int v2 = 0; v2 < TPL / 2; ++v2) {
+          uint32_t w0[KW], w1[KW];
+          // 64-byte rows: odd r takes the pair's rows in swapped order so the
+          // two rows of a shared-memory phase fall in different bank halves
+          constexpr bool kSwap = (RK == 64);
+          const int sw = kSwap ? (r & 1) : 0;
+          const uint8_t* row0 = blk + g.blk_kq + (s0 + TPL * r + 2 * v2 + sw) * RK + c * (RK / 4);
+          const uint8_t* row1 = blk + g.blk_kq + (s0 + TPL * r + 2 * v2 + 1 - sw) * RK + c * (RK / 4);
+          if constexpr (KW >= 4) {
+#pragma unroll
+            for (int i = 0; i < KW; i += 4) {
+              const uint4 x = *reinterpret_cast<const uint4*>(row0 + 4 * i);
+              const uint4 y = *reinterpret_cast<const uint4*>(row1 + 4 * i);
+              w0[i] = x.x; w0[i + 1] = x.y; w0[i + 2] = x.z; w0[i + 3] = x.w;
+              w1[i] = y.x; w1[i + 1] = y.y; w1[i + 2] = y.z; w1[i + 3] = y.w;
+            }
+          } else if constexpr (KW == 2) {
+            const uint2 x = *reinterpret_cast<const uint2*>(row0);
+            const uint2 y = *reinterpret_cast<const uint2*>(row1);
+            w0[0] = x.x; w0[1] = x.y; w1[0] = y.x; w1[1] = y.y;
+          } else {
+            w0[0] = *reinterpret_cast<const uint32_t*>(row0);
+            w1[0] = *reinterpret_cast<const uint32_t*>(row1);
+          }
+          float acc[NA][4];
+#pragma unroll
+          for (int i = 0; i < NA; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+          for (int j = 0; j < NKC; ++j) {
+            const int pa = ord_pair<BITS, NP>(2 * j), pb = ord_pair<BITS, NP>(2 * j + 1);
+            mma16816(acc[acc_of<BITS, NP>(j)], code_pair<BITS>(w0, pa), code_pair<BITS>(w1, pa),
+                     code_pair<BITS>(w0, pb), code_pair<BITS>(w1, pb), bq[pa], bq[pb]);
+          }
+          float s_a = (acc[0][0] + acc[0][1]) * acc_scale<BITS>(0);
+          float s_b = (acc[0][2] + acc[0][3]) * acc_scale<BITS>(0);
+#pragma unroll
+          for (int i = 1; i < NA; ++i) {
+            s_a = fmaf(acc[i][0] + acc[i][1], acc_scale<BITS>(i), s_a);
+            s_b = fmaf(acc[i][2] + acc[i][3], acc_scale<BITS>(i), s_b);
+          }
+          s_a = fmaf(s_a, sc_scale, cst_h);
+          s_b = fmaf(s_b, sc_scale, cst_h);
+          sv[2 * v2] = sw ? s_b : s_a;
+          sv[2 * v2 + 1] = sw ? s_a : s_b;
+        }
+        if (g.window > 0) {   // tokens before T - W are invisible
+#pragma unroll
+          for (int i = 0; i < TPL; ++i)
+            if (a_grp + s0 + TPL * r + i < lo_pos) sv[i] = -INFINITY;
+        }
+        // (4) online softmax for head c, lazy rescale
+        float mx = sv[0];
+#pragma unroll
+        for (int i = 1; i < TPL; ++i) mx = fmaxf(mx, sv[i]);
+        mx = warp_max_rows(mx);
+        if (mx > res_m + kRescale) {   // uniform over the 8 lanes of head c
+          const float corr = (res_m == -INFINITY) ? 0.f : ex2(res_m - mx);
+          res_m = mx;
+          res_l *= corr;
+          res_mn *= corr;
+#pragma unroll
+          for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
+        }
+        const float mref = (res_m == -INFINITY) ? 0.f : res_m;   // every score so far -inf: p = 0
+        float pd[TPL];
+        {
+          float dm[2 * TPL];   // (Δ, min) of the lane's tokens
+          const __half2* vp = reinterpret_cast<const __half2*>(vsc) + s0 + TPL * r;
+          if constexpr (TPL == 4) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vp);
+            const uint32_t xw4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw4[i]));
+              dm[2 * i] = f.x; dm[2 * i + 1] = f.y;
+            }
+          } else {
+            const uint2 x = *reinterpret_cast<const uint2*>(vp);
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
+            dm[0] = f0.x; dm[1] = f0.y; dm[2] = f1.x; dm[3] = f1.y;
+          }
+#pragma unroll
+          for (int i = 0; i < TPL; ++i) {
+            const float p = ex2(sv[i] - mref);
+            res_l += p;
+            res_mn = fmaf(p, dm[2 * i + 1], res_mn);
+            pd[i] = p * dm[2 * i] * vscl[i];
+          }
+        }
+        // (5) P' hi/lo into the exchange buffer (head c, tokens TPL*r ..)
+        {
+          uint32_t hw[TPL / 2], lw[TPL / 2];
+#pragma unroll
+          for (int i = 0; i < TPL / 2; ++i) {
+            const float a0 = pd[2 * i], a1 = pd[2 * i + 1];
+            const float h0f = __uint_as_float(__float_as_uint(a0) & 0xFFFFE000u);
+            const float h1f = __uint_as_float(__float_as_uint(a1) & 0xFFFFE000u);
+            hw[i] = pack_half2(h0f, h1f);
+            lw[i] = pack_half2(a0 - h0f, a1 - h1f);
+          }
+          if constexpr (TPL == 4) {
+            *reinterpret_cast<uint2*>(xw + xch_off<CH>(c, 0, 4 * r)) = make_uint2(hw[0], hw[1]);
+            *reinterpret_cast<uint2*>(xw + xch_off<CH>(c, 1, 4 * r)) = make_uint2(lw[0], lw[1]);
+          } else {
+            *reinterpret_cast<uint32_t*>(xw + xch_off<CH>(c, 0, 2 * r)) = hw[0];
+            *reinterpret_cast<uint32_t*>(xw + xch_off<CH>(c, 1, 2 * r)) = lw[0];
+          }
+        }
+        __syncwarp();
+        // (6) Oᵀ += Vᵀ P': B = P' of tokens c*CH/4 + 4kcn + {0,1 | 2,3} in column r
+        uint32_t bp[NKT][2];
+        if constexpr (NKT == 2) {
+          const uint4 x = *reinterpret_cast<const uint4*>(xw + xch_off<CH>(hh_col, r & 1, 8 * c));
+          bp[0][0] = x.x; bp[0][1] = x.y; bp[1][0] = x.z; bp[1][1] = x.w;
+        } else {
+          const uint2 x = *reinterpret_cast<const uint2*>(xw + xch_off<CH>(hh_col, r & 1, 4 * c));
+          bp[0][0] = x.x; bp[0][1] = x.y;
+        }
+        const uint8_t* vq = blk + g.blk_vq + s0 * BITS / 8;
+        const int vrow = g.G * BITS / 8;
+#pragma unroll
+        for (int ct = 0; ct < NCT; ++ct) {
+          uint32_t v0[VW], v1[VW];
+          const uint8_t* rowa = vq + (16 * ct + r) * vrow;
+          const uint8_t* rowb = rowa + 8 * vrow;
+          if constexpr (QV >= 32) {
+#pragma unroll
+            for (int i = 0; i < VW; ++i) {
+              v0[i] = reinterpret_cast<const uint32_t*>(rowa + c * (QV / 8))[i];
+              v1[i] = reinterpret_cast<const uint32_t*>(rowb + c * (QV / 8))[i];
+            }
+          } else {
+            const int bitpos = c * QV;
+            const int sh = (bitpos % 32) / 2;
+            v0[0] = reinterpret_cast<const uint32_t*>(rowa)[bitpos / 32] >> sh;
+            v1[0] = reinterpret_cast<const uint32_t*>(rowb)[bitpos / 32] >> sh;
+          }
+#pragma unroll
+          for (int kcn = 0; kcn < NKT; ++kcn) {
+            mma16816(oacc[ct], code_pair<BITS>(v0, 2 * kcn), code_pair<BITS>(v1, 2 * kcn),
+                     code_pair<BITS>(v0, 2 * kcn + 1), code_pair<BITS>(v1, 2 * kcn + 1), bp[kcn][0], bp[kcn][1]);
+          }
+        }
+        __syncwarp();
+      }
+      release();
+    } else {
+      // ------------------------------------------------------ a tail chunk
+      const TailChunk tk = tail_chunk(static_cast<int>(pos - n_vis), t_sink, t_res);
+      const uint8_t* kst = my_stages + c_st * a.stage_bytes;
+      const uint8_t* vst = kst + 16 * D;
+      if (!o_real) {   // from here on oacc holds real-scale values
+#pragma unroll
+        for (int i = 0; i < NCT; ++i) { oacc[i][0] *= kTwo24; oacc[i][1] *= kTwo24; oacc[i][2] *= kTwo24; oacc[i][3] *= kTwo24; }
+        o_real = true;
+      }
+      uint32_t q2[NP];
+#pragma unroll
+      for (int i = 0; i < NP / 4; ++i) {
+        const uint4 v = reinterpret_cast<const uint4*>(qlane)[i];
+        q2[4 * i] = v.x; q2[4 * i + 1] = v.y; q2[4 * i + 2] = v.z; q2[4 * i + 3] = v.w;
+      }
+      // keys of token r (zero past the chunk), natural pair order of quarter c
+      uint32_t ka[NP];
+      if (r < tk.n) {
+        if (tk.sink) {
+          const float* kr = reinterpret_cast<const float*>(kst) + r * D + c * QD;
+#pragma unroll
+          for (int i = 0; i < NP / 2; ++i) {
+            const float4 f = reinterpret_cast<const float4*>(kr)[i];
+            ka[2 * i] = pack_half2(f.x, f.y);
+            ka[2 * i + 1] = pack_half2(f.z, f.w);
+          }
+        } else {
+          const uint8_t* kr = kst + (r * D + c * QD) * 2;
+#pragma unroll
+          for (int i = 0; i < NP / 4; ++i) {
+            const uint4 v = reinterpret_cast<const uint4*>(kr)[i];
+            ka[4 * i] = v.x; ka[4 * i + 1] = v.y; ka[4 * i + 2] = v.z; ka[4 * i + 3] = v.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) ka[i] = 0u;
+      }
+      // scores: rows r = tokens, column 2c = head c (every column holds its head's q)
+      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < NKC; ++j) {
+        if (j & 1) mma16816(acc1, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
+        else       mma16816(acc0, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
+      }
+      const float s = (r < tk.n) ? (acc0[0] + acc1[0]) * qscale : -INFINITY;
+      const float mx = warp_max_rows(s);   // finite: the chunk holds a token
+      if (mx > res_m + kRescale) {
+        const float corr = (res_m == -INFINITY) ? 0.f : ex2(res_m - mx);
+        res_m = mx;
+        res_l *= corr;
+        res_mn *= corr;
+#pragma unroll
+        for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
+      }
+      const float p = ex2(s - res_m);
+      res_l += p;
+      {
+        const float h = __uint_as_float(__float_as_uint(p) & 0xFFFFE000u);
+        const __half hh = __float2half_rn(h), ll = __float2half_rn(p - h);
+        *reinterpret_cast<__half*>(xw + xch_off<CH>(c, 0, r)) = hh;
+        *reinterpret_cast<__half*>(xw + xch_off<CH>(c, 1, r)) = ll;
+      }
+      __syncwarp();
+      // Oᵀ += Vᵀ P': B = P' of tokens 2c, 2c + 1 in column r (tokens 8.. are absent)
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xw + xch_off<CH>(hh_col, r & 1, 2 * c));
+      const uint32_t tmask = (2 * c < tk.n ? 0x0000FFFFu : 0u) | (2 * c + 1 < tk.n ? 0xFFFF0000u : 0u);
+      if (tk.sink) {
+        const float* vr = reinterpret_cast<const float*>(vst);
+#pragma unroll
+        for (int ct = 0; ct < NCT; ++ct) {
+          uint32_t a0 = 0u, a1 = 0u;
+          if (2 * c < tk.n) {
+            const float* v0r = vr + (2 * c) * D + 16 * ct + r;
+            const float x0 = v0r[0], y0 = (2 * c + 1 < tk.n) ? v0r[D] : 0.f;
+            const float x1 = v0r[8], y1 = (2 * c + 1 < tk.n) ? v0r[D + 8] : 0.f;
+            a0 = pack_half2(x0, y0);
+            a1 = pack_half2(x1, y1);
+          }
+          mma16816(oacc[ct], a0, a1, 0u, 0u, b0, 0u);
+        }
+      } else {
+        const uint32_t vbase = smem_addr(vst) + (lane & 7) * D * 2 + ((lane >> 3) & 1) * 16;
+#pragma unroll
+        for (int ct = 0; ct < NCT; ++ct) {
+          uint32_t a0, a1;
+          ldsm_x2_trans(a0, a1, vbase + 32 * ct);
+          mma16816(oacc[ct], a0 & tmask, a1 & tmask, 0u, 0u, b0, 0u);
+        }
+      }
+      release();
+    }
+  }
+  // the units not closed yet: the warp's last one, then those it had no work in
+  while (cu < nunits) {
+    if (cu >= 0) close_unit();
+    ++cu;
+    if (cu < nunits) open_unit(cu);
   }
 
   // drain this warp's copies still in flight (only after an abort), bounded
