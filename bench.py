@@ -340,7 +340,7 @@ def run_e2e(args, caches, new_kv, w, device, stream):
 
 
 # --------------------------------------------------------------- oracle arm
-def oracle_sample(w, units_max, seed=0):
+def oracle_sample(w, units_max, seed=0, extra=4096):
     """An oracle cache holding a bounded sample of the workload: the first
     `units` (sequence, kv head) units, built from the same generator."""
     import numpy as np
@@ -352,7 +352,7 @@ def oracle_sample(w, units_max, seed=0):
     bs = max(1, units // hk)
     ws = w.with_(batch=bs, h_kv=hk, h_q=hk * rep)
     p = oracle.Params(bits=w.bits, group=w.group, residual=w.residual, sinks=w.sinks, h_q=ws.h_q, h_kv=ws.h_kv,
-                      head_dim=w.head_dim, batch=ws.batch, max_tokens=0 if w.window else w.tokens + 4096,
+                      head_dim=w.head_dim, batch=ws.batch, max_tokens=0 if w.window else w.tokens + extra,
                       window=w.window)
     c = oracle.Cache(p)
     kv = KVStream(ws, device="cpu")
@@ -365,20 +365,28 @@ def oracle_sample(w, units_max, seed=0):
     return c, ws, kv
 
 
-def time_oracle(w, budget_s=12.0, units_max=None):
+def time_oracle(w, budget_s=12.0, units_max=None, steps_exact=None, warmup=0):
+    """The oracle on the host cores over a bounded sample of the workload:
+    steps of (append one token + fp64 decode).  With steps_exact, `warmup`
+    untimed steps then exactly that many timed ones; else timed steps until
+    about budget_s seconds (at most 50)."""
     import numpy as np
     import torch
     from kivi_quantized_kv_gb300.synth import queries
     cores = os.cpu_count() or 1
     units_max = units_max or max(cores * 2, 8)
     t_build = time.perf_counter()
-    c, ws, kv = oracle_sample(w, units_max)
+    c, ws, kv = oracle_sample(w, units_max, extra=max(4096, (steps_exact or 50) + warmup + 64))
     t_build = time.perf_counter() - t_build
     q = queries(ws).numpy()
+    for _ in range(warmup if steps_exact else 0):
+        k, v = kv.next(1)
+        c.append(k.numpy(), v.numpy())
+        c.decode_attn(q, threads=cores)
     steps = 0
     total = 0
     tt = 0.0
-    while tt < budget_s and steps < 50:
+    while (steps < steps_exact) if steps_exact else (tt < budget_s and steps < 50):
         k, v = kv.next(1)
         t0 = time.perf_counter()
         c.append(k.numpy(), v.numpy())
@@ -402,7 +410,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        base = time_oracle(w, budget_s=min(20.0, 2.0 + 0.2 * args.steps))
+        base = time_oracle(w, steps_exact=args.steps, warmup=args.warmup)
         line = {"metric": METRIC, "value": base["value"], "unit": "GB/s", "n_gpus": args.gpus, "steps": base["steps"],
                 "warmup": args.warmup, "ms_per_step": round(base["seconds"] * 1e3 / max(base["steps"], 1), 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
