@@ -144,6 +144,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
                : "=r"(done) : "r"(bar), "r"(parity) : "memory");
   return done != 0;
 }
+// The same, but a thread whose phase is not complete is suspended (issuing
+// nothing) until it completes or about `hint_ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(done) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+  return done != 0;
+}
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -151,20 +161,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Waits for a barrier phase; gives up after kWaitNs and reports false.
+// Waits for a barrier phase, suspended rather than spinning (a spinning warp
+// would take issue slots from the warps that compute); gives up after
+// kWaitNs and reports false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     if (global_ns() - t0 > kWaitNs) return false;
   }
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
                "{%0,%1,%2,%3};\n"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -176,6 +187,25 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ void ldsm_x2_trans(uint32_t& r0, uint32_t& r1, uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
                : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
+}
+
+// Shared-memory loads at 32-bit shared addresses (ordered like other memory
+// operations: the stage they read is handed back to the copy engine later).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -542,29 +572,38 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const int t_sink = static_cast<int>(a.plan.st.n_sink), t_res = static_cast<int>(a.plan.st.n_res);
   const int rs0 = static_cast<int>((a.plan.st.n_groups * g.G) % g.R);   // ring slot of the oldest ring token
   const int range = static_cast<int>(c_end - c_start);
+  // slot of the first visible group (ring of slots with a window); a unit's
+  // visible groups never outnumber its slots
+  const uint32_t slot0 = ring_slots ? static_cast<uint32_t>(a.plan.g_first % g.n_slots)
+                                    : static_cast<uint32_t>(a.plan.g_first);
   int c_st = 0;                 // consumer: stage, phase parity
   uint32_t c_ph = 0;
-  int inflight = 0;             // items issued and not yet consumed (lane 0)
+  int inflight = 0;             // items issued and not yet consumed (warp-uniform)
   int p_st = 0;                 // producer: next stage
   int p_u = -1;                 // unit (from u_first) of the last claimed position
   bool p_have = false;          // a claimed position waits for a stage
   bool p_q = false;             // the query rows of unit p_u wait for a stage
   bool p_done = false;          // the CTA's positions are all claimed
   int p_rel = 0;
-  int64_t p_end = static_cast<int64_t>(u_first) * a.uw;   // end of unit p_u's positions
+  // end of unit p_u's positions, relative to c_start (negative or zero before the first claim)
+  int p_end = static_cast<int>(static_cast<int64_t>(u_first) * a.uw - c_start);
   const uint8_t* p_unit = nullptr;
   bool aborted = false;
+  // the whole warp runs the bookkeeping on warp-uniform values; lane 0 alone
+  // claims, notes the item and issues the copies
   auto produce = [&]() {
-    if (lane != 0 || aborted) return;
+    if (aborted) return;
     while (inflight < a.ns) {
       if (!p_have) {
         if (p_done) return;
-        const int rel = static_cast<int>(atomicAdd(&s_next, 1u));
+        int rel = 0;
+        if (lane == 0) rel = static_cast<int>(atomicAdd(&s_next, 1u));
+        rel = __shfl_sync(0xffffffffu, rel, 0);
         if (rel >= range) { p_done = true; return; }
         p_rel = rel;
         p_have = true;
-        if (c_start + rel >= p_end) {   // the claim lies in a later unit (claims only grow)
-          do { ++p_u; p_end += a.uw; } while (c_start + rel >= p_end);
+        if (rel >= p_end) {   // the claim lies in a later unit (claims only grow)
+          do { ++p_u; p_end += a.uw; } while (rel >= p_end);
           p_unit = unit_base(u_first + p_u);
           p_q = true;
         }
@@ -574,39 +613,46 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       if (p_q) {
         int nh_q;
         const __half* qsrc = unit_q(u_first + p_u, nh_q);
-        ring_w[p_st] = 2 * p_u + 1;
-        bulk_load(dst, qsrc, static_cast<uint32_t>(nh_q) * D * 2, bar);
+        if (lane == 0) {
+          ring_w[p_st] = 2 * p_u + 1;
+          bulk_load(dst, qsrc, static_cast<uint32_t>(nh_q) * D * 2, bar);
+        }
         p_q = false;
         if (++p_st == a.ns) p_st = 0;
         ++inflight;
         continue;
       }
-      const int64_t pos = c_start + p_rel - static_cast<int64_t>(u_first + p_u) * a.uw;
+      const int pos = p_rel - (p_end - static_cast<int>(a.uw));   // position inside unit p_u
       bool issued = true;
-      ring_w[p_st] = 2 * p_rel;
       if (pos < n_vis) {   // a frozen group block
-        const uint32_t grp = static_cast<uint32_t>(a.plan.g_first + pos);
-        const uint32_t slot = ring_slots ? grp % n_slots : grp;
-        bulk_load(dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
+        uint32_t slot = slot0 + static_cast<uint32_t>(pos);
+        if (ring_slots && slot >= n_slots) slot -= n_slots;
+        if (lane == 0) {
+          ring_w[p_st] = 2 * p_rel;
+          bulk_load(dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
+        }
       } else {                // a tail chunk: key rows then value rows
-        const TailChunk tk = tail_chunk(static_cast<int>(pos - n_vis), t_sink, t_res);
+        const TailChunk tk = tail_chunk(pos - static_cast<int>(n_vis), t_sink, t_res);
         if (tk.n == 0) {
           issued = false;     // nothing to copy or to attend to
-        } else if (tk.sink) {
-          const uint32_t bytes = static_cast<uint32_t>(tk.n) * D * 4;
-          bulk_arm(bar, 2 * bytes);
-          bulk_copy(dst, p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
-          bulk_copy(dst + 16 * D, p_unit + g.sink_v + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
-        } else {
-          int s0 = rs0 + tk.first;
-          if (s0 >= g.R) s0 -= g.R;
-          const int n1 = min(tk.n, g.R - s0), n2 = tk.n - n1;   // the ring may wrap
-          bulk_arm(bar, static_cast<uint32_t>(tk.n) * D * 4);
-          bulk_copy(dst, p_unit + g.res_k + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
-          bulk_copy(dst + 16 * D, p_unit + g.res_v + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
-          if (n2 > 0) {
-            bulk_copy(dst + n1 * D * 2, p_unit + g.res_k, n2 * D * 2, bar);
-            bulk_copy(dst + 16 * D + n1 * D * 2, p_unit + g.res_v, n2 * D * 2, bar);
+        } else if (lane == 0) {
+          ring_w[p_st] = 2 * p_rel;
+          if (tk.sink) {
+            const uint32_t bytes = static_cast<uint32_t>(tk.n) * D * 4;
+            bulk_arm(bar, 2 * bytes);
+            bulk_copy(dst, p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
+            bulk_copy(dst + 16 * D, p_unit + g.sink_v + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
+          } else {
+            int s0 = rs0 + tk.first;
+            if (s0 >= g.R) s0 -= g.R;
+            const int n1 = min(tk.n, g.R - s0), n2 = tk.n - n1;   // the ring may wrap
+            bulk_arm(bar, static_cast<uint32_t>(tk.n) * D * 4);
+            bulk_copy(dst, p_unit + g.res_k + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
+            bulk_copy(dst + 16 * D, p_unit + g.res_v + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
+            if (n2 > 0) {
+              bulk_copy(dst + n1 * D * 2, p_unit + g.res_k, n2 * D * 2, bar);
+              bulk_copy(dst + 16 * D + n1 * D * 2, p_unit + g.res_v, n2 * D * 2, bar);
+            }
           }
         }
       }
@@ -647,6 +693,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   }
   const float sc_scale = qscale * kTwo24;
 
+  // per-lane shared-memory offsets inside a group block (loop invariant)
+  const uint32_t stages_s = smem_addr(my_stages);
+  constexpr bool kSwap = (RK == 64);   // 64-byte key rows: odd r swaps its row pair
+  const int sw = kSwap ? (r & 1) : 0;
+  const uint32_t o_k0 = static_cast<uint32_t>(g.blk_kq) + (TPL * r + sw) * RK + c * (RK / 4);
+  const uint32_t o_k1 = static_cast<uint32_t>(g.blk_kq) + (TPL * r + 1 - sw) * RK + c * (RK / 4);
+  const uint32_t o_ds = static_cast<uint32_t>(g.blk_ks) + c * (D / 2);   // key Δ; key min at + 2D
+  const uint32_t o_vs = static_cast<uint32_t>(g.blk_vs) + TPL * r * 4;   // value (Δ, min) of token TPL*r
+  const uint32_t vrow = static_cast<uint32_t>(g.G) * BITS / 8;           // bytes of one value-code row
+  const uint32_t vrow8 = 8 * vrow, vrow16 = 16 * vrow;
+  const uint32_t o_vq = static_cast<uint32_t>(g.blk_vq) + r * vrow + (QV >= 32 ? c * (QV / 8) : ((c * QV) / 32) * 4);
+  const int vsh = QV >= 32 ? 0 : ((c * QV) % 32) / 2;   // the lane's codes within their word
+
   // ------------------------------------------------------------ consumer
   const int nunits = u_last - u_first + 1;
   int cu = -1;                  // open unit (from u_first); -1 before the first
@@ -658,6 +717,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
 #pragma unroll
   for (int i = 0; i < NCT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
   const uint8_t* qlane = qw + hh_col * WS::kQRow + c * WS::kQS;
+  const uint32_t q_s = smem_addr(qlane);
 
   auto open_unit = [&](int k) {
     const int u = u_first + k;
@@ -721,7 +781,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   for (;;) {
     produce();
     __syncwarp();
-    if (__shfl_sync(0xffffffffu, inflight, 0) == 0) break;   // every claim issued and consumed
+    if (inflight == 0) break;   // every claim issued and consumed
     if (!acquire()) break;
     const int item = *reinterpret_cast<volatile int*>(ring_w + c_st);
     if (item & 1) {
@@ -741,7 +801,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         const int hh = kk / (D / 8), idx = kk % (D / 8);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (hh < nh) v = *reinterpret_cast<const uint4*>(src + hh * D * 2 + idx * 16);
-        *reinterpret_cast<uint4*>(qw + hh * WS::kQRow + (idx / (QD / 8)) * WS::kQS + (idx % (QD / 8)) * 16) = v;
+        // pairs (0, 1, 2, 3) of the chunk stored as (0, 2, 1, 3): the Σ q·min
+        // MMAs then take their B pairs straight from one 16-byte load
+        *reinterpret_cast<uint4*>(qw + hh * WS::kQRow + (idx / (QD / 8)) * WS::kQS + (idx % (QD / 8)) * 16) =
+            make_uint4(v.x, v.z, v.y, v.w);
       }
       release();
       __syncwarp();
@@ -751,21 +814,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
     if (pos < n_vis) {
       // ------------------------------------------------------ a frozen group
       const int64_t grp = a.plan.g_first + pos;
-      const uint8_t* blk = my_stages + c_st * a.stage_bytes;
+      const uint32_t blk = stages_s + c_st * a.stage_bytes;   // shared address of the block
 
       // (1) the query (natural pair order) and the folded B fragments:
       // hi = fp16(q Δ) in even columns, lo = q Δ - hi in odd ones
-      uint32_t q2[NP];
+      uint32_t q2[NP];   // natural pair order (the q area holds pairs 0, 2, 1, 3 of each 4)
 #pragma unroll
       for (int i = 0; i < NP / 4; ++i) {
-        const uint4 v = reinterpret_cast<const uint4*>(qlane)[i];
-        q2[4 * i] = v.x; q2[4 * i + 1] = v.y; q2[4 * i + 2] = v.z; q2[4 * i + 3] = v.w;
+        const uint4 v = lds128(q_s + 16 * i);
+        q2[4 * i] = v.x; q2[4 * i + 1] = v.z; q2[4 * i + 2] = v.y; q2[4 * i + 3] = v.w;
       }
-      const uint8_t* ks = blk + g.blk_ks;
       uint32_t bq[NP];
 #pragma unroll
       for (int i = 0; i < NP / 4; ++i) {
-        const uint4 dv = *reinterpret_cast<const uint4*>(ks + c * (D / 2) + 16 * i);
+        const uint4 dv = lds128(blk + o_ds + 16 * i);
         const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -773,16 +835,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
           bq[4 * i + j] = hfma2_u(q2[4 * i + j], dw[j], (hi ^ 0x80008000u) & partmask);
         }
       }
-      // (2) Σ_c q_c min_c for every head, one MMA per k-chunk (column 2c = head c)
-      float cst[4] = {0.f, 0.f, 0.f, 0.f};
+      // (2) Σ_c q_c min_c for every head (column 2c = head c).  A holds min pairs
+      // 4i, 4i+1, 4i+2, 4i+3 as loaded (rows r | r+8 x k-halves); the first MMA
+      // pairs row r with q of pairs 4i, 4i+2, the second row r+8 with q of
+      // pairs 4i+1, 4i+3, and the two useful rows are added
+      float cst_a[4] = {0.f, 0.f, 0.f, 0.f}, cst_b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < NP / 4; ++i) {
-        const uint4 mv = *reinterpret_cast<const uint4*>(ks + 2 * D + c * (D / 2) + 16 * i);
-        mma16816(cst, mv.x, mv.x, mv.y, mv.y, q2[4 * i], q2[4 * i + 1]);
-        mma16816(cst, mv.z, mv.z, mv.w, mv.w, q2[4 * i + 2], q2[4 * i + 3]);
+        const uint4 mv = lds128(blk + o_ds + 2 * D + 16 * i);
+        mma16816(cst_a, mv.x, mv.y, mv.z, mv.w, q2[4 * i], q2[4 * i + 2]);
+        mma16816(cst_b, mv.x, mv.y, mv.z, mv.w, q2[4 * i + 1], q2[4 * i + 3]);
       }
-      const float cst_h = cst[0] * qscale;
-      const uint8_t* vsc = blk + g.blk_vs;
+      const float cst_h = (cst_a[0] + cst_b[2]) * qscale;
       const int64_t a_grp = g.S + grp * g.G;
 
       for (int s0 = 0; s0 < g.G; s0 += CH) {
@@ -793,25 +857,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
           uint32_t w0[KW], w1[KW];
           // 64-byte rows: odd r takes the pair's rows in swapped order so the
           // two rows of a shared-memory phase fall in different bank halves
-          constexpr bool kSwap = (RK == 64);
-          const int sw = kSwap ? (r & 1) : 0;
-          const uint8_t* row0 = blk + g.blk_kq + (s0 + TPL * r + 2 * v2 + sw) * RK + c * (RK / 4);
-          const uint8_t* row1 = blk + g.blk_kq + (s0 + TPL * r + 2 * v2 + 1 - sw) * RK + c * (RK / 4);
+          const uint32_t row0 = blk + o_k0 + (s0 + 2 * v2) * RK;
+          const uint32_t row1 = blk + o_k1 + (s0 + 2 * v2) * RK;
           if constexpr (KW >= 4) {
 #pragma unroll
             for (int i = 0; i < KW; i += 4) {
-              const uint4 x = *reinterpret_cast<const uint4*>(row0 + 4 * i);
-              const uint4 y = *reinterpret_cast<const uint4*>(row1 + 4 * i);
+              const uint4 x = lds128(row0 + 4 * i);
+              const uint4 y = lds128(row1 + 4 * i);
               w0[i] = x.x; w0[i + 1] = x.y; w0[i + 2] = x.z; w0[i + 3] = x.w;
               w1[i] = y.x; w1[i + 1] = y.y; w1[i + 2] = y.z; w1[i + 3] = y.w;
             }
           } else if constexpr (KW == 2) {
-            const uint2 x = *reinterpret_cast<const uint2*>(row0);
-            const uint2 y = *reinterpret_cast<const uint2*>(row1);
+            const uint2 x = lds64(row0);
+            const uint2 y = lds64(row1);
             w0[0] = x.x; w0[1] = x.y; w1[0] = y.x; w1[1] = y.y;
           } else {
-            w0[0] = *reinterpret_cast<const uint32_t*>(row0);
-            w1[0] = *reinterpret_cast<const uint32_t*>(row1);
+            w0[0] = lds32(row0);
+            w1[0] = lds32(row1);
           }
           float acc[NA][4];
 #pragma unroll
@@ -856,9 +918,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         float pd[TPL];
         {
           float dm[2 * TPL];   // (Δ, min) of the lane's tokens
-          const __half2* vp = reinterpret_cast<const __half2*>(vsc) + s0 + TPL * r;
           if constexpr (TPL == 4) {
-            const uint4 x = *reinterpret_cast<const uint4*>(vp);
+            const uint4 x = lds128(blk + o_vs + 4 * s0);
             const uint32_t xw4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -866,7 +927,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
               dm[2 * i] = f.x; dm[2 * i + 1] = f.y;
             }
           } else {
-            const uint2 x = *reinterpret_cast<const uint2*>(vp);
+            const uint2 x = lds64(blk + o_vs + 4 * s0);
             const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
             const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
             dm[0] = f0.x; dm[1] = f0.y; dm[2] = f1.x; dm[3] = f1.y;
@@ -908,24 +969,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
           const uint2 x = *reinterpret_cast<const uint2*>(xw + xch_off<CH>(hh_col, r & 1, 4 * c));
           bp[0][0] = x.x; bp[0][1] = x.y;
         }
-        const uint8_t* vq = blk + g.blk_vq + s0 * BITS / 8;
-        const int vrow = g.G * BITS / 8;
+        const uint32_t vq = blk + o_vq + s0 * BITS / 8;
 #pragma unroll
         for (int ct = 0; ct < NCT; ++ct) {
           uint32_t v0[VW], v1[VW];
-          const uint8_t* rowa = vq + (16 * ct + r) * vrow;
-          const uint8_t* rowb = rowa + 8 * vrow;
-          if constexpr (QV >= 32) {
-#pragma unroll
-            for (int i = 0; i < VW; ++i) {
-              v0[i] = reinterpret_cast<const uint32_t*>(rowa + c * (QV / 8))[i];
-              v1[i] = reinterpret_cast<const uint32_t*>(rowb + c * (QV / 8))[i];
-            }
+          const uint32_t rowa = vq + ct * vrow16;
+          const uint32_t rowb = rowa + vrow8;
+          if constexpr (VW == 2) {
+            const uint2 x = lds64(rowa), y = lds64(rowb);
+            v0[0] = x.x; v0[1] = x.y; v1[0] = y.x; v1[1] = y.y;
+          } else if constexpr (QV >= 32) {
+            v0[0] = lds32(rowa);
+            v1[0] = lds32(rowb);
           } else {
-            const int bitpos = c * QV;
-            const int sh = (bitpos % 32) / 2;
-            v0[0] = reinterpret_cast<const uint32_t*>(rowa)[bitpos / 32] >> sh;
-            v1[0] = reinterpret_cast<const uint32_t*>(rowb)[bitpos / 32] >> sh;
+            v0[0] = lds32(rowa) >> vsh;
+            v1[0] = lds32(rowb) >> vsh;
           }
 #pragma unroll
           for (int kcn = 0; kcn < NKT; ++kcn) {
@@ -946,11 +1004,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         for (int i = 0; i < NCT; ++i) { oacc[i][0] *= kTwo24; oacc[i][1] *= kTwo24; oacc[i][2] *= kTwo24; oacc[i][3] *= kTwo24; }
         o_real = true;
       }
-      uint32_t q2[NP];
+      uint32_t q2[NP];   // natural pair order
 #pragma unroll
       for (int i = 0; i < NP / 4; ++i) {
-        const uint4 v = reinterpret_cast<const uint4*>(qlane)[i];
-        q2[4 * i] = v.x; q2[4 * i + 1] = v.y; q2[4 * i + 2] = v.z; q2[4 * i + 3] = v.w;
+        const uint4 v = lds128(q_s + 16 * i);
+        q2[4 * i] = v.x; q2[4 * i + 1] = v.z; q2[4 * i + 2] = v.y; q2[4 * i + 3] = v.w;
       }
       // keys of token r (zero past the chunk), natural pair order of quarter c
       uint32_t ka[NP];
@@ -1038,7 +1096,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   }
 
   // drain this warp's copies still in flight (only after an abort), bounded
-  if (aborted && lane == 0) {
+  if (aborted) {
     for (int k = 0; k < inflight; ++k) {
       mbar_wait(bar0 + 8 * c_st, c_ph);
       if (++c_st == a.ns) { c_st = 0; c_ph ^= 1u; }
