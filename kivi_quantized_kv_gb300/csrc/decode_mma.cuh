@@ -208,6 +208,26 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 
+// Lane-0 work without a divergent branch: PTX predicated on `pred`.
+__device__ __forceinline__ uint32_t atom_add_shared_if(bool pred, uint32_t addr, uint32_t v) {
+  uint32_t old = 0u;
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p atom.shared.add.u32 %0, [%1], %3;\n\t}"
+               : "+r"(old) : "r"(addr), "r"(static_cast<uint32_t>(pred)), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void sts32_if(bool pred, uint32_t addr, uint32_t v) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.u32 [%0], %1;\n\t}"
+               :: "r"(addr), "r"(v), "r"(static_cast<uint32_t>(pred)) : "memory");
+}
+// Arms the barrier for `bytes` and issues one bulk copy of them, if pred.
+__device__ __forceinline__ void bulk_load_if(bool pred, uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+               "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %2;\n\t"
+               "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "r"(static_cast<uint32_t>(pred)) : "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -589,16 +609,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   int p_end = static_cast<int>(static_cast<int64_t>(u_first) * a.uw - c_start);
   const uint8_t* p_unit = nullptr;
   bool aborted = false;
+  const uint32_t stages_s = smem_addr(my_stages);
+  const uint32_t ring_s = smem_addr(ring_w);
+  const uint32_t next_s = smem_addr(&s_next);
+  const bool leader = lane == 0;
+  const int n_vis_i = static_cast<int>(n_vis);   // visible groups of one unit
   // the whole warp runs the bookkeeping on warp-uniform values; lane 0 alone
-  // claims, notes the item and issues the copies
+  // claims, notes the item and issues the copies (predicated, no branch)
   auto produce = [&]() {
     if (aborted) return;
     while (inflight < a.ns) {
       if (!p_have) {
         if (p_done) return;
-        int rel = 0;
-        if (lane == 0) rel = static_cast<int>(atomicAdd(&s_next, 1u));
-        rel = __shfl_sync(0xffffffffu, rel, 0);
+        const int rel = __shfl_sync(0xffffffffu, static_cast<int>(atom_add_shared_if(leader, next_s, 1u)), 0);
         if (rel >= range) { p_done = true; return; }
         p_rel = rel;
         p_have = true;
@@ -608,15 +631,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
           p_q = true;
         }
       }
-      const uint32_t dst = smem_addr(my_stages + p_st * a.stage_bytes);
+      const uint32_t dst = stages_s + p_st * a.stage_bytes;
       const uint32_t bar = bar0 + 8 * p_st;
       if (p_q) {
         int nh_q;
         const __half* qsrc = unit_q(u_first + p_u, nh_q);
-        if (lane == 0) {
-          ring_w[p_st] = 2 * p_u + 1;
-          bulk_load(dst, qsrc, static_cast<uint32_t>(nh_q) * D * 2, bar);
-        }
+        sts32_if(leader, ring_s + 4 * p_st, 2 * p_u + 1);
+        bulk_load_if(leader, dst, qsrc, static_cast<uint32_t>(nh_q) * D * 2, bar);
         p_q = false;
         if (++p_st == a.ns) p_st = 0;
         ++inflight;
@@ -624,15 +645,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       }
       const int pos = p_rel - (p_end - static_cast<int>(a.uw));   // position inside unit p_u
       bool issued = true;
-      if (pos < n_vis) {   // a frozen group block
+      if (pos < n_vis_i) {   // a frozen group block
         uint32_t slot = slot0 + static_cast<uint32_t>(pos);
         if (ring_slots && slot >= n_slots) slot -= n_slots;
-        if (lane == 0) {
-          ring_w[p_st] = 2 * p_rel;
-          bulk_load(dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
-        }
+        sts32_if(leader, ring_s + 4 * p_st, 2 * p_rel);
+        bulk_load_if(leader, dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
       } else {                // a tail chunk: key rows then value rows
-        const TailChunk tk = tail_chunk(pos - static_cast<int>(n_vis), t_sink, t_res);
+        const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res);
         if (tk.n == 0) {
           issued = false;     // nothing to copy or to attend to
         } else if (lane == 0) {
@@ -694,7 +713,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const float sc_scale = qscale * kTwo24;
 
   // per-lane shared-memory offsets inside a group block (loop invariant)
-  const uint32_t stages_s = smem_addr(my_stages);
   constexpr bool kSwap = (RK == 64);   // 64-byte key rows: odd r swaps its row pair
   const int sw = kSwap ? (r & 1) : 0;
   const uint32_t o_k0 = static_cast<uint32_t>(g.blk_kq) + (TPL * r + sw) * RK + c * (RK / 4);
@@ -710,7 +728,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const int nunits = u_last - u_first + 1;
   int cu = -1;                  // open unit (from u_first); -1 before the first
   int nh = 0, total = 1, cslot = 0;
-  int64_t u_base = 0;           // first position of the open unit
+  int u_rel = 0;                // first position of the open unit, relative to c_start
   float res_m = -INFINITY, res_l = 0.f, res_mn = 0.f;
   bool o_real = false;          // oacc holds real-scale values (after a tail chunk)
   float oacc[NCT][4];
@@ -722,7 +740,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   auto open_unit = [&](int k) {
     const int u = u_first + k;
     (void)unit_q(u, nh);
-    u_base = static_cast<int64_t>(u) * a.uw;
+    const int64_t u_base = static_cast<int64_t>(u) * a.uw;
+    u_rel = static_cast<int>(u_base - c_start);
     const int first = owner_of(u_base, W, P);
     total = owner_of(u_base + a.uw - 1, W, P) - first + 1;
     cslot = static_cast<int>(blockIdx.x) - first;
@@ -783,7 +802,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
     __syncwarp();
     if (inflight == 0) break;   // every claim issued and consumed
     if (!acquire()) break;
-    const int item = *reinterpret_cast<volatile int*>(ring_w + c_st);
+    const int item = static_cast<int>(lds32(ring_s + 4 * c_st));
     if (item & 1) {
       // ------------------------------------------------------ query rows
       // of the next unit this warp works on; units passed on the way are closed
@@ -810,8 +829,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       __syncwarp();
       continue;
     }
-    const int64_t pos = c_start + (item >> 1) - u_base;   // position inside the open unit
-    if (pos < n_vis) {
+    const int pos = (item >> 1) - u_rel;   // position inside the open unit
+    if (pos < n_vis_i) {
       // ------------------------------------------------------ a frozen group
       const int64_t grp = a.plan.g_first + pos;
       const uint32_t blk = stages_s + c_st * a.stage_bytes;   // shared address of the block
@@ -996,7 +1015,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       release();
     } else {
       // ------------------------------------------------------ a tail chunk
-      const TailChunk tk = tail_chunk(static_cast<int>(pos - n_vis), t_sink, t_res);
+      const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res);
       const uint8_t* kst = my_stages + c_st * a.stage_bytes;
       const uint8_t* vst = kst + 16 * D;
       if (!o_real) {   // from here on oacc holds real-scale values
