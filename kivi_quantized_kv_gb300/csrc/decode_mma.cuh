@@ -11,7 +11,7 @@
 // in chunks of 4 tokens, then the fp16 ring in chunks of 8).  The units'
 // positions, laid end to end, are cut into one equal contiguous range per CTA,
 // and the grid is one wave of resident CTAs.  Inside a CTA the warps claim
-// the range's positions one at a time from a shared counter, so a warp that
+// the range's positions two at a time from a shared counter, so a warp that
 // is held up (say, by combining a unit) simply takes fewer.
 //
 // Warps never wait for one another while they stream:
@@ -66,6 +66,7 @@ constexpr float kTwo24 = 16777216.0f;                    // codes enter the MMAs
 // error word bits
 constexpr unsigned kErrCopy = 1u;   // a copy never completed
 constexpr unsigned kErrSlot = 2u;   // a combine never released the slots
+constexpr unsigned kClaim = 2u;     // positions a warp claims at a time
 
 struct Args {
   Geo g;
@@ -582,8 +583,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   };
 
   // ------------------------------------------------------------ producer
-  // per-warp copy pipeline.  Lane 0 claims the CTA's positions one at a time
-  // from a shared counter (so a warp that is held up takes fewer), and before
+  // per-warp copy pipeline.  Lane 0 claims the CTA's positions kClaim at a
+  // time from a shared counter (so a warp that is held up takes fewer), and before
   // the first position of a unit it issues that unit's query rows; each item
   // is noted in the warp's ring (one int per stage: 2 * rel for a position
   // rel of the CTA's range, 2 * k + 1 for the query rows of unit u_first + k)
@@ -603,8 +604,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   int p_u = -1;                 // unit (from u_first) of the last claimed position
   bool p_have = false;          // a claimed position waits for a stage
   bool p_q = false;             // the query rows of unit p_u wait for a stage
-  bool p_done = false;          // the CTA's positions are all claimed
+  bool p_done = false;          // the CTA's positions are all claimed (and the last claim used up)
   int p_rel = 0;
+  int p_next = 0, p_left = 0;   // the warp's current claim: next position, positions left in it
   // end of unit p_u's positions, relative to c_start (negative or zero before the first claim)
   int p_end = static_cast<int>(static_cast<int64_t>(u_first) * a.uw - c_start);
   const uint8_t* p_unit = nullptr;
@@ -620,13 +622,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
     if (aborted) return;
     while (inflight < a.ns) {
       if (!p_have) {
-        if (p_done) return;
-        const int rel = __shfl_sync(0xffffffffu, static_cast<int>(atom_add_shared_if(leader, next_s, 1u)), 0);
-        if (rel >= range) { p_done = true; return; }
-        p_rel = rel;
+        if (p_left == 0) {   // claim the next kClaim positions of the range
+          if (p_done) return;
+          const int rel = __shfl_sync(0xffffffffu, static_cast<int>(atom_add_shared_if(leader, next_s, kClaim)), 0);
+          if (rel >= range) { p_done = true; return; }
+          p_next = rel;
+          p_left = min(static_cast<int>(kClaim), range - rel);
+        }
+        p_rel = p_next++;
+        --p_left;
         p_have = true;
-        if (rel >= p_end) {   // the claim lies in a later unit (claims only grow)
-          do { ++p_u; p_end += a.uw; } while (rel >= p_end);
+        if (p_rel >= p_end) {   // the position lies in a later unit (positions only grow)
+          do { ++p_u; p_end += a.uw; } while (p_rel >= p_end);
           p_unit = unit_base(u_first + p_u);
           p_q = true;
         }
