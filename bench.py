@@ -1,5 +1,7 @@
 """Benchmark of the KIVI quantized KV cache on GB300: one step = append one
-new K/V token to every sequence + decode attention over the whole cache.
+new K/V token to every sequence + decode attention over the whole cache,
+through the fused kivi_append_decode_attn call (--unfused: kivi_append then
+kivi_decode_attn).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -42,6 +44,7 @@ def parse():
     ap.add_argument("--replicas", type=int, default=0, help="cache replicas (0 = enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="append and decode as two calls (two launches)")
     return ap.parse_args()
 
 
@@ -236,16 +239,23 @@ def run_ours(args, rank, world, device):
     out = torch.empty((w.batch, w.h_q, w.head_dim), dtype=torch.float16, device=device)
     torch.cuda.synchronize(device)
 
+    fused = not args.unfused
+
     def step(s, ev=None):
         c = caches[s % n_rep][0]
         k, v = new_kv[s]
         Lb = c.layout()
         if ev is not None:
             ev[0].record(stream)
-        c.append(k, v)
-        if ev is not None:
-            ev[1].record(stream)
-        c.decode(qs[s % len(qs)], out=out)
+        if fused:   # one call: append + decode (the flush, when a group freezes, is a launch of its own)
+            c.append_decode(k, v, qs[s % len(qs)], out=out)
+            if ev is not None:
+                ev[1].record(stream)
+        else:
+            c.append(k, v)
+            if ev is not None:
+                ev[1].record(stream)
+            c.decode(qs[s % len(qs)], out=out)
         if ev is not None:
             ev[2].record(stream)
         La = c.layout()
@@ -268,13 +278,21 @@ def run_ours(args, rank, world, device):
         clocks.mark_begin()
     t0.record(stream)
     dec_bytes = app_bytes = launches = 0
+    flush_steps = []
+    step_dec_bytes = []
     for i in range(args.steps):
         s = args.warmup + i
         Lb, La, c = step(s, evs[i])
-        dec_bytes += c.decode_bytes()
+        db = c.decode_bytes()
+        dec_bytes += db
+        step_dec_bytes.append(db)
         app_bytes += append_bytes(w, Lb, La)
         flush = La["n_groups"] > Lb["n_groups"]
-        launches += (2 if flush else 1) + 1     # append: write (+ flush); decode: one launch, merge inside
+        flush_steps.append(flush)
+        if fused:
+            launches += 2 if flush else 1       # the fused decode (+ the flush of a freezing group)
+        else:
+            launches += (2 if flush else 1) + 1     # append: write (+ flush); decode: one launch, merge inside
     t1.record(stream)
     torch.cuda.synchronize(device)
     if clocks:
@@ -283,8 +301,18 @@ def run_ours(args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
-    app_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
-    dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    if fused:
+        # the decode kernel's roofline over the steps that froze no group (one
+        # launch each: the decode, which also writes the fresh token)
+        keep = [i for i in range(args.steps) if not flush_steps[i]]
+        dec_ms = sum(evs[i][0].elapsed_time(evs[i][1]) for i in keep)
+        dec_bytes_rl = sum(step_dec_bytes[i] for i in keep)
+        app_ms = ms   # every step appends B tokens
+    else:
+        app_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+        dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+        keep = list(range(args.steps))
+        dec_bytes_rl = dec_bytes
     ms_max = ms
     if world > 1:
         tt = torch.tensor([ms], device=device)
@@ -292,11 +320,11 @@ def run_ours(args, rank, world, device):
         ms_max = float(tt.item())
     step_bytes = (dec_bytes + app_bytes) / args.steps
     value = step_bytes * args.steps * world / (ms_max / 1e3) / 1e9
-    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    dec_gbs = dec_bytes_rl / (dec_ms / 1e3) / 1e9
     res = {
         "w": w, "cfg": cfg, "n_rep": n_rep, "per_cache": per_cache, "ms": ms_max, "value": value,
-        "dec_gbs": dec_gbs, "dec_ms": dec_ms / args.steps, "app_ms": app_ms / args.steps,
-        "dec_bytes": dec_bytes / args.steps, "step_bytes": step_bytes, "launches": launches,
+        "dec_gbs": dec_gbs, "dec_ms": dec_ms / max(len(keep), 1), "app_ms": app_ms / args.steps,
+        "dec_bytes": dec_bytes_rl / max(len(keep), 1), "fused": fused, "step_bytes": step_bytes, "launches": launches,
         "clocks": clk, "app_tok_s": w.batch * args.steps / (app_ms / 1e3),
     }
     if not args.no_e2e:
@@ -317,6 +345,8 @@ def run_e2e(args, caches, new_kv, w, device, stream):
     out_h = torch.empty_like(q_h).pin_memory()
     k_d = torch.empty((w.batch, w.h_kv, 1, w.head_dim), dtype=torch.float16, device=device)
     v_d = torch.empty_like(k_d)
+    q_d = torch.empty((w.batch, w.h_q, w.head_dim), dtype=torch.float16, device=device)
+    out_d = torch.empty_like(q_d)
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -327,8 +357,13 @@ def run_e2e(args, caches, new_kv, w, device, stream):
         Lb = c.layout()
         k_d.copy_(k_h[s], non_blocking=True)
         v_d.copy_(v_h[s], non_blocking=True)
-        c.append(k_d, v_d)
-        c.decode_host(q_h, out_h)
+        if args.unfused:
+            c.append(k_d, v_d)
+            c.decode_host(q_h, out_h)
+        else:
+            q_d.copy_(q_h, non_blocking=True)
+            c.append_decode(k_d, v_d, q_d, out=out_d)
+            out_h.copy_(out_d, non_blocking=True)
         total += c.decode_bytes() + append_bytes(w, Lb, c.layout())
     t1.record(stream)
     torch.cuda.synchronize(device)
@@ -455,8 +490,11 @@ def main():
         "decode_frac_of_8tbs": round(r["dec_gbs"] / NOMINAL_HBM_GBS, 4),
         "decode_us": round(r["dec_ms"] * 1e3, 2),
         "decode_steps_per_s": round(1e3 / r["dec_ms"], 1),
-        "append_us": round(r["app_ms"] * 1e3, 2),
+        "append_us": None if r["fused"] else round(r["app_ms"] * 1e3, 2),
+        "step_call": "kivi_append_decode_attn" if r["fused"] else "kivi_append + kivi_decode_attn",
         "append_tokens_per_s": round(r["app_tok_s"], 1),
+        "append_tokens_per_s_kind": ("tokens appended per second by the whole fused step (append + decode)"
+                                     if r["fused"] else "tokens appended per second of the append call"),
     }
     if "e2e" in r:
         line["e2e"] = r["e2e"]

@@ -155,6 +155,22 @@ int kivi_append(kivi_cache* cache, const void* k_new, const void* v_new, int64_t
  * scratch.  Errors: ENULL, EALIGN, ECUDA. */
 int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_stream);
 
+/* One decode step in one call: appends one token to every sequence and
+ * returns the decode attention over everything including that token, the
+ * fused op of tract #2329 ("What's in the PR": inputs [Q, K_new, V_new],
+ * output with Q's shape).  The result and the cache bytes are those of
+ * kivi_append(k_new, v_new, 1) followed by kivi_decode_attn(q, out) (the
+ * output to within the decode's rounding).  The new token is attended
+ * straight from k_new / v_new and written into its sink or ring slot by the
+ * decode launch itself, so a step is one launch; a step whose token freezes
+ * a group (the ring is full) first runs that group's quantization launch.
+ *   k_new, v_new  device fp16 [B][h_kv][1][d], contiguous, 16-byte aligned.
+ *   q, out        device fp16 [B][h_q][d], contiguous, 16-byte aligned.
+ * Errors: ENULL, EALIGN, ECAPACITY, ECUDA (the token count is then left
+ * at its pre-call value). */
+int kivi_append_decode_attn(kivi_cache* cache, const void* k_new, const void* v_new, const void* q, void* out,
+                            void* cuda_stream);
+
 /* Same as kivi_decode_attn with host-resident q and out (pinned host memory
  * gives asynchronous copies): copies q into the arena's staging area, runs
  * the decode, copies the result back to out_host, all on `stream`.  The call

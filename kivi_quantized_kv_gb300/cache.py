@@ -117,6 +117,26 @@ class KiviCache:
                                                ctypes.c_void_p(_stream_ptr(stream))), "kivi_decode_attn")
         return out
 
+    def append_decode(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """One decode step: append k_new, v_new ([B, H_kv, 1, d] float16) and
+        return the attention of q ([B, H_q, d] float16) over the cache
+        including them (kivi_append_decode_attn)."""
+        c = self.cfg
+        kv_shape = (c.batch, c.h_kv, 1, c.head_dim)
+        self._check_io(k_new, kv_shape, "k_new")
+        self._check_io(v_new, kv_shape, "v_new")
+        shape = (c.batch, c.h_q, c.head_dim)
+        self._check_io(q, shape, "q")
+        if out is None:
+            out = torch.empty(shape, dtype=torch.float16, device=self.arena.device)
+        self._check_io(out, shape, "out")
+        _abi.check(_abi.lib().kivi_append_decode_attn(
+            self._h, ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(_stream_ptr(stream))), "kivi_append_decode_attn")
+        return out
+
     def decode_host(self, q_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> torch.Tensor:
         """Host-resident q and out (pin them for asynchronous copies); the
         copies and the decode are queued on `stream`."""

@@ -119,16 +119,26 @@ constexpr int kSinkChunk = 4;
 constexpr int kRingChunk = 8;
 struct TailChunk {
   int sink;        // 1 = fp32 sink rows
-  int n;           // tokens in the chunk (0 only when the cache is empty)
+  int fresh;       // 1 = the token being appended, fp16 rows from the inputs
+  int n;           // tokens in the chunk (0 only when there is nothing to attend to)
   int first;       // first sink index, or first ring token (0-based, oldest first)
 };
-__device__ __forceinline__ TailChunk tail_chunk(int idx, int n_sink, int n_res) {
+// Tail position idx of a unit: the sink chunks, the ring chunks, then (fused
+// append) the fresh token.
+__device__ __forceinline__ TailChunk tail_chunk(int idx, int n_sink, int n_res, bool fresh) {
   TailChunk t;
   const int n_sc = (n_sink + kSinkChunk - 1) / kSinkChunk;
+  const int n_rc = (n_res + kRingChunk - 1) / kRingChunk;
+  t.fresh = 0;
   if (idx < n_sc) {
     t.sink = 1;
     t.first = idx * kSinkChunk;
     t.n = min(kSinkChunk, n_sink - t.first);
+  } else if (fresh && idx == n_sc + n_rc) {
+    t.sink = 0;
+    t.fresh = 1;
+    t.first = 0;
+    t.n = 1;
   } else {
     t.sink = 0;
     t.first = (idx - n_sc) * kRingChunk;
@@ -575,6 +585,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
     const int bb = u / per_b, hk = (u % per_b) / a.npass;
     return a.arena + (static_cast<int64_t>(bb) * g.hkv + hk) * g.unit_bytes;
   };
+  // (sequence, kv head) index of unit u
+  auto unit_kv = [&](int u) -> int64_t {
+    const int per_b = g.hkv * a.npass;
+    return static_cast<int64_t>(u / per_b) * g.hkv + (u % per_b) / a.npass;
+  };
   auto unit_q = [&](int u, int& nh) -> const __half* {
     const int per_b = g.hkv * a.npass;
     const int bb = u / per_b, hk = (u % per_b) / a.npass, pass = u % a.npass;
@@ -591,6 +606,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const uint32_t n_slots = static_cast<uint32_t>(g.n_slots);
   const bool ring_slots = g.window > 0;
   const int t_sink = static_cast<int>(a.plan.st.n_sink), t_res = static_cast<int>(a.plan.st.n_res);
+  const bool fresh = a.plan.k_fresh != nullptr;   // fused append: the fresh token closes every tail
   const int rs0 = static_cast<int>((a.plan.st.n_groups * g.G) % g.R);   // ring slot of the oldest ring token
   const int range = static_cast<int>(c_end - c_start);
   // slot of the first visible group (ring of slots with a window); a unit's
@@ -658,12 +674,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         sts32_if(leader, ring_s + 4 * p_st, 2 * p_rel);
         bulk_load_if(leader, dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
       } else {                // a tail chunk: key rows then value rows
-        const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res);
+        const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res, fresh);
         if (tk.n == 0) {
           issued = false;     // nothing to copy or to attend to
         } else if (lane == 0) {
           ring_w[p_st] = 2 * p_rel;
-          if (tk.sink) {
+          if (tk.fresh) {     // the appended token's rows, straight from the inputs
+            const int64_t row = unit_kv(u_first + p_u) * D;
+            bulk_arm(bar, 4 * D);
+            bulk_copy(dst, a.plan.k_fresh + row, 2 * D, bar);
+            bulk_copy(dst + 16 * D, a.plan.v_fresh + row, 2 * D, bar);
+          } else if (tk.sink) {
             const uint32_t bytes = static_cast<uint32_t>(tk.n) * D * 4;
             bulk_arm(bar, 2 * bytes);
             bulk_copy(dst, p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
@@ -1022,7 +1043,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       release();
     } else {
       // ------------------------------------------------------ a tail chunk
-      const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res);
+      const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res, fresh);
       const uint8_t* kst = my_stages + c_st * a.stage_bytes;
       const uint8_t* vst = kst + 16 * D;
       if (!o_real) {   // from here on oacc holds real-scale values
@@ -1109,6 +1130,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
           uint32_t a0, a1;
           ldsm_x2_trans(a0, a1, vbase + 32 * ct);
           mma16816(oacc[ct], a0 & tmask, a1 & tmask, 0u, 0u, b0, 0u);
+        }
+      }
+      if (tk.fresh && (u_first + cu) % a.npass == 0) {
+        // fused append: the token into its sink slot (widened to fp32) or its
+        // ring slot; nothing this launch reads lives there
+        uint8_t* base = const_cast<uint8_t*>(unit_base(u_first + cu));
+        const int64_t fp = a.plan.fresh_pos;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          for (int e = 4 * lane; e < D; e += 128) {
+            const uint2 x = *reinterpret_cast<const uint2*>(kst + part * 16 * D + 2 * e);
+            if (fp < g.S) {
+              const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
+              const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
+              *reinterpret_cast<float4*>(base + (part ? g.sink_v : g.sink_k) + (fp * D + e) * 4) =
+                  make_float4(f0.x, f0.y, f1.x, f1.y);
+            } else {
+              const int64_t slot = (fp - g.S) % g.R;
+              *reinterpret_cast<uint2*>(base + (part ? g.res_v : g.res_k) + (slot * D + e) * 2) = x;
+            }
+          }
         }
       }
       release();

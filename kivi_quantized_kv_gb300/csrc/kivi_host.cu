@@ -205,6 +205,44 @@ int kivi_decode_attn(kivi_cache* c, const void* q, void* out, void* cuda_stream)
                                          static_cast<__half*>(out), pl, static_cast<cudaStream_t>(cuda_stream)));
 }
 
+int kivi_append_decode_attn(kivi_cache* c, const void* k_new, const void* v_new, const void* q, void* out,
+                            void* cuda_stream) {
+  if (!c || !k_new || !v_new || !q || !out) return KIVI_ENULL;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
+  const Geo& g = c->g;
+  const int64_t T_old = c->T, T_new = c->T + 1;
+  if (g.window == 0 && T_new > c->p.max_tokens) return KIVI_ECAPACITY;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const auto* kh = static_cast<const __half*>(k_new);
+  const auto* vh = static_cast<const __half*>(v_new);
+  const State s0 = kivi::state_at(g, T_old), s1 = kivi::state_at(g, T_new);
+  if (s1.n_groups > s0.n_groups) {
+    // the token reaches a full ring: its oldest G tokens freeze first, as in
+    // kivi_append (a launch of its own, before the decode reads the group)
+    int64_t g_begin = s0.n_groups;
+    if (s1.n_groups - g.n_slots > g_begin) g_begin = s1.n_groups - g.n_slots;
+    const cudaError_t e = kivi::launch_flush(g, c->arena, kh, vh, T_old, 1, g_begin, s1.n_groups, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  c->T = T_new;
+  kivi::DecodePlan pl = plan_for(*c);
+  // the fresh token is attended straight from the inputs (and written into
+  // its sink or ring slot by the same launch), so the cache's own tail is one
+  // token shorter
+  if (T_old < g.S) pl.st.n_sink -= 1; else pl.st.n_res -= 1;
+  pl.tc = static_cast<int32_t>((pl.st.n_sink + 3) / 4 + (pl.st.n_res + 7) / 8 + 1);
+  pl.k_fresh = kh;
+  pl.v_fresh = vh;
+  pl.fresh_pos = T_old;
+  const cudaError_t e = kivi::launch_decode(g, c->arena, static_cast<const __half*>(q), static_cast<__half*>(out),
+                                            pl, s);
+  if (e != cudaSuccess) {
+    c->T = T_old;
+    return cuda_status(e);
+  }
+  return KIVI_OK;
+}
+
 int kivi_decode_attn_host(kivi_cache* c, const void* q_host, void* out_host, void* cuda_stream) {
   if (!c || !q_host || !out_host) return KIVI_ENULL;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);

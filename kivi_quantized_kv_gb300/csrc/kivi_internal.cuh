@@ -54,11 +54,18 @@ cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, cons
 
 // ---- decode (decode.cu) ----
 struct DecodePlan {
-  State st;
+  State st;               // the sinks and ring tokens read from the cache (st.T counts the fresh token)
   int64_t g_first;        // first frozen group that can hold a visible token
   int64_t n_vis_groups;   // groups [g_first, n_groups)
   int32_t tc;             // work positions (in groups) that stand for one unit's tail
   int32_t ctas;           // CTAs of the wave (the launch clamps it further)
+  // fused append: one token per sequence attended straight from these
+  // [B][H_kv][1][d] inputs and written by the kernel into the cache (at
+  // position fresh_pos: a sink slot if below S, else its ring slot); null for
+  // a plain decode
+  const __half* k_fresh;
+  const __half* v_fresh;
+  int64_t fresh_pos;
 };
 
 // Decode launch shape: up to kDecodeWarps warps per CTA and kDecodeCtasPerSm
