@@ -376,42 +376,57 @@ __device__ __forceinline__ int64_t unit_head0(const Args& a, int u) {
 }
 
 // Merge of the `total` partial records (o[D], m, l, pad, pad) of one query
-// head for channel ch: M = max m_s, w_s = 2^(m_s - M), L = Σ l_s w_s,
-// O = Σ o_s[ch] w_s.  Eight records' loads go out at a time.
+// head for channels ch, ch + 1: M = max m_s, w_s = 2^(m_s - M),
+// L = Σ l_s w_s, O = Σ o_s w_s.  The loads of up to kMergeBatch records go
+// out together (one L2 round trip per batch), one rescale per batch.
+constexpr int kMergeBatch = 16;
 template <int D>
-__device__ __forceinline__ void merge_partials(const float* base, int total, int ch, float& O, float& L) {
+__device__ __forceinline__ void merge_partials(const float* base, int total, int ch, float2& O, float& L) {
   float m = -INFINITY;
-  O = 0.f;
+  O = make_float2(0.f, 0.f);
   L = 0.f;
-  for (int s0 = 0; s0 < total; s0 += 8) {
-    float2 ml[8];
-    float o[8];
+  for (int s0 = 0; s0 < total; s0 += kMergeBatch) {
+    float2 ml[kMergeBatch], o[kMergeBatch];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kMergeBatch; ++k) {
       if (s0 + k < total) {
         const float* ps = base + (s0 + k) * (D + 4);
         ml[k] = __ldcg(reinterpret_cast<const float2*>(ps + D));
-        o[k] = __ldcg(ps + ch);
+        o[k] = __ldcg(reinterpret_cast<const float2*>(ps + ch));
       } else {
         ml[k] = make_float2(-INFINITY, 0.f);
-        o[k] = 0.f;
+        o[k] = make_float2(0.f, 0.f);
       }
     }
     float mb = m;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mb = fmaxf(mb, ml[k].x);
+    for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, ml[k].x);
     if (mb == -INFINITY) continue;
     const float sc = (m == -INFINITY) ? 0.f : ex2(m - mb);
-    O *= sc;
+    O.x *= sc;
+    O.y *= sc;
     L *= sc;
     m = mb;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kMergeBatch; ++k) {
       const float f = (ml[k].x == -INFINITY) ? 0.f : ex2(ml[k].x - m);
-      O = fmaf(o[k], f, O);
+      O.x = fmaf(o[k].x, f, O.x);
+      O.y = fmaf(o[k].y, f, O.y);
       L = fmaf(ml[k].y, f, L);
     }
   }
+}
+
+// Merges channel pair i (head i / (D/2)) of the unit whose first query head
+// is head0 and writes it out.
+template <int D>
+__device__ __forceinline__ void merge_out(const Args& a, int64_t head0, int i, int total) {
+  const int hh = i / (D / 2), ch = 2 * (i % (D / 2));
+  float2 O;
+  float L;
+  merge_partials<D>(a.partials + (head0 + hh) * a.stride * (D + 4), total, ch, O, L);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  *reinterpret_cast<__half2*>(a.out + (head0 + hh) * D + ch) = __floats2half2_rn(O.x * inv, O.y * inv);
 }
 
 // Combines head hh of the nw warp slots (o[D], m, l, pad, pad) for channel ch.
@@ -485,12 +500,7 @@ __device__ __forceinline__ void warp_epilogue(const Args& a, const float* slots,
   last_cta = __shfl_sync(0xffffffffu, last_cta, 0);
   if (!last_cta) return;
   __threadfence();
-  for (int i = lane; i < nh * D; i += 32) {
-    const int hh = i / D, ch = i % D;
-    float O, L;
-    merge_partials<D>(a.partials + (head0 + hh) * a.stride * (D + 4), total, ch, O, L);
-    a.out[(head0 + hh) * D + ch] = __float2half_rn(L > 0.f ? O / L : 0.f);
-  }
+  for (int i = lane; i < nh * D / 2; i += 32) merge_out<D>(a, head0, i, total);
   if (lane == 0) a.counters[u] = 0u;
 }
 
@@ -512,12 +522,7 @@ __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, 
   __syncthreads();
   if (!*s_flag) return;
   __threadfence();
-  for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
-    const int hh = i / D, ch = i % D;
-    float O, L;
-    merge_partials<D>(a.partials + (head0 + hh) * a.stride * (D + 4), total, ch, O, L);
-    a.out[(head0 + hh) * D + ch] = __float2half_rn(L > 0.f ? O / L : 0.f);
-  }
+  for (int i = threadIdx.x; i < nh * D / 2; i += blockDim.x) merge_out<D>(a, head0, i, total);
   if (threadIdx.x == 0) a.counters[u] = 0u;
 }
 
