@@ -201,6 +201,44 @@ def append_bytes(w, L_before, L_after, n=1):
     return units * per_unit
 
 
+def state_at(w, T):
+    """(n_sink, n_groups, n_res) after T tokens, the lazy-flush rule the
+    library uses (a token that reaches a full ring first freezes its oldest
+    G tokens)."""
+    n_sink = min(T, w.sinks)
+    m = max(T - w.sinks, 0)
+    ng = 0 if m <= w.residual else -(-(m - w.residual) // w.group)
+    return n_sink, ng, m - ng * w.group
+
+
+def decode_bytes_at(w, T, n_slots):
+    """Algorithmic bytes of one decode after T tokens; the same sum as
+    kivi_decode_bytes (checked against it in run_ours)."""
+    n_sink, ng, n_res = state_at(w, T)
+    first = max(ng - n_slots, 0)
+    lo = T - w.window if w.window > 0 else 0
+    if w.window > 0 and lo > w.sinks:
+        first = max(first, (lo - w.sinks) // w.group)
+    first = min(first, ng)
+    tq = touched = 0
+    for grp in range(first, ng):
+        a0 = w.sinks + grp * w.group
+        vis = a0 + w.group - max(a0, lo)
+        if vis > 0:
+            tq += vis
+            touched += 1
+    d = w.head_dim
+    per_unit = 2 * tq * d * w.bits // 8 + 4 * d * touched + 4 * tq + 4 * d * n_res + 8 * d * n_sink
+    return per_unit * w.batch * w.h_kv + 4 * d * w.batch * w.h_q
+
+
+def append_bytes_at(w, T, block_bytes):
+    """Algorithmic bytes of appending one token per sequence to T tokens."""
+    new_groups = state_at(w, T + 1)[1] - state_at(w, T)[1]
+    d = w.head_dim
+    return w.batch * w.h_kv * (8 * d + new_groups * (4 * d * w.group + block_bytes))
+
+
 # --------------------------------------------------------------- our arm
 def run_ours(args, rank, world, device):
     import torch
@@ -240,32 +278,36 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize(device)
 
     fused = not args.unfused
-
-    def step(s, ev=None):
+    import ctypes
+    from kivi_quantized_kv_gb300 import _abi
+    L = _abi.lib()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = ctypes.c_void_p
+    for c, _ in caches:   # every call below goes straight through the C ABI; check the shapes once
+        c._check_io(new_kv[0][0], (w.batch, w.h_kv, 1, w.head_dim), "k_new")
+    # per-step C-ABI arguments, marshalled before the timed region
+    args_of = []
+    for s in range(total_steps):
         c = caches[s % n_rep][0]
         k, v = new_kv[s]
-        Lb = c.layout()
-        if ev is not None:
-            ev[0].record(stream)
-        if fused:   # one call: append + decode (the flush, when a group freezes, is a launch of its own)
-            c.append_decode(k, v, qs[s % len(qs)], out=out)
-            if ev is not None:
-                ev[1].record(stream)
+        args_of.append((c._h, vp(k.data_ptr()), vp(v.data_ptr()), vp(qs[s % len(qs)].data_ptr()),
+                        vp(out.data_ptr())))
+
+    def step(s):
+        h, kp, vq, qp, op = args_of[s]
+        if fused:   # one call: append + decode (a freezing group's flush is a launch of its own)
+            st = L.kivi_append_decode_attn(h, kp, vq, qp, op, sp)
         else:
-            c.append(k, v)
-            if ev is not None:
-                ev[1].record(stream)
-            c.decode(qs[s % len(qs)], out=out)
-        if ev is not None:
-            ev[2].record(stream)
-        La = c.layout()
-        return Lb, La, c
+            st = L.kivi_append(h, kp, vq, 1, sp) or L.kivi_decode_attn(h, qp, op, sp)
+        if st != 0:
+            raise RuntimeError(_abi.status_string(st))
 
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize(device)
+    T_before = [caches[s % n_rep][0].tokens for s in range(n_rep)]   # tokens of each replica before the timed steps
+    meta = [(c.layout()["n_slots"], c.layout()["block_bytes"]) for c, _ in caches]
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(device) if rank == 0 else None
@@ -277,22 +319,8 @@ def run_ours(args, rank, world, device):
         time.sleep(0.05)
         clocks.mark_begin()
     t0.record(stream)
-    dec_bytes = app_bytes = launches = 0
-    flush_steps = []
-    step_dec_bytes = []
     for i in range(args.steps):
-        s = args.warmup + i
-        Lb, La, c = step(s, evs[i])
-        db = c.decode_bytes()
-        dec_bytes += db
-        step_dec_bytes.append(db)
-        app_bytes += append_bytes(w, Lb, La)
-        flush = La["n_groups"] > Lb["n_groups"]
-        flush_steps.append(flush)
-        if fused:
-            launches += 2 if flush else 1       # the fused decode (+ the flush of a freezing group)
-        else:
-            launches += (2 if flush else 1) + 1     # append: write (+ flush); decode: one launch, merge inside
+        step(args.warmup + i)
     t1.record(stream)
     torch.cuda.synchronize(device)
     if clocks:
@@ -301,18 +329,20 @@ def run_ours(args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
-    if fused:
-        # the decode kernel's roofline over the steps that froze no group (one
-        # launch each: the decode, which also writes the fresh token)
-        keep = [i for i in range(args.steps) if not flush_steps[i]]
-        dec_ms = sum(evs[i][0].elapsed_time(evs[i][1]) for i in keep)
-        dec_bytes_rl = sum(step_dec_bytes[i] for i in keep)
-        app_ms = ms   # every step appends B tokens
-    else:
-        app_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
-        dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
-        keep = list(range(args.steps))
-        dec_bytes_rl = dec_bytes
+    # bytes of the timed steps, from each replica's token count at each step
+    T_now = list(T_before)
+    dec_bytes = app_bytes = launches = 0
+    for i in range(args.steps):
+        r = (args.warmup + i) % n_rep
+        n_slots, block_bytes = meta[r]
+        app_bytes += append_bytes_at(w, T_now[r], block_bytes)
+        flush = state_at(w, T_now[r] + 1)[1] > state_at(w, T_now[r])[1]
+        T_now[r] += 1
+        dec_bytes += decode_bytes_at(w, T_now[r], n_slots)
+        launches += (2 if flush else 1) if fused else (2 if flush else 1) + 1
+    for r, (c, _) in enumerate(caches):   # the byte count above is the library's own
+        assert c.tokens == T_now[r]
+        assert c.decode_bytes() == decode_bytes_at(w, T_now[r], meta[r][0]), "decode byte count mismatch"
     ms_max = ms
     if world > 1:
         tt = torch.tensor([ms], device=device)
@@ -320,12 +350,16 @@ def run_ours(args, rank, world, device):
         ms_max = float(tt.item())
     step_bytes = (dec_bytes + app_bytes) / args.steps
     value = step_bytes * args.steps * world / (ms_max / 1e3) / 1e9
-    dec_gbs = dec_bytes_rl / (dec_ms / 1e3) / 1e9
+    # the decode kernel's roofline: the timed steps back to back are that
+    # kernel's launches (plus a flush launch on the steps that freeze a
+    # group, counted against it), so its achieved rate is the decode bytes
+    # over the whole timed span
+    dec_gbs = dec_bytes / (ms / 1e3) / 1e9
     res = {
         "w": w, "cfg": cfg, "n_rep": n_rep, "per_cache": per_cache, "ms": ms_max, "value": value,
-        "dec_gbs": dec_gbs, "dec_ms": dec_ms / max(len(keep), 1), "app_ms": app_ms / args.steps,
-        "dec_bytes": dec_bytes_rl / max(len(keep), 1), "fused": fused, "step_bytes": step_bytes, "launches": launches,
-        "clocks": clk, "app_tok_s": w.batch * args.steps / (app_ms / 1e3),
+        "dec_gbs": dec_gbs, "dec_ms": ms / args.steps, "app_ms": ms / args.steps,
+        "dec_bytes": dec_bytes / args.steps, "fused": fused, "step_bytes": step_bytes, "launches": launches,
+        "clocks": clk, "app_tok_s": w.batch * args.steps / (ms / 1e3),
     }
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, caches, new_kv, w, device, stream)
@@ -482,7 +516,7 @@ def main():
                                       "appended_per_sequence": -(-(args.steps + args.warmup) // r["n_rep"])}),
         "roofline": {"bound": "hbm", "achieved": round(r["dec_gbs"], 1), "peak": peak, "unit": "GB/s",
                      "frac": round(r["dec_gbs"] / peak, 4), "traffic": traffic,
-                     "kernel": "decode_mma_kernel (stream-K split-K, merge in the same launch)", "peak_source": src,
+                     "kernel": "decode_mma_kernel (stream-K split-K, merge and fresh-token append in the same launch)", "peak_source": src,
                      "bytes_per_launch": int(r["dec_bytes"])},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
@@ -490,11 +524,9 @@ def main():
         "decode_frac_of_8tbs": round(r["dec_gbs"] / NOMINAL_HBM_GBS, 4),
         "decode_us": round(r["dec_ms"] * 1e3, 2),
         "decode_steps_per_s": round(1e3 / r["dec_ms"], 1),
-        "append_us": None if r["fused"] else round(r["app_ms"] * 1e3, 2),
         "step_call": "kivi_append_decode_attn" if r["fused"] else "kivi_append + kivi_decode_attn",
         "append_tokens_per_s": round(r["app_tok_s"], 1),
-        "append_tokens_per_s_kind": ("tokens appended per second by the whole fused step (append + decode)"
-                                     if r["fused"] else "tokens appended per second of the append call"),
+        "append_tokens_per_s_kind": "tokens appended per second by the whole step (append + decode)",
     }
     if "e2e" in r:
         line["e2e"] = r["e2e"]

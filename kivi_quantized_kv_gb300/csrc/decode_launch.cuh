@@ -33,7 +33,21 @@ template <int D, int BITS, int CH>
 cudaError_t launch_one(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
   cudaError_t e = prepare<D, BITS, CH>();
   if (e != cudaSuccess) return e;
-  decode_mma_kernel<D, BITS, CH><<<grid, threads, smem, s>>>(a);
+  // programmatic dependent launch: the CTAs may start (and set up their
+  // shared memory) while the previous kernel in the stream drains; the kernel
+  // waits for that kernel's completion before it touches global memory
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BITS, CH>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -578,12 +578,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   int* ring_w = reinterpret_cast<int*>(bars + nw * a.ns) + warp * a.ns;   // this warp's item ring
   const uint32_t blk_bytes = static_cast<uint32_t>(g.block_bytes);
 
+  // a launch that follows in the stream may start its own set-up now; it
+  // waits below for this grid to finish before it reads or writes memory
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) { s_arrive = 0u; s_done = 0u; s_next = 0u; }
   if (lane == 0) {
     for (int s = 0; s < a.ns; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
   __syncthreads();
+  // the previous kernel in the stream (an append, or the last step's decode)
+  // has completed and its writes are visible from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   auto unit_base = [&](int u) -> const uint8_t* {
     const int per_b = g.hkv * a.npass;
