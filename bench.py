@@ -367,11 +367,16 @@ def run_ours(args, rank, world, device):
 
 
 def run_e2e(args, caches, new_kv, w, device, stream):
-    """The same step through the public API with host buffers: pinned host
-    K/V and q copied in, out copied back, inside the timed region."""
+    """The same step through the public API with host buffers: one
+    kivi_append_decode_attn_host call per step (kivi_append on a device copy
+    + kivi_decode_attn_host with --unfused), which copies the step's pinned
+    host K/V and q in and the output back, all inside the timed region."""
+    import ctypes
     import torch
+    from kivi_quantized_kv_gb300 import _abi
+    L = _abi.lib()
     n_rep = len(caches)
-    steps = min(args.steps, 100)
+    steps = min(args.steps, 200)
     g = torch.Generator().manual_seed(7)
     k_h = [torch.randn((w.batch, w.h_kv, 1, w.head_dim), generator=g).half().pin_memory() for _ in range(steps)]
     v_h = [torch.randn((w.batch, w.h_kv, 1, w.head_dim), generator=g).half().pin_memory() for _ in range(steps)]
@@ -379,29 +384,36 @@ def run_e2e(args, caches, new_kv, w, device, stream):
     out_h = torch.empty_like(q_h).pin_memory()
     k_d = torch.empty((w.batch, w.h_kv, 1, w.head_dim), dtype=torch.float16, device=device)
     v_d = torch.empty_like(k_d)
-    q_d = torch.empty((w.batch, w.h_q, w.head_dim), dtype=torch.float16, device=device)
-    out_d = torch.empty_like(q_d)
+    vp = ctypes.c_void_p
+    sp = vp(stream.cuda_stream)
+    T_before = [c.tokens for c, _ in caches]
+    meta = [(c.layout()["n_slots"], c.layout()["block_bytes"]) for c, _ in caches]
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    total = 0
     for s in range(steps):
-        c = caches[s % n_rep][0]
-        Lb = c.layout()
-        k_d.copy_(k_h[s], non_blocking=True)
-        v_d.copy_(v_h[s], non_blocking=True)
+        h = caches[s % n_rep][0]._h
         if args.unfused:
-            c.append(k_d, v_d)
-            c.decode_host(q_h, out_h)
+            k_d.copy_(k_h[s], non_blocking=True)
+            v_d.copy_(v_h[s], non_blocking=True)
+            st = L.kivi_append(h, vp(k_d.data_ptr()), vp(v_d.data_ptr()), 1, sp) or \
+                L.kivi_decode_attn_host(h, vp(q_h.data_ptr()), vp(out_h.data_ptr()), sp)
         else:
-            q_d.copy_(q_h, non_blocking=True)
-            c.append_decode(k_d, v_d, q_d, out=out_d)
-            out_h.copy_(out_d, non_blocking=True)
-        total += c.decode_bytes() + append_bytes(w, Lb, c.layout())
+            st = L.kivi_append_decode_attn_host(h, vp(k_h[s].data_ptr()), vp(v_h[s].data_ptr()),
+                                                vp(q_h.data_ptr()), vp(out_h.data_ptr()), sp)
+        if st != 0:
+            raise RuntimeError(_abi.status_string(st))
     t1.record(stream)
     torch.cuda.synchronize(device)
     ms = t0.elapsed_time(t1)
+    total = 0
+    T_now = list(T_before)
+    for s in range(steps):
+        r = s % n_rep
+        total += append_bytes_at(w, T_now[r], meta[r][1])
+        T_now[r] += 1
+        total += decode_bytes_at(w, T_now[r], meta[r][0])
     h2d = (2 * w.batch * w.h_kv + w.batch * w.h_q) * w.head_dim * 2
     d2h = w.batch * w.h_q * w.head_dim * 2
     return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -171,6 +171,15 @@ int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_str
 int kivi_append_decode_attn(kivi_cache* cache, const void* k_new, const void* v_new, const void* q, void* out,
                             void* cuda_stream);
 
+/* Same as kivi_append_decode_attn with host-resident k_new, v_new, q and out
+ * (pinned host memory gives asynchronous copies): copies the inputs into the
+ * arena's staging area, runs the step, copies the result back to out_host,
+ * all on `stream`; the call returns once the work is queued (synchronise the
+ * stream before reading out_host or reusing the input buffers).  Errors: as
+ * kivi_append_decode_attn. */
+int kivi_append_decode_attn_host(kivi_cache* cache, const void* k_host, const void* v_host, const void* q_host,
+                                 void* out_host, void* cuda_stream);
+
 /* Same as kivi_decode_attn with host-resident q and out (pinned host memory
  * gives asynchronous copies): copies q into the arena's staging area, runs
  * the decode, copies the result back to out_host, all on `stream`.  The call

@@ -16,7 +16,8 @@ KIVI_OK, KIVI_EINVAL, KIVI_EALIGN, KIVI_ECAPACITY, KIVI_ENOSPC, KIVI_ECUDA, KIVI
 # every entry point include/kivi.h declares
 EXPORTS = (
     "kivi_cache_bytes", "kivi_cache_create", "kivi_cache_destroy", "kivi_append",
-    "kivi_decode_attn", "kivi_append_decode_attn", "kivi_decode_attn_host", "kivi_decode_attn_noalloc",
+    "kivi_decode_attn", "kivi_append_decode_attn", "kivi_append_decode_attn_host", "kivi_decode_attn_host",
+    "kivi_decode_attn_noalloc",
     "kivi_set_num_splits", "kivi_cache_layout",
     "kivi_decode_bytes", "kivi_status_string",
 )
@@ -66,6 +67,7 @@ def lib():
         "kivi_append": (ctypes.c_int, [vp, vp, vp, i64, vp]),
         "kivi_decode_attn": (ctypes.c_int, [vp, vp, vp, vp]),
         "kivi_append_decode_attn": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
+        "kivi_append_decode_attn_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "kivi_decode_attn_host": (ctypes.c_int, [vp, vp, vp, vp]),
         "kivi_decode_attn_noalloc": (ctypes.c_int, [vp, vp, vp, vp]),
         "kivi_set_num_splits": (ctypes.c_int, [vp, i32]),

@@ -137,6 +137,22 @@ class KiviCache:
             ctypes.c_void_p(_stream_ptr(stream))), "kivi_append_decode_attn")
         return out
 
+    def append_decode_host(self, k_host: torch.Tensor, v_host: torch.Tensor, q_host: torch.Tensor,
+                           out_host: torch.Tensor, stream=None) -> torch.Tensor:
+        """append_decode with host-resident tensors (pin them for asynchronous
+        copies); the copies and the step are queued on `stream`."""
+        c = self.cfg
+        shapes = ((k_host, (c.batch, c.h_kv, 1, c.head_dim), "k_host"), (v_host, (c.batch, c.h_kv, 1, c.head_dim), "v_host"),
+                  (q_host, (c.batch, c.h_q, c.head_dim), "q_host"), (out_host, (c.batch, c.h_q, c.head_dim), "out_host"))
+        for t, shape, what in shapes:
+            if t.device.type != "cpu" or t.dtype != torch.float16 or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError(f"{what} must be a contiguous float16 CPU tensor of shape {shape}")
+        _abi.check(_abi.lib().kivi_append_decode_attn_host(
+            self._h, ctypes.c_void_p(k_host.data_ptr()), ctypes.c_void_p(v_host.data_ptr()),
+            ctypes.c_void_p(q_host.data_ptr()), ctypes.c_void_p(out_host.data_ptr()),
+            ctypes.c_void_p(_stream_ptr(stream))), "kivi_append_decode_attn_host")
+        return out_host
+
     def decode_host(self, q_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> torch.Tensor:
         """Host-resident q and out (pin them for asynchronous copies); the
         copies and the decode are queued on `stream`."""

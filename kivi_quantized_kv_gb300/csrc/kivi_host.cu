@@ -91,11 +91,14 @@ Geo geometry(const kivi_params& p) {
   g.ws_error = round_up(g.ws_counters + static_cast<int64_t>(p.batch) * p.h_kv * npass * 4, kAlign);
   g.ws_q = round_up(g.ws_error + 4, kAlign);
   g.ws_out = round_up(g.ws_q + bhq * d * 2, kAlign);
+  const int64_t bhkv = static_cast<int64_t>(p.batch) * p.h_kv;
+  g.ws_k = round_up(g.ws_out + bhq * d * 2, kAlign);
+  g.ws_v = round_up(g.ws_k + bhkv * d * 2, kAlign);
   return g;
 }
 
 int64_t arena_bytes_of(const Geo& g) {
-  return round_up(g.ws_out + static_cast<int64_t>(g.B) * g.hq * g.d * 2, kAlign);
+  return round_up(g.ws_v + static_cast<int64_t>(g.B) * g.hkv * g.d * 2, kAlign);
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ECUDA; }
@@ -241,6 +244,27 @@ int kivi_append_decode_attn(kivi_cache* c, const void* k_new, const void* v_new,
     return cuda_status(e);
   }
   return KIVI_OK;
+}
+
+int kivi_append_decode_attn_host(kivi_cache* c, const void* k_host, const void* v_host, const void* q_host,
+                                 void* out_host, void* cuda_stream) {
+  if (!c || !k_host || !v_host || !q_host || !out_host) return KIVI_ENULL;
+  const Geo& g = c->g;
+  if (g.window == 0 && c->T + 1 > c->p.max_tokens) return KIVI_ECAPACITY;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const size_t q_bytes = static_cast<size_t>(g.B) * g.hq * g.d * 2;
+  const size_t kv_bytes = static_cast<size_t>(g.B) * g.hkv * g.d * 2;
+  void* dk = c->arena + g.ws_k;
+  void* dv = c->arena + g.ws_v;
+  void* dq = c->arena + g.ws_q;
+  void* dout = c->arena + g.ws_out;
+  if (cudaMemcpyAsync(dk, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(dq, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return KIVI_ECUDA;
+  const int st = kivi_append_decode_attn(c, dk, dv, dq, dout, cuda_stream);
+  if (st != KIVI_OK) return st;
+  return cuda_status(cudaMemcpyAsync(out_host, dout, q_bytes, cudaMemcpyDeviceToHost, s));
 }
 
 int kivi_decode_attn_host(kivi_cache* c, const void* q_host, void* out_host, void* cuda_stream) {

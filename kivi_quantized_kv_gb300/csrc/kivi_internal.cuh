@@ -21,6 +21,7 @@ struct Geo {
   int64_t ws_counters;   // arena offset of the per-unit merge counters
   int64_t ws_error;      // arena offset of the device error word
   int64_t ws_q, ws_out;  // arena offsets of the host-call staging buffers
+  int64_t ws_k, ws_v;    // staging of one new token per sequence (fused host-buffer step)
   int32_t max_splits;    // CTAs that may share one unit (partial records - 2)
   int32_t split_stride;  // partial records per query head
 };

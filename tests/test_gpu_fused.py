@@ -100,3 +100,23 @@ def test_fused_step_errors_leave_state_untouched():
     assert L.kivi_append_decode_attn(c._h, None, ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(q.data_ptr()),
                                      ctypes.c_void_p(q.data_ptr()), None) == _abi.KIVI_ENULL
     assert c.tokens == 3
+
+
+def test_fused_step_with_host_buffers_matches_device_buffers():
+    """kivi_append_decode_attn_host (pinned host K/V/q/out) leaves the same
+    cache bytes and output as the device-buffer step."""
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
+    cfg = KiviConfig(bits=4, group=16, residual=32, sinks=2, h_q=8, h_kv=2, head_dim=128, batch=2, max_tokens=120)
+    a, b = KiviCache(cfg), KiviCache(cfg)
+    k, v = random_stream(cfg, 100, seed=21)
+    for t in range(100):
+        kt, vt = k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous()
+        q = random_q(cfg, 7 * t)
+        out_d = a.append_decode(kt.cuda(), vt.cuda(), q.cuda())
+        # pinned inputs held until the queued copies have run
+        k_h, v_h, q_h = kt.pin_memory(), vt.pin_memory(), q.pin_memory()
+        out_h = torch.empty_like(q).pin_memory()
+        b.append_decode_host(k_h, v_h, q_h, out_h)
+        torch.cuda.synchronize()
+        assert torch.equal(out_h, out_d.cpu())
+    assert torch.equal(a.cache_region(), b.cache_region())
