@@ -959,18 +959,22 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
           for (int i = 0; i < TPL; ++i)
             if (a_grp + s0 + TPL * r + i < lo_pos) sv[i] = -INFINITY;
         }
-        // (4) online softmax for head c, lazy rescale
+        // (4) online softmax for head c, lazy rescale: the head maxima are
+        // reduced only when some lane's score exceeds its head's running max
+        // by more than 2^8 (a warp vote; rare after a unit's first group)
         float mx = sv[0];
 #pragma unroll
         for (int i = 1; i < TPL; ++i) mx = fmaxf(mx, sv[i]);
-        mx = warp_max_rows(mx);
-        if (mx > res_m + kRescale) {   // uniform over the 8 lanes of head c
-          const float corr = (res_m == -INFINITY) ? 0.f : ex2(res_m - mx);
-          res_m = mx;
-          res_l *= corr;
-          res_mn *= corr;
+        if (__any_sync(0xffffffffu, mx > res_m + kRescale)) {
+          mx = warp_max_rows(mx);
+          if (mx > res_m + kRescale) {   // uniform over the 8 lanes of head c
+            const float corr = (res_m == -INFINITY) ? 0.f : ex2(res_m - mx);
+            res_m = mx;
+            res_l *= corr;
+            res_mn *= corr;
 #pragma unroll
-          for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
+            for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
+          }
         }
         const float mref = (res_m == -INFINITY) ? 0.f : res_m;   // every score so far -inf: p = 0
         float pd[TPL];
