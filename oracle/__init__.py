@@ -73,6 +73,7 @@ def lib():
         "ko_arena": (vp, [vp]),
         "ko_dequant_unit": (ctypes.c_int, [vp, ctypes.c_int32, ctypes.c_int32, f64p, f64p, u8p]),
         "ko_decode_attn": (ctypes.c_int, [vp, u16p, f64p, ctypes.c_int32]),
+        "ko_prefill_attn": (ctypes.c_int, [vp, u16p, ctypes.c_int64, f64p, ctypes.c_int32]),
         "ko_decode_bytes": (ctypes.c_int64, [vp]),
     }
     for name, (res, args) in sig.items():
@@ -248,6 +249,16 @@ class Cache:
         out = np.zeros(qq.shape, dtype=np.float64)
         rc = lib().ko_decode_attn(self._h, _ptr(qq, ctypes.c_uint16), _ptr(out, ctypes.c_double), threads)
         assert rc == 0
+        return out
+
+    def prefill_attn(self, q, threads: int = 1) -> np.ndarray:
+        """q: [B, M, H_q, d] fp16, the M newest tokens as queries -> out [B, M, H_q, d] fp64."""
+        qq = _u16(q)
+        assert qq.ndim == 4 and qq.shape[0] == self.p.batch and qq.shape[2:] == (self.p.h_q, self.p.head_dim)
+        out = np.zeros(qq.shape, dtype=np.float64)
+        rc = lib().ko_prefill_attn(self._h, _ptr(qq, ctypes.c_uint16), qq.shape[1], _ptr(out, ctypes.c_double),
+                                   threads)
+        assert rc == 0, rc
         return out
 
     def decode_bytes(self) -> int:

@@ -306,24 +306,24 @@ void flush_group(ko_cache& c, uint8_t* unit, int64_t g) {
   }
 }
 
-// Dequantized keys/values of every token of one unit, fp64, plus visibility.
-void dequant_unit(const ko_cache& c, int64_t b_idx, int64_t h, double* K, double* V, uint8_t* vis) {
+// Dequantized keys/values of every token of one unit, fp64, and which tokens
+// the cache still holds (res[a] = 0 once a's group slot was overwritten).
+void dequant_resident(const ko_cache& c, int64_t b_idx, int64_t h, double* K, double* V, uint8_t* res) {
   const ko_params& p = c.p;
   const int d = p.head_dim, G = p.group, b = p.bits, R = p.residual, S = p.sinks;
   const uint8_t* unit = unit_ptr(c, b_idx, h);
   const int64_t T = c.T;
-  const int64_t lo = (p.window > 0) ? T - p.window : 0;   // window start
   std::vector<uint8_t> row(std::max(d, G));
   for (int64_t a = 0; a < T; ++a) {
     double* kr = K + a * d;
     double* vr = V + a * d;
-    vis[a] = 0;
+    res[a] = 0;
     if (a < S) {   // sink: fp32 as stored, always visible
       for (int ch = 0; ch < d; ++ch) {
         kr[ch] = get_f32(unit + c.L.sink_k + (a * d + ch) * 4);
         vr[ch] = get_f32(unit + c.L.sink_v + (a * d + ch) * 4);
       }
-      vis[a] = 1;
+      res[a] = 1;
       continue;
     }
     const int64_t g = (a - S) / G;
@@ -352,10 +352,44 @@ void dequant_unit(const ko_cache& c, int64_t b_idx, int64_t h, double* K, double
         vr[ch] = f16_to_f32(get_u16(unit + c.L.res_v + (ring_slot * d + ch) * 2));
       }
     }
-    // reading: with a window, sinks stay visible and every other token is
-    // visible when it is among the most recent W tokens.
-    vis[a] = (a >= lo) ? 1 : 0;
+    res[a] = 1;
   }
+}
+
+// Dequantized keys/values of one unit plus visibility for a query at the
+// newest position T - 1.  Reading: with a window, sinks stay visible and every
+// other token is visible when it is among the most recent W tokens.
+void dequant_unit(const ko_cache& c, int64_t b_idx, int64_t h, double* K, double* V, uint8_t* vis) {
+  dequant_resident(c, b_idx, h, K, V, vis);
+  const int64_t lo = (c.p.window > 0) ? c.T - c.p.window : 0;   // window start
+  for (int64_t a = c.p.sinks; a < c.T; ++a)
+    if (a < lo) vis[a] = 0;
+}
+
+// softmax(q Kᵀ / sqrt(d)) V of one query row over the visible tokens, two
+// passes in fp64 (scores and their max, then the weights); all zero when no
+// token is visible.
+void attend_row(const double* qd, const double* K, const double* V, const uint8_t* vis, int64_t T, int d,
+                double* o) {
+  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(d));
+  std::vector<double> s(static_cast<size_t>(T));
+  double m = -std::numeric_limits<double>::infinity();
+  for (int64_t a = 0; a < T; ++a) {
+    if (!vis[a]) continue;
+    double acc = 0.0;
+    for (int ch = 0; ch < d; ++ch) acc += qd[ch] * K[a * d + ch];
+    s[a] = acc * inv_sqrt_d;
+    m = std::max(m, s[a]);
+  }
+  double l = 0.0;
+  std::vector<double> acc(d, 0.0);
+  for (int64_t a = 0; a < T; ++a) {
+    if (!vis[a]) continue;
+    const double w = std::exp(s[a] - m);
+    l += w;
+    for (int ch = 0; ch < d; ++ch) acc[ch] += w * V[a * d + ch];
+  }
+  for (int ch = 0; ch < d; ++ch) o[ch] = (l > 0.0) ? acc[ch] / l : 0.0;
 }
 
 // fp64 decode attention of one unit (all query heads mapped to this kv head).
@@ -368,31 +402,43 @@ void attend_unit(const ko_cache& c, int64_t b_idx, int64_t h, const uint16_t* q,
   std::vector<double> K(static_cast<size_t>(T) * d), V(static_cast<size_t>(T) * d);
   std::vector<uint8_t> vis(static_cast<size_t>(T));
   dequant_unit(c, b_idx, h, K.data(), V.data(), vis.data());
-  std::vector<double> s(static_cast<size_t>(T));
-  const double inv_sqrt_d = 1.0 / std::sqrt(static_cast<double>(d));
+  std::vector<double> qd(d);
   for (int r = 0; r < rep; ++r) {
     const int64_t hq = h * rep + r;
     const uint16_t* qh = q + (b_idx * p.h_q + hq) * d;
-    double* oh = out + (b_idx * p.h_q + hq) * d;
-    std::vector<double> qd(d);
     for (int ch = 0; ch < d; ++ch) qd[ch] = f16_to_f32(qh[ch]);
-    double m = -std::numeric_limits<double>::infinity();
-    for (int64_t a = 0; a < T; ++a) {
-      if (!vis[a]) continue;
-      double acc = 0.0;
-      for (int ch = 0; ch < d; ++ch) acc += qd[ch] * K[a * d + ch];
-      s[a] = acc * inv_sqrt_d;
-      m = std::max(m, s[a]);
+    attend_row(qd.data(), K.data(), V.data(), vis.data(), T, d, out + (b_idx * p.h_q + hq) * d);
+  }
+}
+
+// fp64 causal attention of the M newest tokens of one unit as queries, over
+// the cache as it stands (chunked prefill: the chunk was appended first, then
+// each of its tokens attends to what precedes it and to itself; kvquant++
+// README, long-document example, where prefill_chunk_size bounds each
+// attention step while the context accumulates in the cache).
+// Query j sits at position P = T - M + j; q and out are [B][M][H_q][d].
+// Token a is visible to it when the cache still holds a, a <= P, and, with a
+// window, a is a sink or among the W tokens ending at P.  Tokens of the chunk
+// are read as the cache holds them now (fp16 in the ring, codes once frozen).
+void attend_unit_causal(const ko_cache& c, int64_t b_idx, int64_t h, const uint16_t* q, int64_t M,
+                        double* out) {
+  const ko_params& p = c.p;
+  const int d = p.head_dim;
+  const int64_t T = c.T, S = p.sinks;
+  const int rep = p.h_q / p.h_kv;
+  std::vector<double> K(static_cast<size_t>(T) * d), V(static_cast<size_t>(T) * d);
+  std::vector<uint8_t> res(static_cast<size_t>(T)), vis(static_cast<size_t>(T));
+  dequant_resident(c, b_idx, h, K.data(), V.data(), res.data());
+  std::vector<double> qd(d);
+  for (int64_t j = 0; j < M; ++j) {
+    const int64_t P = T - M + j;
+    const int64_t lo = (p.window > 0) ? P + 1 - p.window : 0;
+    for (int64_t a = 0; a < T; ++a) vis[a] = (res[a] && a <= P && (a < S || a >= lo)) ? 1 : 0;
+    for (int r = 0; r < rep; ++r) {
+      const int64_t row = (b_idx * M + j) * p.h_q + h * rep + r;
+      for (int ch = 0; ch < d; ++ch) qd[ch] = f16_to_f32(q[row * d + ch]);
+      attend_row(qd.data(), K.data(), V.data(), vis.data(), T, d, out + row * d);
     }
-    double l = 0.0;
-    std::vector<double> o(d, 0.0);
-    for (int64_t a = 0; a < T; ++a) {
-      if (!vis[a]) continue;
-      const double w = std::exp(s[a] - m);
-      l += w;
-      for (int ch = 0; ch < d; ++ch) o[ch] += w * V[a * d + ch];
-    }
-    for (int ch = 0; ch < d; ++ch) oh[ch] = (l > 0.0) ? o[ch] / l : 0.0;
   }
 }
 
@@ -507,6 +553,21 @@ int ko_decode_attn(const ko_cache* c, const uint16_t* q, double* out, int32_t th
   const int nt = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(threads, units)));
   auto work = [&](int tid) {
     for (int64_t u = tid; u < units; u += nt) attend_unit(*c, u / c->p.h_kv, u % c->p.h_kv, q, out);
+  };
+  if (nt == 1) { work(0); return kOk; }
+  std::vector<std::thread> pool;
+  for (int t = 0; t < nt; ++t) pool.emplace_back(work, t);
+  for (auto& th : pool) th.join();
+  return kOk;
+}
+
+int ko_prefill_attn(const ko_cache* c, const uint16_t* q, int64_t n_queries, double* out, int32_t threads) {
+  if (!c || n_queries < 1 || n_queries > c->T) return kInvalid;
+  const int64_t units = static_cast<int64_t>(c->p.batch) * c->p.h_kv;
+  const int nt = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(threads, units)));
+  auto work = [&](int tid) {
+    for (int64_t u = tid; u < units; u += nt)
+      attend_unit_causal(*c, u / c->p.h_kv, u % c->p.h_kv, q, n_queries, out);
   };
   if (nt == 1) { work(0); return kOk; }
   std::vector<std::thread> pool;

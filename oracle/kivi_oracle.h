@@ -97,6 +97,12 @@ int ko_dequant_unit(const ko_cache* c, int32_t b, int32_t hkv, double* k_hat, do
  * Work is spread over `threads` host threads by (batch, kv-head) unit. */
 int ko_decode_attn(const ko_cache* c, const uint16_t* q, double* out, int32_t threads);
 
+/* Causal attention of the n_queries newest tokens, fp64: q [B][M][H_q][d]
+ * fp16 -> out [B][M][H_q][d] fp64, query j at position T - M + j attending to
+ * the resident tokens a <= T - M + j (sinks, and with a window the W tokens
+ * ending at its own position).  1 <= n_queries <= T, else 1 (invalid). */
+int ko_prefill_attn(const ko_cache* c, const uint16_t* q, int64_t n_queries, double* out, int32_t threads);
+
 /* Algorithmic bytes one decode pass must read/write at the current state. */
 int64_t ko_decode_bytes(const ko_cache* c);
 
