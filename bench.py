@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--unfused", action="store_true", help="append and decode as two calls (two launches)")
+    ap.add_argument("--prefill", type=int, default=0, metavar="M",
+                    help="chunked prefill instead of decode: a step appends M tokens per sequence and runs "
+                         "the causal attention of those M queries (kivi_append + kivi_prefill_attn)")
     return ap.parse_args()
 
 
@@ -232,6 +235,42 @@ def decode_bytes_at(w, T, n_slots):
     return per_unit * w.batch * w.h_kv + 4 * d * w.batch * w.h_q
 
 
+def prefill_bytes_at(w, T, m, n_slots):
+    """Algorithmic bytes of one causal attention of the m newest tokens
+    after T tokens: every token some query sees, counted as decode_bytes_at
+    counts them (the oldest query's window reaches furthest back), plus q
+    and out for m rows; the same sum as kivi_prefill_bytes."""
+    n_sink, ng, n_res = state_at(w, T)
+    first = max(ng - n_slots, 0)
+    lo = T - m + 1 - w.window if w.window > 0 else 0
+    if w.window > 0 and lo > w.sinks:
+        first = max(first, (lo - w.sinks) // w.group)
+    first = min(first, ng)
+    tq = touched = 0
+    for grp in range(first, ng):
+        a0 = w.sinks + grp * w.group
+        vis = a0 + w.group - max(a0, lo)
+        if vis > 0:
+            tq += vis
+            touched += 1
+    d = w.head_dim
+    per_unit = 2 * tq * d * w.bits // 8 + 4 * d * touched + 4 * tq + 4 * d * n_res + 8 * d * n_sink
+    return per_unit * w.batch * w.h_kv + 4 * d * w.batch * m * w.h_q
+
+
+def prefill_flops_at(w, T, m, n_slots):
+    """Algorithmic FLOPs of that attention: 4 d per (query row, visible
+    token) (q·k and p·v, a multiply and an add each)."""
+    _, ng, _ = state_at(w, T)
+    first_pos = w.sinks + max(ng - n_slots, 0) * w.group if w.window > 0 else 0   # oldest resident non-sink
+    pairs = 0
+    for j in range(m):
+        P = T - m + j
+        start = max(w.sinks, first_pos, P + 1 - w.window) if w.window > 0 else w.sinks
+        pairs += min(P + 1, w.sinks) + max(0, P - start + 1)
+    return 4 * w.head_dim * pairs * w.batch * w.h_q
+
+
 def append_bytes_at(w, T, block_bytes):
     """Algorithmic bytes of appending one token per sequence to T tokens."""
     new_groups = state_at(w, T + 1)[1] - state_at(w, T)[1]
@@ -364,6 +403,130 @@ def run_ours(args, rank, world, device):
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, caches, new_kv, w, device, stream)
     return res
+
+
+def run_prefill(args, device):
+    """Chunked prefill: a step appends an M-token chunk to every sequence
+    (kivi_append) and runs the causal attention of the chunk's M queries over
+    the packed cache (kivi_prefill_attn).  The replicas start M tokens short
+    of the workload's length, so the first chunk on each ends at it; later
+    chunks grow it (the byte and FLOP counts follow each replica's length).
+    The attention launches are timed on their own with CUDA events around
+    each call on the launching stream."""
+    import ctypes
+    import torch
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig, _abi, cache_bytes
+    from kivi_quantized_kv_gb300.synth import KVStream
+
+    w = workload(args.workload)
+    m = args.prefill
+    total_steps = args.steps + args.warmup
+    l2 = 129 * 1024 * 1024
+    cfg0 = KiviConfig.from_workload(w)
+    n_rep = args.replicas or max(2, -(-4 * l2 // cache_bytes(cfg0)))
+    per_rep = -(-total_steps // n_rep)
+    cfg = cfg0 if w.window else KiviConfig(**{**cfg0.__dict__, "max_tokens": w.tokens + per_rep * m})
+    per_cache = cache_bytes(cfg)
+    stream = torch.cuda.current_stream(device)
+    caches = []
+    for r in range(n_rep):
+        c = KiviCache(cfg, device=device)
+        kv = KVStream(w.with_(seed=w.seed + 100 * r), device=device)
+        t = 0
+        while t < w.tokens - m:
+            n = min(4096, w.tokens - m - t)
+            k, v = kv.next(n)
+            c.append(k, v)
+            t += n
+        caches.append((c, kv))
+    chunks = [caches[s % n_rep][1].next(m) for s in range(total_steps)]
+    g = torch.Generator(device=device).manual_seed(w.seed + 4242)
+    qs = [torch.randn((w.batch, m, w.h_q, w.head_dim), generator=g, device=device).half() for _ in range(4)]
+    out = torch.empty_like(qs[0])
+    need = caches[0][0].prefill_scratch_bytes(m)
+    scratch = torch.empty(need, dtype=torch.uint8, device=device)
+    torch.cuda.synchronize(device)
+    L = _abi.lib()
+    vp = ctypes.c_void_p
+    sp = vp(stream.cuda_stream)
+    args_of = [(caches[s % n_rep][0]._h, vp(chunks[s][0].data_ptr()), vp(chunks[s][1].data_ptr()),
+                vp(qs[s % len(qs)].data_ptr())) for s in range(total_steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(s, e=None):
+        h, kp, vq, qp = args_of[s]
+        st = L.kivi_append(h, kp, vq, m, sp)
+        if e is not None:
+            e[0].record(stream)
+        st = st or L.kivi_prefill_attn(h, qp, vp(out.data_ptr()), m, vp(scratch.data_ptr()), need, sp)
+        if e is not None:
+            e[1].record(stream)
+        if st != 0:
+            raise RuntimeError(_abi.status_string(st))
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize(device)
+    T_now = [c.tokens for c, _ in caches]
+    meta = [(c.layout()["n_slots"], c.layout()["block_bytes"]) for c, _ in caches]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device)
+    clocks.start()
+    time.sleep(0.05)
+    clocks.mark_begin()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clocks.mark_end()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev)
+    attn_bytes = attn_flops = launches = 0
+    for i in range(args.steps):
+        r = (args.warmup + i) % n_rep
+        T0 = T_now[r]
+        T_now[r] += m
+        flush = state_at(w, T_now[r])[1] > state_at(w, T0)[1]
+        attn_bytes += prefill_bytes_at(w, T_now[r], m, meta[r][0])
+        attn_flops += prefill_flops_at(w, T_now[r], m, meta[r][0])
+        launches += (3 if flush else 2)
+    for r, (c, _) in enumerate(caches):   # the byte count above is the library's own
+        assert c.tokens == T_now[r]
+        assert c.prefill_bytes(m) == prefill_bytes_at(w, T_now[r], m, meta[r][0]), "prefill byte count mismatch"
+        assert c.read_error() == 0
+    peaks, src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    tensor = float(peaks.get("bf16_tflops", 1900.0))
+    gbs = attn_bytes / (attn_ms / 1e3) / 1e9
+    tflops = attn_flops / (attn_ms / 1e3) / 1e12
+    # the roofline the attention launch is bound by: the larger of its
+    # memory time and its tensor time at the measured peaks
+    t_mem = attn_bytes / (hbm * 1e9)
+    t_math = attn_flops / (tensor * 1e12)
+    if t_mem >= t_math:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tensor, "unit": "TFLOP/s",
+                "frac": round(tflops / tensor, 4)}
+    roof.update({"traffic": None, "peak_source": src, "kernel": "decode_mma_kernel (several query tokens, causal masks)",
+                 "bytes_per_launch": int(attn_bytes / args.steps), "flops_per_launch": int(attn_flops / args.steps),
+                 "hbm_frac": round(gbs / hbm, 4), "tensor_frac": round(tflops / tensor, 5)})
+    tok = w.batch * m * args.steps
+    return {
+        "metric": f"chunked prefill query tokens/s (append {m} tokens + their causal attention over the packed cache)",
+        "value": round(tok / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32", "data": "synthetic",
+        "config": workload_config(w, {"chunk": m, "parallelism": "replicas1",
+                                      "l2": f"{n_rep} rotating cache replicas x {per_cache / 1e6:.0f} MB (> 4x 129 MB L2)",
+                                      "tokens_at_first_chunk": w.tokens}),
+        "roofline": roof, "gpu_launches": launches, "clocks": clk,
+        "attn_us": round(attn_ms * 1e3 / args.steps, 2), "attn_gbs": round(gbs, 1), "attn_tflops": round(tflops, 2),
+        "step_call": "kivi_append + kivi_prefill_attn",
+    }
 
 
 def run_e2e(args, caches, new_kv, w, device, stream):
@@ -510,6 +673,11 @@ def main():
     import __graft_entry__ as ge
     ge.build()
 
+    if args.prefill > 0:
+        if world > 1:
+            raise SystemExit("--prefill runs on one GPU")
+        print(json.dumps(run_prefill(args, device)), flush=True)
+        return
     r = run_ours(args, rank, world, device)
     if rank != 0:
         if world > 1:

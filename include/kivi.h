@@ -21,9 +21,10 @@
  *     shape; "Relationship to other PRs": a bounded sliding window composes
  *     with the quantized storage.
  *
- * Memory ownership: the caller allocates every device buffer (the arena and
- * all inputs/outputs).  The library allocates only the small host-side handle
- * and never allocates, frees or synchronises device memory.
+ * Memory ownership: the caller allocates every device buffer (the arena,
+ * prefill scratch and all inputs/outputs).  The library allocates only the
+ * small host-side handle and never allocates or frees device memory; only
+ * kivi_read_error synchronises a stream.
  *
  * Concurrency: every call is asynchronous on the given CUDA stream (NULL =
  * the legacy default stream).  A handle must not be used from two streams or
@@ -186,6 +187,50 @@ int kivi_append_decode_attn_host(kivi_cache* cache, const void* k_host, const vo
  * returns once the work is queued; synchronise the stream before reading
  * out_host.  Errors: as kivi_decode_attn. */
 int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host, void* cuda_stream);
+
+/* Causal attention of the n_queries newest tokens of every sequence over the
+ * cache (chunked prefill: kvquant++ README, long-document example, where
+ * prefill_chunk_size bounds each attention step to one chunk of queries while
+ * the context accumulates in the cache; the per-query attention is that of
+ * kivi_decode_attn).  Append the chunk first (kivi_append), then call this
+ * with the chunk's queries.
+ *   q    device fp16 [B][n_queries][h_q][d], contiguous, 16-byte aligned;
+ *        query j of a sequence is the token at position T - n_queries + j.
+ *   out  device fp16 [B][n_queries][h_q][d], contiguous, 16-byte aligned.
+ *   scratch  device memory of at least kivi_prefill_scratch_bytes(cache,
+ *        n_queries) bytes, 256-byte aligned, owned by the caller; its
+ *        contents are scratch (the call clears what it needs on `stream`).
+ * Query j attends to the tokens at positions <= T - n_queries + j that the
+ * cache holds: the sinks (fp32), frozen groups (dequantized in registers) and
+ * the ring (fp16), as the cache stands after the append (a chunk token that
+ * the append froze is read from its codes); with a window, the sinks plus the
+ * W tokens ending at the query's own position, less any whose group slot the
+ * window's ring has reused (a chunk longer than about R tokens can lose the
+ * oldest part of its first queries' windows).  The newest query's row equals
+ * kivi_decode_attn's output for it.  Work: as kivi_decode_attn with n_queries
+ * times the query rows per kv head, each row masked to its own positions.
+ * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536), EALIGN, ENOSPC
+ * (scratch too small), ECUDA. */
+int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_queries, void* scratch,
+                      size_t scratch_bytes, void* cuda_stream);
+
+/* Device scratch bytes kivi_prefill_attn needs for n_queries query tokens per
+ * sequence (independent of T), or 0 for a NULL handle or an n_queries outside
+ * [1, 65536].  Host only. */
+size_t kivi_prefill_scratch_bytes(const kivi_cache* cache, int64_t n_queries);
+
+/* Algorithmic bytes of one kivi_prefill_attn call at the current state: the
+ * cache bytes of every token some query sees (as kivi_decode_bytes counts
+ * them) plus q and out.  -1 for a NULL handle or an invalid n_queries. */
+int64_t kivi_prefill_bytes(const kivi_cache* cache, int64_t n_queries);
+
+/* Reads and clears the device error word that the cache's attention launches
+ * set instead of hanging: bit 0 = a bulk copy into shared memory did not
+ * complete within its bounded wait (2 s), bit 1 = a warp waited in vain for
+ * its combine slot to be released.  Either bit means the affected outputs are
+ * not valid.  Unlike every other call this one synchronises `stream` (it
+ * returns the value).  Errors: ENULL, ECUDA. */
+int kivi_read_error(kivi_cache* cache, uint32_t* flags, void* cuda_stream);
 
 /* Decode attention that allocates nothing (the method's pages have no
  * counterpart: this is a deployment variant of kivi_decode_attn).  For callers

@@ -17,8 +17,8 @@ KIVI_OK, KIVI_EINVAL, KIVI_EALIGN, KIVI_ECAPACITY, KIVI_ENOSPC, KIVI_ECUDA, KIVI
 EXPORTS = (
     "kivi_cache_bytes", "kivi_cache_create", "kivi_cache_destroy", "kivi_append",
     "kivi_decode_attn", "kivi_append_decode_attn", "kivi_append_decode_attn_host", "kivi_decode_attn_host",
-    "kivi_decode_attn_noalloc",
-    "kivi_set_num_splits", "kivi_cache_layout",
+    "kivi_decode_attn_noalloc", "kivi_prefill_attn", "kivi_prefill_scratch_bytes", "kivi_prefill_bytes",
+    "kivi_read_error", "kivi_set_num_splits", "kivi_cache_layout",
     "kivi_decode_bytes", "kivi_status_string",
 )
 
@@ -70,6 +70,10 @@ def lib():
         "kivi_append_decode_attn_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "kivi_decode_attn_host": (ctypes.c_int, [vp, vp, vp, vp]),
         "kivi_decode_attn_noalloc": (ctypes.c_int, [vp, vp, vp, vp]),
+        "kivi_prefill_attn": (ctypes.c_int, [vp, vp, vp, i64, vp, ctypes.c_size_t, vp]),
+        "kivi_prefill_scratch_bytes": (ctypes.c_size_t, [vp, i64]),
+        "kivi_prefill_bytes": (i64, [vp, i64]),
+        "kivi_read_error": (ctypes.c_int, [vp, P(ctypes.c_uint32), vp]),
         "kivi_set_num_splits": (ctypes.c_int, [vp, i32]),
         "kivi_cache_layout": (ctypes.c_int, [vp, P(KiviLayout)]),
         "kivi_decode_bytes": (i64, [vp]),

@@ -66,6 +66,7 @@ class KiviCache:
         if arena is None:
             arena = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         self.arena = arena
+        self._scratch = None   # prefill scratch, grown on demand
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
             _abi.check(L.kivi_cache_create(ctypes.byref(p), ctypes.c_void_p(arena.data_ptr()),
@@ -166,6 +167,46 @@ class KiviCache:
                                                     ctypes.c_void_p(_stream_ptr(stream))),
                    "kivi_decode_attn_host")
         return out_host
+
+    def prefill(self, q: torch.Tensor, out: torch.Tensor | None = None, scratch: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+        """Causal attention of the M newest tokens (append the chunk first):
+        q [B, M, H_q, d] float16 -> out [B, M, H_q, d] float16
+        (kivi_prefill_attn).  `scratch` is a uint8 device tensor of at least
+        prefill_scratch_bytes(M) bytes; by default the cache keeps one and
+        grows it as needed."""
+        c = self.cfg
+        m = q.shape[1] if q.dim() == 4 else -1
+        shape = (c.batch, m, c.h_q, c.head_dim)
+        self._check_io(q, shape, "q")
+        if out is None:
+            out = torch.empty(shape, dtype=torch.float16, device=self.arena.device)
+        self._check_io(out, shape, "out")
+        need = self.prefill_scratch_bytes(m)
+        if need == 0:
+            raise _abi.KiviError(_abi.KIVI_EINVAL, "kivi_prefill_scratch_bytes")
+        if scratch is None:
+            if self._scratch is None or self._scratch.numel() < need:
+                self._scratch = torch.empty(need, dtype=torch.uint8, device=self.arena.device)
+            scratch = self._scratch
+        _abi.check(_abi.lib().kivi_prefill_attn(self._h, ctypes.c_void_p(q.data_ptr()),
+                                                ctypes.c_void_p(out.data_ptr()), m,
+                                                ctypes.c_void_p(scratch.data_ptr()), scratch.numel(),
+                                                ctypes.c_void_p(_stream_ptr(stream))), "kivi_prefill_attn")
+        return out
+
+    def prefill_scratch_bytes(self, n_queries: int) -> int:
+        return int(_abi.lib().kivi_prefill_scratch_bytes(self._h, n_queries))
+
+    def prefill_bytes(self, n_queries: int) -> int:
+        return int(_abi.lib().kivi_prefill_bytes(self._h, n_queries))
+
+    def read_error(self, stream=None) -> int:
+        """Reads and clears the device error word (synchronises the stream)."""
+        flags = ctypes.c_uint32(0)
+        _abi.check(_abi.lib().kivi_read_error(self._h, ctypes.byref(flags), ctypes.c_void_p(_stream_ptr(stream))),
+                   "kivi_read_error")
+        return int(flags.value)
 
     def set_num_splits(self, n: int) -> None:
         _abi.check(_abi.lib().kivi_set_num_splits(self._h, n), "kivi_set_num_splits")

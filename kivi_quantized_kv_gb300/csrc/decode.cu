@@ -72,8 +72,9 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
   a.ns = sh.ns;
   a.stage_bytes = sh.stage_bytes;
   a.stride = stride;
-  a.npass = sh.npass;
-  a.units = g.B * g.hkv * sh.npass;
+  if (plan.nq < 1) return cudaErrorInvalidValue;
+  a.npass = (plan.nq * g.rep + 3) / 4;   // head passes over the nq * rep query rows of a kv head
+  a.units = g.B * g.hkv * a.npass;
   a.tc = plan.tc;
   a.uw = plan.n_vis_groups + plan.tc;
   // one wave of CTAs; each range holds at least one work position, and no unit

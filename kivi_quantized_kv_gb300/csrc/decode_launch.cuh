@@ -9,7 +9,7 @@
 namespace kivi {
 namespace mma {
 
-template <int D, int BITS, int CH>
+template <int D, int BITS, int CH, bool MQ>
 cudaError_t prepare() {
   // opt in to the largest dynamic shared memory once per instantiation
   static std::atomic<int> done{0};
@@ -20,18 +20,18 @@ cudaError_t prepare() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, decode_mma_kernel<D, BITS, CH>);
+  e = cudaFuncGetAttributes(&fa, decode_mma_kernel<D, BITS, CH, MQ>);
   if (e != cudaSuccess) return e;
   // the opt-in limit covers static + dynamic shared memory
-  e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, CH, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            optin - static_cast<int>(fa.sharedSizeBytes));
   if (e == cudaSuccess) done.store(1, std::memory_order_release);
   return e;
 }
 
-template <int D, int BITS, int CH>
+template <int D, int BITS, int CH, bool MQ>
 cudaError_t launch_one(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
-  cudaError_t e = prepare<D, BITS, CH>();
+  cudaError_t e = prepare<D, BITS, CH, MQ>();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the CTAs may start (and set up their
   // shared memory) while the previous kernel in the stream drains; the kernel
@@ -46,33 +46,44 @@ cudaError_t launch_one(const Args& a, dim3 grid, int threads, int smem, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BITS, CH>, a);
+  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BITS, CH, MQ>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D, int BITS, int CH>
+template <int D, int BITS, int CH, bool MQ>
 int occupancy_one(int threads, int smem) {
-  if (prepare<D, BITS, CH>() != cudaSuccess) return 1;
+  if (prepare<D, BITS, CH, MQ>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, BITS, CH>, threads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, BITS, CH, MQ>, threads, smem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
-template <int BITS>
-cudaError_t launch_bits(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+// one instantiation per (head dim, chunk of the group, several query tokens)
+template <int BITS, bool MQ>
+cudaError_t launch_mq(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
   const bool ch32 = (a.g.G % 32) == 0;
   if (a.g.d == 64)
-    return ch32 ? launch_one<64, BITS, 32>(a, grid, threads, smem, s) : launch_one<64, BITS, 16>(a, grid, threads, smem, s);
-  return ch32 ? launch_one<128, BITS, 32>(a, grid, threads, smem, s) : launch_one<128, BITS, 16>(a, grid, threads, smem, s);
+    return ch32 ? launch_one<64, BITS, 32, MQ>(a, grid, threads, smem, s)
+                : launch_one<64, BITS, 16, MQ>(a, grid, threads, smem, s);
+  return ch32 ? launch_one<128, BITS, 32, MQ>(a, grid, threads, smem, s)
+              : launch_one<128, BITS, 16, MQ>(a, grid, threads, smem, s);
 }
 
 template <int BITS>
+cudaError_t launch_bits(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+  return a.plan.nq > 1 ? launch_mq<BITS, true>(a, grid, threads, smem, s)
+                       : launch_mq<BITS, false>(a, grid, threads, smem, s);
+}
+
+// the multi-query instantiations have the same launch bounds and shared memory
+template <int BITS>
 int occupancy_bits(const Geo& g, int threads, int smem) {
   const bool ch32 = (g.G % 32) == 0;
-  if (g.d == 64) return ch32 ? occupancy_one<64, BITS, 32>(threads, smem) : occupancy_one<64, BITS, 16>(threads, smem);
-  return ch32 ? occupancy_one<128, BITS, 32>(threads, smem) : occupancy_one<128, BITS, 16>(threads, smem);
+  if (g.d == 64)
+    return ch32 ? occupancy_one<64, BITS, 32, false>(threads, smem) : occupancy_one<64, BITS, 16, false>(threads, smem);
+  return ch32 ? occupancy_one<128, BITS, 32, false>(threads, smem) : occupancy_one<128, BITS, 16, false>(threads, smem);
 }
 
 // defined in decode_b2.cu, decode_b4.cu, decode_b8.cu

@@ -6,7 +6,12 @@
 // kv head (tract #2329, "What's in the PR").
 //
 // Work split (stream-K).  A "unit" is one (sequence, kv head, head pass); a
-// head pass covers up to four query heads.  Unit u owns `uw` work positions:
+// head pass covers up to four query rows.  The rows of a kv head are its
+// query heads times the query tokens: nq = 1 for a decode, and nq = M for the
+// causal attention of a chunk's M newest tokens, where row v is query token
+// v / rep (position q_pos0 + v / rep) of head v % rep of the GQA group, and
+// each row sees only the tokens at or before its position (and, with a
+// window, within the W tokens ending there).  Unit u owns `uw` work positions:
 // its visible frozen groups, then `tc` positions for its tail (the fp32 sinks
 // in chunks of 4 tokens, then the fp16 ring in chunks of 8).  The units'
 // positions, laid end to end, are cut into one equal contiguous range per CTA,
@@ -73,14 +78,14 @@ struct Args {
   const uint8_t* arena;
   const __half* q;
   __half* out;
-  float* partials;      // [B][h_q][stride][d + 4]: o[d], m, l, 2 pad
+  float* partials;      // [B * nq * h_q][stride][d + 4]: o[d], m, l, 2 pad
   unsigned* counters;   // [units]: CTAs finished per unit
   unsigned* error;      // kErrCopy | kErrSlot
   DecodePlan plan;
   int32_t ns;           // copy stages per warp
   int32_t stage_bytes;  // bytes per stage (block bytes rounded up to 128)
   int32_t stride;       // partial records per (sequence, query head)
-  int32_t npass;        // head passes per kv head
+  int32_t npass;        // head passes (4 query rows each) per kv head: ceil(nq * rep / 4)
   int32_t units;        // B * h_kv * npass
   int32_t tc;           // work positions standing for one tail
   int64_t uw;           // work positions per unit: visible groups + tc
@@ -369,10 +374,24 @@ struct WarpSmem {
   static constexpr int kXch = CH == 32 ? 512 : 256;
 };
 
-// First query head of unit u (sequence, kv head, head pass).
-__device__ __forceinline__ int64_t unit_head0(const Args& a, int u) {
+// Row (of q, out and the partial records: [B][nq][h_q]) of query row hh of
+// unit u (sequence, kv head, head pass).  MQ: several query tokens per
+// sequence; otherwise nq = 1 and the rows of a pass are adjacent heads.
+template <bool MQ>
+__device__ __forceinline__ int64_t q_row(const Args& a, int u, int hh) {
   const int per_b = a.g.hkv * a.npass;
-  return static_cast<int64_t>(u / per_b) * a.g.hq + ((u % per_b) / a.npass) * a.g.rep + 4 * (u % a.npass);
+  const int bb = u / per_b, hk = (u % per_b) / a.npass;
+  if constexpr (MQ) {
+    const int v = 4 * (u % a.npass) + hh;   // row of the kv head: query token v / rep, head v % rep
+    return (static_cast<int64_t>(bb) * a.plan.nq + v / a.g.rep) * a.g.hq + hk * a.g.rep + v % a.g.rep;
+  } else {
+    return static_cast<int64_t>(bb) * a.g.hq + hk * a.g.rep + 4 * (u % a.npass) + hh;
+  }
+}
+// Query rows of unit u (at most four).
+template <bool MQ>
+__device__ __forceinline__ int unit_rows(const Args& a, int u) {
+  return min(4, (MQ ? a.plan.nq : 1) * a.g.rep - 4 * (u % a.npass));
 }
 
 // Merge of the `total` partial records (o[D], m, l, pad, pad) of one query
@@ -417,16 +436,16 @@ __device__ __forceinline__ void merge_partials(const float* base, int total, int
   }
 }
 
-// Merges channel pair i (head i / (D/2)) of the unit whose first query head
-// is head0 and writes it out.
-template <int D>
-__device__ __forceinline__ void merge_out(const Args& a, int64_t head0, int i, int total) {
+// Merges channel pair i (query row i / (D/2)) of unit u and writes it out.
+template <int D, bool MQ>
+__device__ __forceinline__ void merge_out(const Args& a, int u, int i, int total) {
   const int hh = i / (D / 2), ch = 2 * (i % (D / 2));
+  const int64_t row = q_row<MQ>(a, u, hh);
   float2 O;
   float L;
-  merge_partials<D>(a.partials + (head0 + hh) * a.stride * (D + 4), total, ch, O, L);
+  merge_partials<D>(a.partials + row * a.stride * (D + 4), total, ch, O, L);
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  *reinterpret_cast<__half2*>(a.out + (head0 + hh) * D + ch) = __floats2half2_rn(O.x * inv, O.y * inv);
+  *reinterpret_cast<__half2*>(a.out + row * D + ch) = __floats2half2_rn(O.x * inv, O.y * inv);
 }
 
 // Combines head hh of the nw warp slots (o[D], m, l, pad, pad) for channel ch.
@@ -464,12 +483,12 @@ __device__ __forceinline__ void publish(const Args& a, int64_t head, int ch, int
 // Epilogue of a unit that is not the CTA's last, run by the last warp to sign
 // in: combines the slots, publishes, releases the slots (s_done) and, in the
 // unit's last CTA, merges the partials.
-template <int D>
+template <int D, bool MQ>
 __device__ __forceinline__ void warp_epilogue(const Args& a, const float* slots, int slot_floats, int nw, int u,
                                            int nh, int total, int cslot, int useq, unsigned* s_done) {
   const int lane = threadIdx.x & 31;
-  const int64_t head0 = unit_head0(a, u);
   for (int hh = 0; hh < nh; ++hh) {
+    const int64_t row = q_row<MQ>(a, u, hh);
     // per head: the max and the slot weights once, channels lane + 32 j
     float M = -INFINITY;
     for (int w = 0; w < nw; ++w) M = fmaxf(M, slots[w * slot_floats + hh * (D + 4) + D]);
@@ -487,7 +506,7 @@ __device__ __forceinline__ void warp_epilogue(const Args& a, const float* slots,
       }
     }
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) publish<D>(a, head0 + hh, lane + 32 * j, total, cslot, M, L, O[j]);
+    for (int j = 0; j < D / 32; ++j) publish<D>(a, row, lane + 32 * j, total, cslot, M, L, O[j]);
   }
   __syncwarp();
   __threadfence_block();
@@ -500,20 +519,19 @@ __device__ __forceinline__ void warp_epilogue(const Args& a, const float* slots,
   last_cta = __shfl_sync(0xffffffffu, last_cta, 0);
   if (!last_cta) return;
   __threadfence();
-  for (int i = lane; i < nh * D / 2; i += 32) merge_out<D>(a, head0, i, total);
+  for (int i = lane; i < nh * D / 2; i += 32) merge_out<D, MQ>(a, u, i, total);
   if (lane == 0) a.counters[u] = 0u;
 }
 
 // Epilogue of the CTA's last unit, run by every thread of the CTA.
-template <int D>
+template <int D, bool MQ>
 __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, int slot_floats, int nw, int u,
                                           int nh, int total, int cslot, unsigned* s_flag) {
-  const int64_t head0 = unit_head0(a, u);
   for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
     const int hh = i / D, ch = i % D;
     float M, L, O;
     combine_slots<D>(slots, slot_floats, nw, hh, ch, M, L, O);
-    publish<D>(a, head0 + hh, ch, total, cslot, M, L, O);
+    publish<D>(a, q_row<MQ>(a, u, hh), ch, total, cslot, M, L, O);
   }
   if (total == 1) return;
   __threadfence();
@@ -522,11 +540,11 @@ __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, 
   __syncthreads();
   if (!*s_flag) return;
   __threadfence();
-  for (int i = threadIdx.x; i < nh * D / 2; i += blockDim.x) merge_out<D>(a, head0, i, total);
+  for (int i = threadIdx.x; i < nh * D / 2; i += blockDim.x) merge_out<D, MQ>(a, u, i, total);
   if (threadIdx.x == 0) a.counters[u] = 0u;
 }
 
-template <int D, int BITS, int CH>
+template <int D, int BITS, int CH, bool MQ>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mma_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   using WS = WarpSmem<D, CH>;
@@ -547,8 +565,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
   const int rep = g.rep;
-  const int64_t T = a.plan.st.T;
-  const int64_t lo_pos = g.window > 0 ? T - g.window : INT64_MIN;
   const float qscale = kLog2e * rsqrtf(static_cast<float>(D));
   const int64_t n_vis = a.plan.n_vis_groups;
   const int64_t P = gridDim.x;
@@ -600,12 +616,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   auto unit_kv = [&](int u) -> int64_t {
     const int per_b = g.hkv * a.npass;
     return static_cast<int64_t>(u / per_b) * g.hkv + (u % per_b) / a.npass;
-  };
-  auto unit_q = [&](int u, int& nh) -> const __half* {
-    const int per_b = g.hkv * a.npass;
-    const int bb = u / per_b, hk = (u % per_b) / a.npass, pass = u % a.npass;
-    nh = min(4, rep - 4 * pass);
-    return a.q + (static_cast<int64_t>(bb) * g.hq + hk * rep + 4 * pass) * D;
   };
 
   // ------------------------------------------------------------ producer
@@ -668,10 +678,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       const uint32_t dst = stages_s + p_st * a.stage_bytes;
       const uint32_t bar = bar0 + 8 * p_st;
       if (p_q) {
-        int nh_q;
-        const __half* qsrc = unit_q(u_first + p_u, nh_q);
+        const int uq = u_first + p_u;
+        const int nh_q = unit_rows<MQ>(a, uq);
         sts32_if(leader, ring_s + 4 * p_st, 2 * p_u + 1);
-        bulk_load_if(leader, dst, qsrc, static_cast<uint32_t>(nh_q) * D * 2, bar);
+        if constexpr (MQ) {
+          if (lane == 0) {   // one copy per query row (the rows of a pass need not be adjacent)
+            bulk_arm(bar, static_cast<uint32_t>(nh_q) * D * 2);
+            for (int hh = 0; hh < nh_q; ++hh)
+              bulk_copy(dst + hh * D * 2, a.q + q_row<MQ>(a, uq, hh) * D, 2 * D, bar);
+          }
+        } else {             // adjacent heads: one copy
+          bulk_load_if(leader, dst, a.q + q_row<MQ>(a, uq, 0) * D, static_cast<uint32_t>(nh_q) * D * 2, bar);
+        }
         p_q = false;
         if (++p_st == a.ns) p_st = 0;
         ++inflight;
@@ -776,9 +794,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const uint8_t* qlane = qw + hh_col * WS::kQRow + c * WS::kQS;
   const uint32_t q_s = smem_addr(qlane);
 
+  // token masks, needed with a window or with several query tokens: this
+  // lane's score column c is query row 4 pass + c of the open unit, i.e.
+  // query token jq at position hi = q_pos0 + jq, which sees the positions
+  // [lo, hi] with lo = hi + 1 - W (a window) and every sink up to hi.  With
+  // one query token (jq = 0, hi = T - 1) only a window masks anything, and
+  // only in frozen groups (the ring and the sinks lie inside any window)
+  int jq = 0;
+  auto masked = [&]() { return MQ || g.window > 0; };
+  auto col_hi = [&]() -> int64_t { return a.plan.q_pos0 + (MQ ? jq : 0); };
+  auto col_lo = [&](int64_t hi) { return g.window > 0 ? hi + 1 - g.window : static_cast<int64_t>(INT64_MIN); };
   auto open_unit = [&](int k) {
     const int u = u_first + k;
-    (void)unit_q(u, nh);
+    nh = unit_rows<MQ>(a, u);
+    if constexpr (MQ) jq = (4 * (u % a.npass) + c) / rep;
     const int64_t u_base = static_cast<int64_t>(u) * a.uw;
     u_rel = static_cast<int>(u_base - c_start);
     const int first = owner_of(u_base, W, P);
@@ -828,11 +857,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       if (last) {
         __threadfence_block();
         if (lane == 0) s_arrive = 0u;
-        warp_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, cu, &s_done);
+        warp_epilogue<D, MQ>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, cu, &s_done);
       }
     } else {
       __syncthreads();
-      cta_epilogue<D>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, &s_flag);
+      cta_epilogue<D, MQ>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, &s_flag);
     }
   };
 
@@ -954,10 +983,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
           sv[2 * v2] = sw ? s_b : s_a;
           sv[2 * v2 + 1] = sw ? s_a : s_b;
         }
-        if (g.window > 0) {   // tokens before T - W are invisible
+        if (masked()) {   // tokens outside [lo, hi] are invisible to column c
+          const int64_t hi = col_hi(), lo = col_lo(hi);
 #pragma unroll
-          for (int i = 0; i < TPL; ++i)
-            if (a_grp + s0 + TPL * r + i < lo_pos) sv[i] = -INFINITY;
+          for (int i = 0; i < TPL; ++i) {
+            const int64_t t = a_grp + s0 + TPL * r + i;
+            if (t < lo || (MQ && t > hi)) sv[i] = -INFINITY;
+          }
         }
         // (4) online softmax for head c, lazy rescale: the head maxima are
         // reduced only when some lane's score exceeds its head's running max
@@ -1102,8 +1134,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         if (j & 1) mma16816(acc1, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
         else       mma16816(acc0, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
       }
-      const float s = (r < tk.n) ? (acc0[0] + acc1[0]) * qscale : -INFINITY;
-      const float mx = warp_max_rows(s);   // finite: the chunk holds a token
+      float s = (r < tk.n) ? (acc0[0] + acc1[0]) * qscale : -INFINITY;
+      if constexpr (MQ) {   // token r's position against column c's visible range
+        const int64_t hi = col_hi(), lo = col_lo(hi);
+        const int64_t t = tk.fresh ? a.plan.fresh_pos
+                        : tk.sink  ? static_cast<int64_t>(tk.first) + r
+                                   : g.S + a.plan.st.n_groups * g.G + tk.first + r;
+        if (t > hi || (t >= g.S && t < lo)) s = -INFINITY;
+      }
+      const float mx = warp_max_rows(s);   // -inf only for a column that sees no token of the chunk
       if (mx > res_m + kRescale) {
         const float corr = (res_m == -INFINITY) ? 0.f : ex2(res_m - mx);
         res_m = mx;
@@ -1112,7 +1151,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
 #pragma unroll
         for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
       }
-      const float p = ex2(s - res_m);
+      const float p = (MQ && s == -INFINITY) ? 0.f : ex2(s - res_m);
       res_l += p;
       {
         const float h = __uint_as_float(__float_as_uint(p) & 0xFFFFE000u);

@@ -103,14 +103,18 @@ int64_t arena_bytes_of(const Geo& g) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ECUDA; }
 
-// First frozen group that can hold a visible token, and the plan of splits.
-kivi::DecodePlan plan_for(const kivi_cache& c) {
+// First frozen group that can hold a visible token, and the plan of splits,
+// for nq query tokens per sequence at positions T - nq .. T - 1 (1 for a
+// decode).
+kivi::DecodePlan plan_for(const kivi_cache& c, int32_t nq = 1) {
   kivi::DecodePlan pl{};
   pl.st = kivi::state_at(c.g, c.T);
+  pl.nq = nq;
+  pl.q_pos0 = c.T - nq;
   int64_t first = pl.st.n_groups - c.g.n_slots;
   if (first < 0) first = 0;
   if (c.g.window > 0) {
-    const int64_t lo = c.T - c.g.window;                 // first visible position
+    const int64_t lo = pl.q_pos0 + 1 - c.g.window;       // first position the oldest query sees
     if (lo > c.g.S) {
       const int64_t gl = (lo - c.g.S) / c.g.G;            // group holding position lo
       if (gl > first) first = gl;
@@ -125,7 +129,7 @@ kivi::DecodePlan plan_for(const kivi_cache& c) {
   int64_t ctas = static_cast<int64_t>(c.num_sms) * c.ctas_per_sm;
   if (ctas > kMaxDecodeCtas) ctas = kMaxDecodeCtas;
   if (c.forced_splits > 0) {   // a fixed number of CTAs per unit
-    const int64_t units = static_cast<int64_t>(c.g.B) * c.g.hkv * ((c.g.rep + 3) / 4);
+    const int64_t units = static_cast<int64_t>(c.g.B) * c.g.hkv * ((static_cast<int64_t>(nq) * c.g.rep + 3) / 4);
     ctas = units * c.forced_splits;
   }
   pl.ctas = static_cast<int32_t>(ctas > 0 ? ctas : 1);
@@ -377,12 +381,15 @@ int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
   return KIVI_OK;
 }
 
-int64_t kivi_decode_bytes(const kivi_cache* c) {
-  if (!c) return -1;
+namespace {
+// Algorithmic bytes of one attention call with nq query tokens per sequence:
+// the cache bytes the union of the queries' visible sets needs, plus q and
+// out (fp16).
+int64_t attn_bytes(const kivi_cache* c, int32_t nq) {
   const Geo& g = c->g;
-  const kivi::DecodePlan pl = plan_for(*c);
-  const int64_t T = c->T, d = g.d;
-  const int64_t lo = g.window > 0 ? T - g.window : 0;
+  const kivi::DecodePlan pl = plan_for(*c, nq);
+  const int64_t d = g.d;
+  const int64_t lo = g.window > 0 ? pl.q_pos0 + 1 - g.window : 0;
   int64_t tq = 0, touched = 0;
   for (int64_t grp = pl.g_first; grp < pl.st.n_groups; ++grp) {
     const int64_t a0 = g.S + grp * g.G, a1 = a0 + g.G;
@@ -392,7 +399,71 @@ int64_t kivi_decode_bytes(const kivi_cache* c) {
   }
   const int64_t per_unit = 2 * tq * d * g.bits / 8 + 4 * d * touched + 4 * tq + 4 * d * pl.st.n_res +
                            8 * d * pl.st.n_sink;
-  return per_unit * g.B * g.hkv + 4 * d * static_cast<int64_t>(g.B) * g.hq;
+  return per_unit * g.B * g.hkv + 4 * d * static_cast<int64_t>(g.B) * nq * g.hq;
+}
+
+// Query tokens per prefill call: bounded so that the units and the row
+// indices stay well inside 32-bit kernel arithmetic.
+constexpr int64_t kMaxQueries = 65536;
+int64_t prefill_units(const Geo& g, int64_t nq) {
+  return static_cast<int64_t>(g.B) * g.hkv * ((nq * g.rep + 3) / 4);
+}
+bool prefill_count_ok(const Geo& g, int64_t nq) {
+  return nq >= 1 && nq <= kMaxQueries && prefill_units(g, nq) <= (int64_t{1} << 28);
+}
+// Scratch of a prefill call: [merge counters, one word per unit][partials,
+// B * nq * h_q * split_stride records of d + 4 floats].
+int64_t prefill_head_bytes(const Geo& g, int64_t nq) { return round_up(prefill_units(g, nq) * 4, kAlign); }
+int64_t prefill_scratch_of(const Geo& g, int64_t nq) {
+  return prefill_head_bytes(g, nq) +
+         static_cast<int64_t>(g.B) * nq * g.hq * g.split_stride * (g.d + 4) * 4;
+}
+}  // namespace
+
+int64_t kivi_decode_bytes(const kivi_cache* c) {
+  if (!c) return -1;
+  return attn_bytes(c, 1);
+}
+
+int64_t kivi_prefill_bytes(const kivi_cache* c, int64_t n_queries) {
+  if (!c || n_queries > c->T || !prefill_count_ok(c->g, n_queries)) return -1;
+  return attn_bytes(c, static_cast<int32_t>(n_queries));
+}
+
+size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
+  if (!c || !prefill_count_ok(c->g, n_queries)) return 0;
+  return static_cast<size_t>(prefill_scratch_of(c->g, n_queries));
+}
+
+int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries, void* scratch,
+                      size_t scratch_bytes, void* cuda_stream) {
+  if (!c || !q || !out || !scratch) return KIVI_ENULL;
+  if (n_queries > c->T || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
+  const Geo& g = c->g;
+  if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(g, n_queries)) return KIVI_ENOSPC;
+  const kivi::DecodePlan pl = plan_for(*c, static_cast<int32_t>(n_queries));
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  uint8_t* bytes = static_cast<uint8_t*>(scratch);
+  const int64_t head = prefill_head_bytes(g, n_queries);
+  if (cudaMemsetAsync(bytes, 0, static_cast<size_t>(head), s) != cudaSuccess) return KIVI_ECUDA;
+  return cuda_status(kivi::launch_decode_scratch(g, c->arena, static_cast<const __half*>(q),
+                                                 static_cast<__half*>(out), pl,
+                                                 reinterpret_cast<float*>(bytes + head), g.split_stride,
+                                                 reinterpret_cast<unsigned*>(bytes),
+                                                 reinterpret_cast<unsigned*>(c->arena + g.ws_error), s));
+}
+
+int kivi_read_error(kivi_cache* c, uint32_t* flags, void* cuda_stream) {
+  if (!c || !flags) return KIVI_ENULL;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  uint32_t word = 0;
+  void* dev = c->arena + c->g.ws_error;
+  if (cudaMemcpyAsync(&word, dev, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return KIVI_ECUDA;
+  if (cudaMemsetAsync(dev, 0, 4, s) != cudaSuccess) return KIVI_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KIVI_ECUDA;
+  *flags = word;
+  return KIVI_OK;
 }
 
 const char* kivi_status_string(int status) {

@@ -67,6 +67,11 @@ struct DecodePlan {
   const __half* k_fresh;
   const __half* v_fresh;
   int64_t fresh_pos;
+  // query tokens per sequence: 1 for a decode; M for the causal attention of
+  // a chunk's M newest tokens, query j at position q_pos0 + j (q and out are
+  // then [B][M][H_q][d])
+  int32_t nq;
+  int64_t q_pos0;
 };
 
 // Decode launch shape: up to kDecodeWarps warps per CTA and kDecodeCtasPerSm
@@ -91,8 +96,9 @@ int decode_ctas_per_sm(const Geo& g);
 // Decode with the arena's own workspace for the split-K partials.
 cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,
                           const DecodePlan& plan, cudaStream_t stream);
-// Decode with caller-chosen scratch: `partials` holds B * h_q * stride
-// records of (d + 4) floats, `counters` npass words per (sequence, kv head),
+// Decode with caller-chosen scratch: `partials` holds B * nq * h_q * stride
+// records of (d + 4) floats, `counters` ceil(nq * rep / 4) words per
+// (sequence, kv head),
 // zero on entry and left zero on exit, `error` one word that the kernel ORs
 // with 1 if a copy never arrived.
 cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
