@@ -64,7 +64,9 @@ typedef enum kivi_status {
  *   h_q, h_kv  query and key/value heads; h_q % h_kv == 0; query head h reads
  *              kv head h / (h_q / h_kv) (contiguous GQA groups).
  *   head_dim   d in {64, 128}.
- *   batch      B >= 1 sequences, all of the same length.
+ *   batch      B >= 1 sequences; each keeps its own token count (they grow
+ *              alike through kivi_append and differently through
+ *              kivi_append_ragged).
  *   max_tokens capacity in tokens per sequence when window == 0.
  *   window     W: 0 = attend to every token; W > 0 (W >= R) = attend to the
  *              sinks and to the most recent W tokens, the stream is unbounded
@@ -106,7 +108,9 @@ typedef struct kivi_layout {
   int64_t block_bytes, blk_kq, blk_ks, blk_vq, blk_vs;
   int64_t unit_bytes, cache_bytes;
   int64_t workspace_offset, workspace_bytes, arena_bytes;
-  int64_t tokens;     /* T: tokens appended per sequence */
+  int64_t tokens;     /* T: tokens appended per sequence; -1 when the
+                         sequences' counts differ (kivi_cache_tokens);
+                         the three fields below are sequence 0's */
   int64_t n_sink;     /* min(T, S) */
   int64_t n_groups;   /* frozen groups written so far */
   int64_t n_res;      /* tokens live in the ring */
@@ -144,6 +148,23 @@ void kivi_cache_destroy(kivi_cache* cache);
 int kivi_append(kivi_cache* cache, const void* k_new, const void* v_new, int64_t n_tokens,
                 void* cuda_stream);
 
+/* Appends a different number of tokens to each sequence (ragged batches:
+ * chunked prefill of sequences of different lengths).
+ *   k_new, v_new  device fp16 [B][h_kv][n_max][d], contiguous, 16-byte
+ *                 aligned; row (b, h) holds sequence b's new tokens first,
+ *                 the rest of the row is ignored.
+ *   n_tokens      host array of B counts, each in [0, n_max].
+ * Each sequence's bytes are those kivi_append would give it alone.  The
+ * library launches the append once per run of consecutive sequences with
+ * equal (length, count).  Errors: ENULL, EALIGN, EINVAL (n_max < 1 or a
+ * count outside [0, n_max]), ECAPACITY, ECUDA. */
+int kivi_append_ragged(kivi_cache* cache, const void* k_new, const void* v_new, const int64_t* n_tokens,
+                       int64_t n_max, void* cuda_stream);
+
+/* Token counts of the B sequences into the host array tokens[B].
+ * Errors: ENULL. */
+int kivi_cache_tokens(const kivi_cache* cache, int64_t* tokens);
+
 /* Decode attention over everything appended so far (KV-cache quantization
  * guide, step 5; tract #2329 GQA and output shape).
  *   q    device fp16 [B][h_q][d], contiguous, 16-byte aligned.
@@ -153,7 +174,10 @@ int kivi_append(kivi_cache* cache, const void* k_new, const void* v_new, int64_t
  * in registers) and the ring (fp16); with a window, the sinks plus the most
  * recent W tokens.  With T == 0 the output is all zeros.  The work is split
  * over the sequence (split-K) and merged in the same call; the workspace is
- * scratch.  Errors: ENULL, EALIGN, ECUDA. */
+ * scratch.  Sequences of different lengths each attend over their own
+ * tokens (one launch per run of consecutive sequences of equal length; the
+ * same holds for every attention call below).  Errors: ENULL, EALIGN,
+ * ECUDA. */
 int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_stream);
 
 /* One decode step in one call: appends one token to every sequence and
@@ -213,6 +237,18 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  * (scratch too small), ECUDA. */
 int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream);
+
+/* kivi_prefill_attn for sequences of different lengths and chunk sizes:
+ * sequence b's n_queries[b] newest tokens attend, each to the tokens at or
+ * before its own position in that sequence (n_queries: host array of B
+ * counts in [0, min(m_max, its token count)]).
+ *   q, out  device fp16 [B][m_max][h_q][d]; rows j >= n_queries[b] of a
+ *           sequence are not read (q) and not written (out).
+ *   scratch at least kivi_prefill_scratch_bytes(cache, m_max) bytes.
+ * One launch per run of consecutive sequences with equal (length, count).
+ * Errors: ENULL, EINVAL, EALIGN, ENOSPC, ECUDA. */
+int kivi_prefill_attn_ragged(kivi_cache* cache, const void* q, void* out, const int64_t* n_queries,
+                             int64_t m_max, void* scratch, size_t scratch_bytes, void* cuda_stream);
 
 /* Device scratch bytes kivi_prefill_attn needs for n_queries query tokens per
  * sequence (independent of T), or 0 for a NULL handle or an n_queries outside

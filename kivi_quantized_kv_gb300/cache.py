@@ -105,6 +105,24 @@ class KiviCache:
                                           ctypes.c_void_p(v_new.data_ptr()), n,
                                           ctypes.c_void_p(_stream_ptr(stream))), "kivi_append")
 
+    def append_ragged(self, k_new: torch.Tensor, v_new: torch.Tensor, n_tokens, stream=None) -> None:
+        """k_new, v_new: [B, H_kv, n_max, d] float16; sequence b takes the
+        first n_tokens[b] tokens of its rows (kivi_append_ragged)."""
+        c = self.cfg
+        n_max = k_new.shape[2] if k_new.dim() == 4 else -1
+        shape = (c.batch, c.h_kv, n_max, c.head_dim)
+        self._check_io(k_new, shape, "k_new")
+        self._check_io(v_new, shape, "v_new")
+        counts = (ctypes.c_int64 * c.batch)(*[int(n) for n in n_tokens])
+        _abi.check(_abi.lib().kivi_append_ragged(self._h, ctypes.c_void_p(k_new.data_ptr()),
+                                                 ctypes.c_void_p(v_new.data_ptr()), counts, n_max,
+                                                 ctypes.c_void_p(_stream_ptr(stream))), "kivi_append_ragged")
+
+    def tokens_per_sequence(self) -> list:
+        out = (ctypes.c_int64 * self.cfg.batch)()
+        _abi.check(_abi.lib().kivi_cache_tokens(self._h, out), "kivi_cache_tokens")
+        return list(out)
+
     def decode(self, q: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
         """q: [B, H_q, d] float16 -> out [B, H_q, d] float16."""
         c = self.cfg
@@ -193,6 +211,33 @@ class KiviCache:
                                                 ctypes.c_void_p(out.data_ptr()), m,
                                                 ctypes.c_void_p(scratch.data_ptr()), scratch.numel(),
                                                 ctypes.c_void_p(_stream_ptr(stream))), "kivi_prefill_attn")
+        return out
+
+    def prefill_ragged(self, q: torch.Tensor, n_queries, out: torch.Tensor | None = None,
+                       scratch: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """q [B, m_max, H_q, d] float16; sequence b's n_queries[b] newest
+        tokens attend (kivi_prefill_attn_ragged).  Rows past a sequence's
+        count are left as they are in `out` (zeros when out is None)."""
+        c = self.cfg
+        m = q.shape[1] if q.dim() == 4 else -1
+        shape = (c.batch, m, c.h_q, c.head_dim)
+        self._check_io(q, shape, "q")
+        if out is None:
+            out = torch.zeros(shape, dtype=torch.float16, device=self.arena.device)
+        self._check_io(out, shape, "out")
+        need = self.prefill_scratch_bytes(m)
+        if need == 0:
+            raise _abi.KiviError(_abi.KIVI_EINVAL, "kivi_prefill_scratch_bytes")
+        if scratch is None:
+            if self._scratch is None or self._scratch.numel() < need:
+                self._scratch = torch.empty(need, dtype=torch.uint8, device=self.arena.device)
+            scratch = self._scratch
+        counts = (ctypes.c_int64 * c.batch)(*[int(n) for n in n_queries])
+        _abi.check(_abi.lib().kivi_prefill_attn_ragged(self._h, ctypes.c_void_p(q.data_ptr()),
+                                                       ctypes.c_void_p(out.data_ptr()), counts, m,
+                                                       ctypes.c_void_p(scratch.data_ptr()), scratch.numel(),
+                                                       ctypes.c_void_p(_stream_ptr(stream))),
+                   "kivi_prefill_attn_ragged")
         return out
 
     def prefill_scratch_bytes(self, n_queries: int) -> int:

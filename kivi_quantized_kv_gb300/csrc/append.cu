@@ -30,7 +30,7 @@ constexpr int kFlushThreads = 256;
 // value codes [G][d] u8.
 __global__ void __launch_bounds__(kFlushThreads)
 flush_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
-             const __half* __restrict__ v_new, int64_t T_old, int64_t n_new, int64_t g_begin) {
+             const __half* __restrict__ v_new, int64_t T_old, int64_t n_stride, int64_t g_begin) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int G = g.G, d = g.d, b = g.bits;
   const int64_t grp = g_begin + blockIdx.x;
@@ -41,7 +41,7 @@ flush_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_ne
   uint8_t* vc = kc + G * d;
 
   uint8_t* unit = arena + (static_cast<int64_t>(bb) * g.hkv + h) * g.unit_bytes;
-  const int64_t in_off = (static_cast<int64_t>(bb) * g.hkv + h) * n_new * d;
+  const int64_t in_off = (static_cast<int64_t>(bb) * g.hkv + h) * n_stride * d;   // input row of (bb, h)
   const int64_t a0 = g.S + grp * G;
 
   // stage the group's tokens: 16-byte chunks of each d-wide row
@@ -151,7 +151,7 @@ flush_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_ne
 // One thread per 8 channels of one token of one unit.
 __global__ void write_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
                              const __half* __restrict__ v_new, int64_t T_old, int64_t n_new,
-                             int64_t sink_end, int64_t ring_begin) {
+                             int64_t n_stride, int64_t sink_end, int64_t ring_begin) {
   const int d = g.d, chunks = d / 8;
   const int64_t n_sink_new = sink_end > T_old ? sink_end - T_old : 0;
   const int64_t n_ring_new = T_old + n_new - ring_begin;
@@ -163,7 +163,7 @@ __global__ void write_kernel(Geo g, uint8_t* __restrict__ arena, const __half* _
     const int64_t k = r / chunks;
     const int c8 = static_cast<int>(r % chunks) * 8;
     const int64_t a = (k < n_sink_new) ? T_old + k : ring_begin + (k - n_sink_new);
-    const int64_t src = (u * n_new + (a - T_old)) * d + c8;
+    const int64_t src = (u * n_stride + (a - T_old)) * d + c8;
     uint8_t* unit = arena + u * g.unit_bytes;
     const uint4 kv = *reinterpret_cast<const uint4*>(k_new + src);
     const uint4 vv = *reinterpret_cast<const uint4*>(v_new + src);
@@ -192,7 +192,7 @@ __global__ void write_kernel(Geo g, uint8_t* __restrict__ arena, const __half* _
 }  // namespace
 
 cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
-                         int64_t T_old, int64_t n_new, int64_t g_begin, int64_t g_end,
+                         int64_t T_old, int64_t n_stride, int64_t g_begin, int64_t g_end,
                          cudaStream_t stream) {
   if (g_end <= g_begin) return cudaSuccess;
   const size_t smem = static_cast<size_t>(g.G) * g.d * (2 * sizeof(__half) + 2);
@@ -204,7 +204,7 @@ cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, cons
   while (left > 0) {   // grid.x is limited to 2^31-1; chunk for safety
     const int64_t n = left < 65535 * 256 ? left : 65535 * 256;
     dim3 grid(static_cast<unsigned>(n), g.hkv, g.B);
-    flush_kernel<<<grid, kFlushThreads, smem, stream>>>(g, arena, k_new, v_new, T_old, n_new, start);
+    flush_kernel<<<grid, kFlushThreads, smem, stream>>>(g, arena, k_new, v_new, T_old, n_stride, start);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     start += n;
@@ -214,7 +214,7 @@ cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, cons
 }
 
 cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
-                         int64_t T_old, int64_t n_new, int64_t ring_begin, cudaStream_t stream) {
+                         int64_t T_old, int64_t n_new, int64_t n_stride, int64_t ring_begin, cudaStream_t stream) {
   const int64_t T_new = T_old + n_new;
   const int64_t sink_end = T_new < g.S ? T_new : g.S;
   const int64_t n_sink_new = sink_end > T_old ? sink_end - T_old : 0;
@@ -225,7 +225,7 @@ cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, cons
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 32) blocks = 152 * 32;
   write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(g, arena, k_new, v_new, T_old, n_new,
-                                                                       sink_end, ring_begin);
+                                                                       n_stride, sink_end, ring_begin);
   return cudaGetLastError();
 }
 

@@ -72,7 +72,7 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
   a.ns = sh.ns;
   a.stage_bytes = sh.stage_bytes;
   a.stride = stride;
-  if (plan.nq < 1) return cudaErrorInvalidValue;
+  if (plan.nq < 1 || plan.q_rows < plan.nq) return cudaErrorInvalidValue;
   a.npass = (plan.nq * g.rep + 3) / 4;   // head passes over the nq * rep query rows of a kv head
   a.units = g.B * g.hkv * a.npass;
   a.tc = plan.tc;
@@ -85,6 +85,16 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
   const int64_t cap = static_cast<int64_t>(stride - 2) * a.units;
   if (cap < 1) return cudaErrorInvalidValue;
   if (ctas > cap) ctas = cap;
+  if (plan.q_rows > 1 && a.npass > 1) {
+    // several query tokens: units are ordered pass-slowest, so in a grid of
+    // P CTAs the passes of one group block are processed at P / npass CTAs
+    // apart; when npass divides P they run at the same moment and L2 serves
+    // all but the first read (npass / gcd(P, npass) DRAM reads otherwise).
+    // The kernel is issue-bound, so the grid is trimmed to a multiple of
+    // npass only when that keeps at least 95 % of the CTAs.
+    const int64_t trimmed = ctas / a.npass * a.npass;
+    if (trimmed > 0 && 20 * trimmed >= 19 * ctas) ctas = trimmed;
+  }
   const dim3 grid(static_cast<unsigned>(ctas));
   const int threads = sh.nw * 32;
   const int smem = decode_smem(sh, stride);

@@ -73,7 +73,8 @@ cudaError_t launch_mq(const Args& a, dim3 grid, int threads, int smem, cudaStrea
 
 template <int BITS>
 cudaError_t launch_bits(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
-  return a.plan.nq > 1 ? launch_mq<BITS, true>(a, grid, threads, smem, s)
+  // the single-query instantiation assumes one query token per sequence row
+  return a.plan.q_rows > 1 ? launch_mq<BITS, true>(a, grid, threads, smem, s)
                        : launch_mq<BITS, false>(a, grid, threads, smem, s);
 }
 

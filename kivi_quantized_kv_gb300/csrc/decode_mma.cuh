@@ -374,24 +374,46 @@ struct WarpSmem {
   static constexpr int kXch = CH == 32 ? 512 : 256;
 };
 
-// Row (of q, out and the partial records: [B][nq][h_q]) of query row hh of
-// unit u (sequence, kv head, head pass).  MQ: several query tokens per
-// sequence; otherwise nq = 1 and the rows of a pass are adjacent heads.
+// Unit u as (sequence bb, kv head hk, head pass).  A decode orders units
+// pass-fastest; several query tokens (MQ) order them pass-slowest, so that
+// with a grid of a multiple of npass CTAs the passes of one group block are
+// processed at the same moment by CTAs npass apart (one DRAM read, the other
+// passes served by L2).
+template <bool MQ>
+__device__ __forceinline__ void unit_parts(const Args& a, int u, int& bb, int& hk, int& pass) {
+  if constexpr (MQ) {
+    const int u0 = a.g.B * a.g.hkv;
+    pass = u / u0;
+    bb = (u % u0) / a.g.hkv;
+    hk = u % a.g.hkv;
+  } else {
+    const int per_b = a.g.hkv * a.npass;
+    bb = u / per_b;
+    hk = (u % per_b) / a.npass;
+    pass = u % a.npass;
+  }
+}
+
+// Row (of q, out and the partial records: [B][q_rows][h_q]) of query row hh
+// of unit u.  MQ: query tokens in rows q_rows apart per sequence; otherwise
+// nq = q_rows = 1 and the rows of a pass are adjacent heads.
 template <bool MQ>
 __device__ __forceinline__ int64_t q_row(const Args& a, int u, int hh) {
-  const int per_b = a.g.hkv * a.npass;
-  const int bb = u / per_b, hk = (u % per_b) / a.npass;
+  int bb, hk, pass;
+  unit_parts<MQ>(a, u, bb, hk, pass);
   if constexpr (MQ) {
-    const int v = 4 * (u % a.npass) + hh;   // row of the kv head: query token v / rep, head v % rep
-    return (static_cast<int64_t>(bb) * a.plan.nq + v / a.g.rep) * a.g.hq + hk * a.g.rep + v % a.g.rep;
+    const int v = 4 * pass + hh;   // row of the kv head: query token v / rep, head v % rep
+    return (static_cast<int64_t>(bb) * a.plan.q_rows + v / a.g.rep) * a.g.hq + hk * a.g.rep + v % a.g.rep;
   } else {
-    return static_cast<int64_t>(bb) * a.g.hq + hk * a.g.rep + 4 * (u % a.npass) + hh;
+    return static_cast<int64_t>(bb) * a.g.hq + hk * a.g.rep + 4 * pass + hh;
   }
 }
 // Query rows of unit u (at most four).
 template <bool MQ>
 __device__ __forceinline__ int unit_rows(const Args& a, int u) {
-  return min(4, (MQ ? a.plan.nq : 1) * a.g.rep - 4 * (u % a.npass));
+  int bb, hk, pass;
+  unit_parts<MQ>(a, u, bb, hk, pass);
+  return min(4, (MQ ? a.plan.nq : 1) * a.g.rep - 4 * pass);
 }
 
 // Merge of the `total` partial records (o[D], m, l, pad, pad) of one query
@@ -608,14 +630,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   auto unit_base = [&](int u) -> const uint8_t* {
-    const int per_b = g.hkv * a.npass;
-    const int bb = u / per_b, hk = (u % per_b) / a.npass;
+    int bb, hk, pass;
+    unit_parts<MQ>(a, u, bb, hk, pass);
     return a.arena + (static_cast<int64_t>(bb) * g.hkv + hk) * g.unit_bytes;
   };
   // (sequence, kv head) index of unit u
   auto unit_kv = [&](int u) -> int64_t {
-    const int per_b = g.hkv * a.npass;
-    return static_cast<int64_t>(u / per_b) * g.hkv + (u % per_b) / a.npass;
+    int bb, hk, pass;
+    unit_parts<MQ>(a, u, bb, hk, pass);
+    return static_cast<int64_t>(bb) * g.hkv + hk;
   };
 
   // ------------------------------------------------------------ producer
@@ -807,7 +830,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   auto open_unit = [&](int k) {
     const int u = u_first + k;
     nh = unit_rows<MQ>(a, u);
-    if constexpr (MQ) jq = (4 * (u % a.npass) + c) / rep;
+    if constexpr (MQ) jq = (4 * (u / (g.B * g.hkv)) + c) / rep;   // pass-slowest order
     const int64_t u_base = static_cast<int64_t>(u) * a.uw;
     u_rel = static_cast<int>(u_base - c_start);
     const int first = owner_of(u_base, W, P);

@@ -8,13 +8,14 @@
 
 #include <mutex>
 #include <new>
+#include <vector>
 
 struct kivi_cache {
   kivi_params p;
   kivi::Geo g;
   uint8_t* arena;
   size_t arena_bytes;
-  int64_t T;
+  std::vector<int64_t> T;   // tokens appended so far, per sequence
   int32_t forced_splits;
   int32_t num_sms;
   int32_t ctas_per_sm;   // resident decode CTAs per SM for this geometry
@@ -103,14 +104,64 @@ int64_t arena_bytes_of(const Geo& g) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ECUDA; }
 
+// Sequences may hold different token counts (ragged batches).  Every call
+// works on runs of consecutive sequences that share their token count (and,
+// for the ragged calls, their count of new tokens or queries): a run is a
+// batch of its own for the kernels, addressed through a geometry with B = nb
+// and the cache region shifted to its first sequence (a unit's bytes do not
+// depend on its sequence index).  A batch of equal lengths is one run.
+struct Run {
+  int32_t b0, nb;   // sequences [b0, b0 + nb)
+  int64_t T, n;     // their token count and per-call count (0 when unused)
+};
+
+// Runs of equal (T[b], n_of(b)).
+template <class F>
+std::vector<Run> runs_of(const kivi_cache& c, F n_of) {
+  std::vector<Run> out;
+  for (int32_t b = 0; b < c.g.B; ++b) {
+    const int64_t n = n_of(b);
+    if (!out.empty() && out.back().T == c.T[b] && out.back().n == n) {
+      out.back().nb += 1;
+    } else {
+      out.push_back(Run{b, 1, c.T[b], n});
+    }
+  }
+  return out;
+}
+std::vector<Run> runs_of(const kivi_cache& c) {
+  return runs_of(c, [](int32_t) { return int64_t{0}; });
+}
+
+Geo sub_geo(const Geo& g, int32_t nb) {
+  Geo s = g;
+  s.B = nb;
+  return s;
+}
+uint8_t* run_base(const kivi_cache& c, const Run& r) {
+  return c.arena + static_cast<int64_t>(r.b0) * c.g.hkv * c.g.unit_bytes;
+}
+int64_t max_tokens_of(const kivi_cache& c) {
+  int64_t m = 0;
+  for (const int64_t t : c.T) m = t > m ? t : m;
+  return m;
+}
+int64_t min_tokens_of(const kivi_cache& c) {
+  int64_t m = c.T.empty() ? 0 : c.T[0];
+  for (const int64_t t : c.T) m = t < m ? t : m;
+  return m;
+}
+
 // First frozen group that can hold a visible token, and the plan of splits,
-// for nq query tokens per sequence at positions T - nq .. T - 1 (1 for a
-// decode).
-kivi::DecodePlan plan_for(const kivi_cache& c, int32_t nq = 1) {
+// for nb sequences of T tokens each and nq query tokens per sequence at
+// positions T - nq .. T - 1 (1 for a decode), whose q and out rows are
+// q_rows tokens apart per sequence.
+kivi::DecodePlan plan_for(const kivi_cache& c, int64_t T, int32_t nb, int32_t nq = 1, int32_t q_rows = 1) {
   kivi::DecodePlan pl{};
-  pl.st = kivi::state_at(c.g, c.T);
+  pl.st = kivi::state_at(c.g, T);
   pl.nq = nq;
-  pl.q_pos0 = c.T - nq;
+  pl.q_rows = q_rows;
+  pl.q_pos0 = T - nq;
   int64_t first = pl.st.n_groups - c.g.n_slots;
   if (first < 0) first = 0;
   if (c.g.window > 0) {
@@ -129,7 +180,7 @@ kivi::DecodePlan plan_for(const kivi_cache& c, int32_t nq = 1) {
   int64_t ctas = static_cast<int64_t>(c.num_sms) * c.ctas_per_sm;
   if (ctas > kMaxDecodeCtas) ctas = kMaxDecodeCtas;
   if (c.forced_splits > 0) {   // a fixed number of CTAs per unit
-    const int64_t units = static_cast<int64_t>(c.g.B) * c.g.hkv * ((static_cast<int64_t>(nq) * c.g.rep + 3) / 4);
+    const int64_t units = static_cast<int64_t>(nb) * c.g.hkv * ((static_cast<int64_t>(nq) * c.g.rep + 3) / 4);
     ctas = units * c.forced_splits;
   }
   pl.ctas = static_cast<int32_t>(ctas > 0 ? ctas : 1);
@@ -164,7 +215,12 @@ int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_byt
   c->g = g;
   c->arena = static_cast<uint8_t*>(d_arena);
   c->arena_bytes = arena_bytes;
-  c->T = 0;
+  try {
+    c->T.assign(static_cast<size_t>(params->batch), 0);
+  } catch (...) {
+    delete c;
+    return KIVI_ENULL;
+  }
   c->forced_splits = 0;
   c->num_sms = sms > 0 ? sms : 1;
   c->ctas_per_sm = kivi::decode_ctas_per_sm(g);
@@ -177,39 +233,101 @@ int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_byt
 
 void kivi_cache_destroy(kivi_cache* cache) { delete cache; }
 
+}  // extern "C"
+
+namespace {
+
+// Appends n tokens to every sequence of run r (its token count r.T) from
+// inputs whose (sequence, kv head) rows hold n_stride tokens.
+cudaError_t append_run(const kivi_cache& c, const Run& r, const __half* k_new, const __half* v_new, int64_t n,
+                       int64_t n_stride, cudaStream_t s) {
+  const Geo gs = sub_geo(c.g, r.nb);
+  const int64_t T_old = r.T, T_new = r.T + n;
+  const State s0 = kivi::state_at(gs, T_old), s1 = kivi::state_at(gs, T_new);
+  const int64_t in = static_cast<int64_t>(r.b0) * gs.hkv * n_stride * gs.d;
+  uint8_t* base = run_base(c, r);
+  // groups created by this append; with a window only the last n_slots survive
+  int64_t g_begin = s0.n_groups;
+  if (s1.n_groups - gs.n_slots > g_begin) g_begin = s1.n_groups - gs.n_slots;
+  cudaError_t e = kivi::launch_flush(gs, base, k_new + in, v_new + in, T_old, n_stride, g_begin, s1.n_groups, s);
+  if (e != cudaSuccess) return e;
+  // the ring keeps the last R tokens of the stream (flushed or not)
+  int64_t ring_begin = T_old;
+  if (ring_begin < gs.S) ring_begin = gs.S;
+  if (T_new - gs.R > ring_begin) ring_begin = T_new - gs.R;
+  if (ring_begin > T_new) ring_begin = T_new;
+  return kivi::launch_write(gs, base, k_new + in, v_new + in, T_old, n, n_stride, ring_begin, s);
+}
+
+// The attention of run r: q and out rows of its first sequence at
+// b0 * q_rows * h_q; scratch pointers absolute.
+cudaError_t attn_run(const kivi_cache& c, const Run& r, const kivi::DecodePlan& pl, const __half* q, __half* out,
+                     float* partials, int32_t stride, unsigned* counters, unsigned* error, cudaStream_t s) {
+  const Geo gs = sub_geo(c.g, r.nb);
+  const int64_t row0 = static_cast<int64_t>(r.b0) * pl.q_rows * gs.hq * gs.d;
+  return kivi::launch_decode_scratch(gs, run_base(c, r), q + row0, out + row0, pl, partials, stride, counters,
+                                     error, s);
+}
+float* ws_partials(const kivi_cache& c) { return reinterpret_cast<float*>(c.arena + c.g.ws_partials); }
+unsigned* ws_counters(const kivi_cache& c) { return reinterpret_cast<unsigned*>(c.arena + c.g.ws_counters); }
+unsigned* ws_error(const kivi_cache& c) { return reinterpret_cast<unsigned*>(c.arena + c.g.ws_error); }
+
+}  // namespace
+
+extern "C" {
+
 int kivi_append(kivi_cache* c, const void* k_new, const void* v_new, int64_t n, void* cuda_stream) {
   if (!c || !k_new || !v_new) return KIVI_ENULL;
   if (n < 1) return KIVI_EINVAL;
   if (!aligned(k_new, 16) || !aligned(v_new, 16)) return KIVI_EALIGN;
-  const Geo& g = c->g;
-  const int64_t T_old = c->T, T_new = c->T + n;
-  if (g.window == 0 && T_new > c->p.max_tokens) return KIVI_ECAPACITY;
+  if (c->g.window == 0 && max_tokens_of(*c) + n > c->p.max_tokens) return KIVI_ECAPACITY;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  const State s0 = kivi::state_at(g, T_old), s1 = kivi::state_at(g, T_new);
-  // groups created by this append; with a window only the last n_slots survive
-  int64_t g_begin = s0.n_groups;
-  if (s1.n_groups - g.n_slots > g_begin) g_begin = s1.n_groups - g.n_slots;
-  const auto* kh = static_cast<const __half*>(k_new);
-  const auto* vh = static_cast<const __half*>(v_new);
-  cudaError_t e = kivi::launch_flush(g, c->arena, kh, vh, T_old, n, g_begin, s1.n_groups, s);
-  if (e != cudaSuccess) return cuda_status(e);
-  // the ring keeps the last R tokens of the stream (flushed or not)
-  int64_t ring_begin = T_old;
-  if (ring_begin < g.S) ring_begin = g.S;
-  if (T_new - g.R > ring_begin) ring_begin = T_new - g.R;
-  if (ring_begin > T_new) ring_begin = T_new;
-  e = kivi::launch_write(g, c->arena, kh, vh, T_old, n, ring_begin, s);
-  if (e != cudaSuccess) return cuda_status(e);
-  c->T = T_new;
+  for (const Run& r : runs_of(*c)) {
+    const cudaError_t e = append_run(*c, r, static_cast<const __half*>(k_new), static_cast<const __half*>(v_new),
+                                     n, n, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  for (int64_t& t : c->T) t += n;
+  return KIVI_OK;
+}
+
+int kivi_append_ragged(kivi_cache* c, const void* k_new, const void* v_new, const int64_t* n_tokens,
+                       int64_t n_max, void* cuda_stream) {
+  if (!c || !k_new || !v_new || !n_tokens) return KIVI_ENULL;
+  if (n_max < 1) return KIVI_EINVAL;
+  for (int32_t b = 0; b < c->g.B; ++b) {
+    if (n_tokens[b] < 0 || n_tokens[b] > n_max) return KIVI_EINVAL;
+    if (c->g.window == 0 && c->T[b] + n_tokens[b] > c->p.max_tokens) return KIVI_ECAPACITY;
+  }
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return KIVI_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  for (const Run& r : runs_of(*c, [&](int32_t b) { return n_tokens[b]; })) {
+    if (r.n == 0) continue;
+    const cudaError_t e = append_run(*c, r, static_cast<const __half*>(k_new), static_cast<const __half*>(v_new),
+                                     r.n, n_max, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  for (int32_t b = 0; b < c->g.B; ++b) c->T[b] += n_tokens[b];
+  return KIVI_OK;
+}
+
+int kivi_cache_tokens(const kivi_cache* c, int64_t* tokens) {
+  if (!c || !tokens) return KIVI_ENULL;
+  for (int32_t b = 0; b < c->g.B; ++b) tokens[b] = c->T[b];
   return KIVI_OK;
 }
 
 int kivi_decode_attn(kivi_cache* c, const void* q, void* out, void* cuda_stream) {
   if (!c || !q || !out) return KIVI_ENULL;
   if (!aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
-  const kivi::DecodePlan pl = plan_for(*c);
-  return cuda_status(kivi::launch_decode(c->g, c->arena, static_cast<const __half*>(q),
-                                         static_cast<__half*>(out), pl, static_cast<cudaStream_t>(cuda_stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  for (const Run& r : runs_of(*c)) {
+    const kivi::DecodePlan pl = plan_for(*c, r.T, r.nb);
+    const cudaError_t e = attn_run(*c, r, pl, static_cast<const __half*>(q), static_cast<__half*>(out),
+                                   ws_partials(*c), c->g.split_stride, ws_counters(*c), ws_error(*c), s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KIVI_OK;
 }
 
 int kivi_append_decode_attn(kivi_cache* c, const void* k_new, const void* v_new, const void* q, void* out,
@@ -217,36 +335,38 @@ int kivi_append_decode_attn(kivi_cache* c, const void* k_new, const void* v_new,
   if (!c || !k_new || !v_new || !q || !out) return KIVI_ENULL;
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
   const Geo& g = c->g;
-  const int64_t T_old = c->T, T_new = c->T + 1;
-  if (g.window == 0 && T_new > c->p.max_tokens) return KIVI_ECAPACITY;
+  if (g.window == 0 && max_tokens_of(*c) + 1 > c->p.max_tokens) return KIVI_ECAPACITY;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   const auto* kh = static_cast<const __half*>(k_new);
   const auto* vh = static_cast<const __half*>(v_new);
-  const State s0 = kivi::state_at(g, T_old), s1 = kivi::state_at(g, T_new);
-  if (s1.n_groups > s0.n_groups) {
-    // the token reaches a full ring: its oldest G tokens freeze first, as in
-    // kivi_append (a launch of its own, before the decode reads the group)
-    int64_t g_begin = s0.n_groups;
-    if (s1.n_groups - g.n_slots > g_begin) g_begin = s1.n_groups - g.n_slots;
-    const cudaError_t e = kivi::launch_flush(g, c->arena, kh, vh, T_old, 1, g_begin, s1.n_groups, s);
+  for (const Run& r : runs_of(*c)) {
+    const Geo gs = sub_geo(g, r.nb);
+    const int64_t T_old = r.T, T_new = r.T + 1;
+    const int64_t in = static_cast<int64_t>(r.b0) * g.hkv * g.d;   // the run's first input row
+    const State s0 = kivi::state_at(g, T_old), s1 = kivi::state_at(g, T_new);
+    if (s1.n_groups > s0.n_groups) {
+      // the token reaches a full ring: its oldest G tokens freeze first, as in
+      // kivi_append (a launch of its own, before the decode reads the group)
+      int64_t g_begin = s0.n_groups;
+      if (s1.n_groups - g.n_slots > g_begin) g_begin = s1.n_groups - g.n_slots;
+      const cudaError_t e = kivi::launch_flush(gs, run_base(*c, r), kh + in, vh + in, T_old, 1, g_begin,
+                                               s1.n_groups, s);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    kivi::DecodePlan pl = plan_for(*c, T_new, r.nb);
+    // the fresh token is attended straight from the inputs (and written into
+    // its sink or ring slot by the same launch), so the cache's own tail is
+    // one token shorter
+    if (T_old < g.S) pl.st.n_sink -= 1; else pl.st.n_res -= 1;
+    pl.tc = static_cast<int32_t>((pl.st.n_sink + 3) / 4 + (pl.st.n_res + 7) / 8 + 1);
+    pl.k_fresh = kh + in;
+    pl.v_fresh = vh + in;
+    pl.fresh_pos = T_old;
+    const cudaError_t e = attn_run(*c, r, pl, static_cast<const __half*>(q), static_cast<__half*>(out),
+                                   ws_partials(*c), g.split_stride, ws_counters(*c), ws_error(*c), s);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  c->T = T_new;
-  kivi::DecodePlan pl = plan_for(*c);
-  // the fresh token is attended straight from the inputs (and written into
-  // its sink or ring slot by the same launch), so the cache's own tail is one
-  // token shorter
-  if (T_old < g.S) pl.st.n_sink -= 1; else pl.st.n_res -= 1;
-  pl.tc = static_cast<int32_t>((pl.st.n_sink + 3) / 4 + (pl.st.n_res + 7) / 8 + 1);
-  pl.k_fresh = kh;
-  pl.v_fresh = vh;
-  pl.fresh_pos = T_old;
-  const cudaError_t e = kivi::launch_decode(g, c->arena, static_cast<const __half*>(q), static_cast<__half*>(out),
-                                            pl, s);
-  if (e != cudaSuccess) {
-    c->T = T_old;
-    return cuda_status(e);
-  }
+  for (int64_t& t : c->T) t += 1;
   return KIVI_OK;
 }
 
@@ -254,7 +374,7 @@ int kivi_append_decode_attn_host(kivi_cache* c, const void* k_host, const void* 
                                  void* out_host, void* cuda_stream) {
   if (!c || !k_host || !v_host || !q_host || !out_host) return KIVI_ENULL;
   const Geo& g = c->g;
-  if (g.window == 0 && c->T + 1 > c->p.max_tokens) return KIVI_ECAPACITY;
+  if (g.window == 0 && max_tokens_of(*c) + 1 > c->p.max_tokens) return KIVI_ECAPACITY;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   const size_t q_bytes = static_cast<size_t>(g.B) * g.hq * g.d * 2;
   const size_t kv_bytes = static_cast<size_t>(g.B) * g.hkv * g.d * 2;
@@ -341,7 +461,6 @@ int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda
   const int64_t record = static_cast<int64_t>(c->g.B) * c->g.hq * (c->g.d + 4) * 4;   // one CTA per unit
   const int64_t fit = (static_cast<int64_t>(kNoAllocScratchBytes) - head_bytes) / record;
   if (fit < 3) return KIVI_ESCRATCH;   // at least two CTAs per unit
-  const kivi::DecodePlan pl = plan_for(*c);   // the launch caps the CTAs so a unit's partials fit
   void* base = nullptr;
   const int st = noalloc_scratch(&base);
   if (st != KIVI_OK) return st;
@@ -351,9 +470,15 @@ int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda
   unsigned* counters = reinterpret_cast<unsigned*>(bytes + kAlign);
   float* partials = reinterpret_cast<float*>(bytes + head_bytes);
   if (cudaMemsetAsync(bytes, 0, static_cast<size_t>(head_bytes), s) != cudaSuccess) return KIVI_ECUDA;
-  return cuda_status(kivi::launch_decode_scratch(c->g, c->arena, static_cast<const __half*>(q),
-                                                 static_cast<__half*>(out), pl, partials,
-                                                 static_cast<int32_t>(fit), counters, error, s));
+  // one launch per run of equal lengths; each leaves the counters zero, and
+  // the launch caps the CTAs so a unit's partials fit
+  for (const Run& r : runs_of(*c)) {
+    const kivi::DecodePlan pl = plan_for(*c, r.T, r.nb);
+    const cudaError_t e = attn_run(*c, r, pl, static_cast<const __half*>(q), static_cast<__half*>(out), partials,
+                                   static_cast<int32_t>(fit), counters, error, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KIVI_OK;
 }
 
 int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {
@@ -366,7 +491,9 @@ int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {
 int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
   if (!c || !out) return KIVI_ENULL;
   const Geo& g = c->g;
-  const State st = kivi::state_at(g, c->T);
+  const State st = kivi::state_at(g, c->T[0]);
+  bool uniform = true;
+  for (const int64_t t : c->T) uniform = uniform && t == c->T[0];
   kivi_layout L{};
   L.n_slots = g.n_slots;
   L.sink_k = g.sink_k; L.sink_v = g.sink_v; L.res_k = g.res_k; L.res_v = g.res_v; L.groups = g.groups;
@@ -375,19 +502,20 @@ int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
   L.workspace_offset = g.ws_partials;
   L.arena_bytes = arena_bytes_of(g);
   L.workspace_bytes = L.arena_bytes - g.ws_partials;
-  L.tokens = c->T; L.n_sink = st.n_sink; L.n_groups = st.n_groups; L.n_res = st.n_res;
+  // the state of sequence 0; tokens is -1 when the sequences' lengths differ
+  L.tokens = uniform ? c->T[0] : -1; L.n_sink = st.n_sink; L.n_groups = st.n_groups; L.n_res = st.n_res;
   L.max_splits = g.max_splits;
   *out = L;
   return KIVI_OK;
 }
 
 namespace {
-// Algorithmic bytes of one attention call with nq query tokens per sequence:
-// the cache bytes the union of the queries' visible sets needs, plus q and
-// out (fp16).
-int64_t attn_bytes(const kivi_cache* c, int32_t nq) {
-  const Geo& g = c->g;
-  const kivi::DecodePlan pl = plan_for(*c, nq);
+// Algorithmic bytes of one attention call over run r with nq query tokens
+// per sequence: the cache bytes the union of the queries' visible sets
+// needs, plus q and out (fp16).
+int64_t attn_bytes(const kivi_cache& c, const Run& r, int64_t nq) {
+  const Geo& g = c.g;
+  const kivi::DecodePlan pl = plan_for(c, r.T, r.nb, static_cast<int32_t>(nq));
   const int64_t d = g.d;
   const int64_t lo = g.window > 0 ? pl.q_pos0 + 1 - g.window : 0;
   int64_t tq = 0, touched = 0;
@@ -399,7 +527,7 @@ int64_t attn_bytes(const kivi_cache* c, int32_t nq) {
   }
   const int64_t per_unit = 2 * tq * d * g.bits / 8 + 4 * d * touched + 4 * tq + 4 * d * pl.st.n_res +
                            8 * d * pl.st.n_sink;
-  return per_unit * g.B * g.hkv + 4 * d * static_cast<int64_t>(g.B) * nq * g.hq;
+  return per_unit * r.nb * g.hkv + 4 * d * static_cast<int64_t>(r.nb) * nq * g.hq;
 }
 
 // Query tokens per prefill call: bounded so that the units and the row
@@ -418,16 +546,40 @@ int64_t prefill_scratch_of(const Geo& g, int64_t nq) {
   return prefill_head_bytes(g, nq) +
          static_cast<int64_t>(g.B) * nq * g.hq * g.split_stride * (g.d + 4) * 4;
 }
+
+// The prefill attention over the runs of equal (T, n) with n = that run's
+// query count (runs with none are skipped); q and out rows m_max per sequence.
+int prefill_runs(kivi_cache* c, const std::vector<Run>& runs, const void* q, void* out, int64_t m_max,
+                 void* scratch, cudaStream_t s) {
+  const Geo& g = c->g;
+  uint8_t* bytes = static_cast<uint8_t*>(scratch);
+  const int64_t head = prefill_head_bytes(g, m_max);
+  // the counters start at zero; every launch leaves them zero
+  if (cudaMemsetAsync(bytes, 0, static_cast<size_t>(head), s) != cudaSuccess) return KIVI_ECUDA;
+  for (const Run& r : runs) {
+    if (r.n == 0) continue;
+    const kivi::DecodePlan pl = plan_for(*c, r.T, r.nb, static_cast<int32_t>(r.n), static_cast<int32_t>(m_max));
+    const cudaError_t e = attn_run(*c, r, pl, static_cast<const __half*>(q), static_cast<__half*>(out),
+                                   reinterpret_cast<float*>(bytes + head), g.split_stride,
+                                   reinterpret_cast<unsigned*>(bytes), ws_error(*c), s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return KIVI_OK;
+}
 }  // namespace
 
 int64_t kivi_decode_bytes(const kivi_cache* c) {
   if (!c) return -1;
-  return attn_bytes(c, 1);
+  int64_t sum = 0;
+  for (const Run& r : runs_of(*c)) sum += attn_bytes(*c, r, 1);
+  return sum;
 }
 
 int64_t kivi_prefill_bytes(const kivi_cache* c, int64_t n_queries) {
-  if (!c || n_queries > c->T || !prefill_count_ok(c->g, n_queries)) return -1;
-  return attn_bytes(c, static_cast<int32_t>(n_queries));
+  if (!c || n_queries > min_tokens_of(*c) || !prefill_count_ok(c->g, n_queries)) return -1;
+  int64_t sum = 0;
+  for (const Run& r : runs_of(*c)) sum += attn_bytes(*c, r, n_queries);
+  return sum;
 }
 
 size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
@@ -438,20 +590,23 @@ size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
 int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch) return KIVI_ENULL;
-  if (n_queries > c->T || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
+  if (n_queries > min_tokens_of(*c) || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
-  const Geo& g = c->g;
-  if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(g, n_queries)) return KIVI_ENOSPC;
-  const kivi::DecodePlan pl = plan_for(*c, static_cast<int32_t>(n_queries));
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  uint8_t* bytes = static_cast<uint8_t*>(scratch);
-  const int64_t head = prefill_head_bytes(g, n_queries);
-  if (cudaMemsetAsync(bytes, 0, static_cast<size_t>(head), s) != cudaSuccess) return KIVI_ECUDA;
-  return cuda_status(kivi::launch_decode_scratch(g, c->arena, static_cast<const __half*>(q),
-                                                 static_cast<__half*>(out), pl,
-                                                 reinterpret_cast<float*>(bytes + head), g.split_stride,
-                                                 reinterpret_cast<unsigned*>(bytes),
-                                                 reinterpret_cast<unsigned*>(c->arena + g.ws_error), s));
+  if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(c->g, n_queries)) return KIVI_ENOSPC;
+  return prefill_runs(c, runs_of(*c, [&](int32_t) { return n_queries; }), q, out, n_queries, scratch,
+                      static_cast<cudaStream_t>(cuda_stream));
+}
+
+int kivi_prefill_attn_ragged(kivi_cache* c, const void* q, void* out, const int64_t* n_queries, int64_t m_max,
+                             void* scratch, size_t scratch_bytes, void* cuda_stream) {
+  if (!c || !q || !out || !scratch || !n_queries) return KIVI_ENULL;
+  if (!prefill_count_ok(c->g, m_max)) return KIVI_EINVAL;
+  for (int32_t b = 0; b < c->g.B; ++b)
+    if (n_queries[b] < 0 || n_queries[b] > m_max || n_queries[b] > c->T[b]) return KIVI_EINVAL;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
+  if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(c->g, m_max)) return KIVI_ENOSPC;
+  return prefill_runs(c, runs_of(*c, [&](int32_t b) { return n_queries[b]; }), q, out, m_max, scratch,
+                      static_cast<cudaStream_t>(cuda_stream));
 }
 
 int kivi_read_error(kivi_cache* c, uint32_t* flags, void* cuda_stream) {

@@ -44,14 +44,16 @@ inline State state_at(const Geo& g, int64_t T) {
 
 // ---- append (append.cu) ----
 // Quantizes and packs groups [g_begin, g_end) of every unit.  Tokens with
-// position < T_old come from the ring, the others from the new input.
+// position < T_old come from the ring, the others from the new input, whose
+// (sequence, kv head) rows hold n_stride tokens each.
 cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
-                         int64_t T_old, int64_t n_new, int64_t g_begin, int64_t g_end,
+                         int64_t T_old, int64_t n_stride, int64_t g_begin, int64_t g_end,
                          cudaStream_t stream);
 // Writes new sink tokens [T_old, min(T_new, S)) and ring tokens
-// [ring_begin, T_new) of every unit from the new input.
+// [ring_begin, T_new) of every unit from the new input (T_new = T_old +
+// n_new; rows of n_stride tokens).
 cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
-                         int64_t T_old, int64_t n_new, int64_t ring_begin, cudaStream_t stream);
+                         int64_t T_old, int64_t n_new, int64_t n_stride, int64_t ring_begin, cudaStream_t stream);
 
 // ---- decode (decode.cu) ----
 struct DecodePlan {
@@ -71,6 +73,7 @@ struct DecodePlan {
   // a chunk's M newest tokens, query j at position q_pos0 + j (q and out are
   // then [B][M][H_q][d])
   int32_t nq;
+  int32_t q_rows;         // query tokens per sequence in the q and out buffers (>= nq)
   int64_t q_pos0;
 };
 
