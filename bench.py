@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--prefill", type=int, default=0, metavar="M",
                     help="chunked prefill instead of decode: a step appends M tokens per sequence and runs "
                          "the causal attention of those M queries (kivi_append + kivi_prefill_attn)")
+    ap.add_argument("--ragged", action="store_true",
+                    help="with --prefill: sequence b takes a chunk of M - M*b/(2B) tokens (all lengths differ; "
+                         "kivi_append_ragged + kivi_prefill_attn_ragged)")
     return ap.parse_args()
 
 
@@ -420,6 +423,8 @@ def run_prefill(args, device):
 
     w = workload(args.workload)
     m = args.prefill
+    counts = [m - (m * b) // (2 * w.batch) for b in range(w.batch)] if args.ragged else [m] * w.batch
+    w1 = w.with_(batch=1)
     total_steps = args.steps + args.warmup
     l2 = 129 * 1024 * 1024
     cfg0 = KiviConfig.from_workload(w)
@@ -451,14 +456,22 @@ def run_prefill(args, device):
     sp = vp(stream.cuda_stream)
     args_of = [(caches[s % n_rep][0]._h, vp(chunks[s][0].data_ptr()), vp(chunks[s][1].data_ptr()),
                 vp(qs[s % len(qs)].data_ptr())) for s in range(total_steps)]
+    counts_arr = (ctypes.c_int64 * w.batch)(*counts)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
 
     def step(s, e=None):
         h, kp, vq, qp = args_of[s]
-        st = L.kivi_append(h, kp, vq, m, sp)
+        if args.ragged:
+            st = L.kivi_append_ragged(h, kp, vq, counts_arr, m, sp)
+        else:
+            st = L.kivi_append(h, kp, vq, m, sp)
         if e is not None:
             e[0].record(stream)
-        st = st or L.kivi_prefill_attn(h, qp, vp(out.data_ptr()), m, vp(scratch.data_ptr()), need, sp)
+        if args.ragged:
+            st = st or L.kivi_prefill_attn_ragged(h, qp, vp(out.data_ptr()), counts_arr, m, vp(scratch.data_ptr()),
+                                                  need, sp)
+        else:
+            st = st or L.kivi_prefill_attn(h, qp, vp(out.data_ptr()), m, vp(scratch.data_ptr()), need, sp)
         if e is not None:
             e[1].record(stream)
         if st != 0:
@@ -467,7 +480,7 @@ def run_prefill(args, device):
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize(device)
-    T_now = [c.tokens for c, _ in caches]
+    T_now = [c.tokens_per_sequence() for c, _ in caches]
     meta = [(c.layout()["n_slots"], c.layout()["block_bytes"]) for c, _ in caches]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -487,15 +500,23 @@ def run_prefill(args, device):
     attn_bytes = attn_flops = launches = 0
     for i in range(args.steps):
         r = (args.warmup + i) % n_rep
-        T0 = T_now[r]
-        T_now[r] += m
-        flush = state_at(w, T_now[r])[1] > state_at(w, T0)[1]
-        attn_bytes += prefill_bytes_at(w, T_now[r], m, meta[r][0])
-        attn_flops += prefill_flops_at(w, T_now[r], m, meta[r][0])
-        launches += (3 if flush else 2)
+        T0 = list(T_now[r])
+        runs = []   # the library's runs: consecutive sequences of equal (length, count)
+        for b in range(w.batch):
+            if runs and runs[-1][1] == (T0[b], counts[b]):
+                runs[-1][0].append(b)
+            else:
+                runs.append(([b], (T0[b], counts[b])))
+        for seqs, (t0, n) in runs:
+            launches += 2 + (1 if state_at(w, t0 + n)[1] > state_at(w, t0)[1] else 0)   # write, prefill, flush
+        for b in range(w.batch):
+            T_now[r][b] += counts[b]
+            attn_bytes += prefill_bytes_at(w1, T_now[r][b], counts[b], meta[r][0])
+            attn_flops += prefill_flops_at(w1, T_now[r][b], counts[b], meta[r][0])
     for r, (c, _) in enumerate(caches):   # the byte count above is the library's own
-        assert c.tokens == T_now[r]
-        assert c.prefill_bytes(m) == prefill_bytes_at(w, T_now[r], m, meta[r][0]), "prefill byte count mismatch"
+        assert c.tokens_per_sequence() == T_now[r]
+        if not args.ragged:
+            assert c.prefill_bytes(m) == prefill_bytes_at(w, T_now[r][0], m, meta[r][0]), "prefill byte count mismatch"
         assert c.read_error() == 0
     peaks, src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", 6800.0))
@@ -514,18 +535,21 @@ def run_prefill(args, device):
     roof.update({"traffic": None, "peak_source": src, "kernel": "decode_mma_kernel (several query tokens, causal masks)",
                  "bytes_per_launch": int(attn_bytes / args.steps), "flops_per_launch": int(attn_flops / args.steps),
                  "hbm_frac": round(gbs / hbm, 4), "tensor_frac": round(tflops / tensor, 5)})
-    tok = w.batch * m * args.steps
+    tok = sum(counts) * args.steps
     return {
-        "metric": f"chunked prefill query tokens/s (append {m} tokens + their causal attention over the packed cache)",
+        "metric": (f"chunked prefill query tokens/s (append {'up to ' if args.ragged else ''}{m} tokens per sequence "
+                   f"+ their causal attention over the packed cache)"),
         "value": round(tok / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32", "data": "synthetic",
-        "config": workload_config(w, {"chunk": m, "parallelism": "replicas1",
+        "config": workload_config(w, {"chunk": m, "chunks_per_sequence": counts if args.ragged else m,
+                                      "parallelism": "replicas1",
                                       "l2": f"{n_rep} rotating cache replicas x {per_cache / 1e6:.0f} MB (> 4x 129 MB L2)",
                                       "tokens_at_first_chunk": w.tokens}),
         "roofline": roof, "gpu_launches": launches, "clocks": clk,
         "attn_us": round(attn_ms * 1e3 / args.steps, 2), "attn_gbs": round(gbs, 1), "attn_tflops": round(tflops, 2),
-        "step_call": "kivi_append + kivi_prefill_attn",
+        "step_call": ("kivi_append_ragged + kivi_prefill_attn_ragged" if args.ragged
+                      else "kivi_append + kivi_prefill_attn"),
     }
 
 
