@@ -282,6 +282,21 @@ def append_bytes_at(w, T, block_bytes):
 
 
 # --------------------------------------------------------------- our arm
+def across_ranks(ms, nbytes, world, device):
+    """(max of the ranks' timed spans, sum of their bytes) over the process
+    group: every rank runs its own replica of the workload (weak scaling; the
+    path needs no exchange), so the job moved the sum of the bytes in the
+    slowest rank's time."""
+    if world == 1:
+        return ms, nbytes
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(b, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
 def run_ours(args, rank, world, device):
     import torch
     from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
@@ -385,13 +400,9 @@ def run_ours(args, rank, world, device):
     for r, (c, _) in enumerate(caches):   # the byte count above is the library's own
         assert c.tokens == T_now[r]
         assert c.decode_bytes() == decode_bytes_at(w, T_now[r], meta[r][0]), "decode byte count mismatch"
-    ms_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max, all_bytes = across_ranks(ms, dec_bytes + app_bytes, world, device)
     step_bytes = (dec_bytes + app_bytes) / args.steps
-    value = step_bytes * args.steps * world / (ms_max / 1e3) / 1e9
+    value = all_bytes / (ms_max / 1e3) / 1e9
     # the decode kernel's roofline: the timed steps back to back are that
     # kernel's launches (plus a flush launch on the steps that freeze a
     # group, counted against it), so its achieved rate is the decode bytes
