@@ -132,6 +132,26 @@ size_t kivi_cache_bytes(const kivi_params* params);
 int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_bytes,
                       void* cuda_stream, kivi_cache** out);
 
+/* Re-attaches a handle to an arena that already holds a cache written by this
+ * library with the same parameters (checkpoint / resume: the arena's cache
+ * region, the kivi_params and the B token counts are the whole state, so a
+ * byte copy of the arena taken after its stream was synchronised, with
+ * kivi_cache_tokens, restores it; no file format).  tokens: host array of B
+ * counts.  Unlike kivi_cache_create it keeps the cache region; it clears the
+ * workspace's merge counters and error word on `stream`.  Errors: ENULL,
+ * EINVAL (parameters, or a count < 0, or above max_tokens when window == 0),
+ * EALIGN, ENOSPC, ECUDA. */
+int kivi_cache_restore(const kivi_params* params, void* d_arena, size_t arena_bytes, const int64_t* tokens,
+                       void* cuda_stream, kivi_cache** out);
+
+/* Host-side fault injection for tests of the error paths (the method's pages
+ * have no counterpart): n >= 1 arms the n-th kernel launch the library makes
+ * from now on, in any handle of the process, to fail with ECUDA without
+ * being made; the call that hits it returns ECUDA with its token counts
+ * unchanged (launches it made before stay made).  0 disarms.  Nothing is
+ * injected on the device.  Errors: EINVAL (n < 0). */
+int kivi_debug_inject_launch_failure(int64_t n);
+
 /* Frees the host handle.  The arena stays the caller's. */
 void kivi_cache_destroy(kivi_cache* cache);
 

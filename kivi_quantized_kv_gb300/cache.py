@@ -53,7 +53,11 @@ def _stream_ptr(stream) -> int:
 class KiviCache:
     """A quantized KV cache of one attention layer on one GPU."""
 
-    def __init__(self, cfg: KiviConfig, device="cuda", stream=None, arena: torch.Tensor | None = None):
+    def __init__(self, cfg: KiviConfig, device="cuda", stream=None, arena: torch.Tensor | None = None,
+                 restore_tokens=None):
+        """A new cache (the arena is zeroed), or with restore_tokens (one
+        count per sequence) a handle over an `arena` that already holds a
+        cache of this config (kivi_cache_restore)."""
         self.cfg = cfg
         self.device = torch.device(device)
         if self.device.type != "cuda":
@@ -69,9 +73,15 @@ class KiviCache:
         self._scratch = None   # prefill scratch, grown on demand
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
-            _abi.check(L.kivi_cache_create(ctypes.byref(p), ctypes.c_void_p(arena.data_ptr()),
-                                           arena.numel(), ctypes.c_void_p(_stream_ptr(stream)),
-                                           ctypes.byref(h)), "kivi_cache_create")
+            if restore_tokens is None:
+                _abi.check(L.kivi_cache_create(ctypes.byref(p), ctypes.c_void_p(arena.data_ptr()),
+                                               arena.numel(), ctypes.c_void_p(_stream_ptr(stream)),
+                                               ctypes.byref(h)), "kivi_cache_create")
+            else:
+                toks = (ctypes.c_int64 * cfg.batch)(*[int(t) for t in restore_tokens])
+                _abi.check(L.kivi_cache_restore(ctypes.byref(p), ctypes.c_void_p(arena.data_ptr()),
+                                                arena.numel(), toks, ctypes.c_void_p(_stream_ptr(stream)),
+                                                ctypes.byref(h)), "kivi_cache_restore")
         self._h = h
 
     def __del__(self):

@@ -204,6 +204,7 @@ cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, cons
   while (left > 0) {   // grid.x is limited to 2^31-1; chunk for safety
     const int64_t n = left < 65535 * 256 ? left : 65535 * 256;
     dim3 grid(static_cast<unsigned>(n), g.hkv, g.B);
+    if (injected_launch_failure()) return cudaErrorLaunchFailure;
     flush_kernel<<<grid, kFlushThreads, smem, stream>>>(g, arena, k_new, v_new, T_old, n_stride, start);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -224,6 +225,7 @@ cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, cons
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 32) blocks = 152 * 32;
+  if (injected_launch_failure()) return cudaErrorLaunchFailure;
   write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(g, arena, k_new, v_new, T_old, n_new,
                                                                        n_stride, sink_end, ring_begin);
   return cudaGetLastError();

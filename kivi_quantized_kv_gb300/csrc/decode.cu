@@ -96,6 +96,7 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
     if (trimmed > 0 && 20 * trimmed >= 19 * ctas) ctas = trimmed;
   }
   const dim3 grid(static_cast<unsigned>(ctas));
+  if (injected_launch_failure()) return cudaErrorLaunchFailure;
   const int threads = sh.nw * 32;
   const int smem = decode_smem(sh, stride);
   if (g.bits == 2) return mma::launch_b2(a, grid, threads, smem, stream);

@@ -6,9 +6,23 @@
 // freed or synchronised here.
 #include "kivi_internal.cuh"
 
+#include <atomic>
 #include <mutex>
 #include <new>
 #include <vector>
+
+namespace kivi {
+namespace {
+std::atomic<int64_t> g_fail_countdown{0};   // 0 = disarmed; n = the n-th launch from now fails
+}  // namespace
+bool injected_launch_failure() {
+  int64_t n = g_fail_countdown.load(std::memory_order_relaxed);
+  while (n > 0) {
+    if (g_fail_countdown.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return n == 1;
+  }
+  return false;
+}
+}  // namespace kivi
 
 struct kivi_cache {
   kivi_params p;
@@ -198,14 +212,23 @@ size_t kivi_cache_bytes(const kivi_params* params) {
   return static_cast<size_t>(arena_bytes_of(geometry(*params)));
 }
 
-int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_bytes, void* cuda_stream,
-                      kivi_cache** out) {
+}  // extern "C"
+
+namespace {
+// A handle over an arena; the cache region is zeroed (a new cache) or kept
+// (restore), the workspace's counters and error word are always cleared.
+int open_handle(const kivi_params* params, void* d_arena, size_t arena_bytes, const int64_t* tokens, bool keep,
+                void* cuda_stream, kivi_cache** out) {
   if (!out || !d_arena) return KIVI_ENULL;
   const int v = validate(params);
   if (v != KIVI_OK) return v;
   if (!aligned(d_arena, kAlign)) return KIVI_EALIGN;
   const Geo g = geometry(*params);
   if (static_cast<int64_t>(arena_bytes) < arena_bytes_of(g)) return KIVI_ENOSPC;
+  if (keep) {
+    for (int32_t b = 0; b < params->batch; ++b)
+      if (tokens[b] < 0 || (params->window == 0 && tokens[b] > params->max_tokens)) return KIVI_EINVAL;
+  }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KIVI_ECUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KIVI_ECUDA;
@@ -221,13 +244,36 @@ int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_byt
     delete c;
     return KIVI_ENULL;
   }
+  if (keep) c->T.assign(tokens, tokens + params->batch);
   c->forced_splits = 0;
   c->num_sms = sms > 0 ? sms : 1;
   c->ctas_per_sm = kivi::decode_ctas_per_sm(g);
-  const cudaError_t e = cudaMemsetAsync(d_arena, 0, static_cast<size_t>(arena_bytes_of(g)),
-                                        static_cast<cudaStream_t>(cuda_stream));
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const int64_t from = keep ? g.ws_counters : 0;   // counters and error word are adjacent
+  const int64_t to = keep ? g.ws_error + 4 : arena_bytes_of(g);
+  const cudaError_t e = cudaMemsetAsync(c->arena + from, 0, static_cast<size_t>(to - from), s);
   if (e != cudaSuccess) { delete c; return KIVI_ECUDA; }
   *out = c;
+  return KIVI_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int kivi_cache_create(const kivi_params* params, void* d_arena, size_t arena_bytes, void* cuda_stream,
+                      kivi_cache** out) {
+  return open_handle(params, d_arena, arena_bytes, nullptr, false, cuda_stream, out);
+}
+
+int kivi_cache_restore(const kivi_params* params, void* d_arena, size_t arena_bytes, const int64_t* tokens,
+                       void* cuda_stream, kivi_cache** out) {
+  if (!tokens) return KIVI_ENULL;
+  return open_handle(params, d_arena, arena_bytes, tokens, true, cuda_stream, out);
+}
+
+int kivi_debug_inject_launch_failure(int64_t n) {
+  if (n < 0) return KIVI_EINVAL;
+  kivi::g_fail_countdown.store(n, std::memory_order_relaxed);
   return KIVI_OK;
 }
 

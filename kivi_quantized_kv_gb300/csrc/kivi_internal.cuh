@@ -42,6 +42,11 @@ inline State state_at(const Geo& g, int64_t T) {
   return s;
 }
 
+// Host-side fault injection (kivi_debug_inject_launch_failure): true when
+// the launch about to be made is the one armed to fail; it is then not made
+// and the caller reports cudaErrorLaunchFailure.
+bool injected_launch_failure();
+
 // ---- append (append.cu) ----
 // Quantizes and packs groups [g_begin, g_end) of every unit.  Tokens with
 // position < T_old come from the ring, the others from the new input, whose

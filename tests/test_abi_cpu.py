@@ -98,3 +98,29 @@ def test_python_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(_abi, "LIB_PATH", "/nonexistent/libkivi.so")
     with pytest.raises(ImportError):
         _abi.lib()
+
+
+def test_fault_injection_arming_is_host_only(abi):
+    L = abi.lib()
+    assert L.kivi_debug_inject_launch_failure(-1) == abi.KIVI_EINVAL
+    assert L.kivi_debug_inject_launch_failure(3) == abi.KIVI_OK
+    assert L.kivi_debug_inject_launch_failure(0) == abi.KIVI_OK
+
+
+def test_restore_rejects_bad_arguments_before_any_device_call(abi):
+    import ctypes
+    p = params().c()
+    h = ctypes.c_void_p()
+    toks = (ctypes.c_int64 * 1)(5)
+    L = abi.lib()
+    assert L.kivi_cache_restore(ctypes.byref(p), None, 1 << 20, toks, None, ctypes.byref(h)) == abi.KIVI_ENULL
+    assert L.kivi_cache_restore(ctypes.byref(p), ctypes.c_void_p(256), 1 << 30, None, None,
+                                ctypes.byref(h)) == abi.KIVI_ENULL
+    bad = (ctypes.c_int64 * 1)(-1)
+    assert L.kivi_cache_restore(ctypes.byref(p), ctypes.c_void_p(256), 1 << 30, bad, None,
+                                ctypes.byref(h)) == abi.KIVI_EINVAL
+    over = (ctypes.c_int64 * 1)(257)   # max_tokens 256
+    assert L.kivi_cache_restore(ctypes.byref(p), ctypes.c_void_p(256), 1 << 30, over, None,
+                                ctypes.byref(h)) == abi.KIVI_EINVAL
+    assert L.kivi_cache_restore(ctypes.byref(p), ctypes.c_void_p(258), 1 << 30, toks, None,
+                                ctypes.byref(h)) == abi.KIVI_EALIGN
