@@ -49,8 +49,8 @@ def parse():
                     help="chunked prefill instead of decode: a step appends M tokens per sequence and runs "
                          "the causal attention of those M queries (kivi_append + kivi_prefill_attn)")
     ap.add_argument("--ragged", action="store_true",
-                    help="with --prefill: sequence b takes a chunk of M - M*b/(2B) tokens (all lengths differ; "
-                         "kivi_append_ragged + kivi_prefill_attn_ragged)")
+                    help="ragged batch: decode with sequence b holding T - T*b/(2B) tokens; with --prefill, "
+                         "sequence b takes a chunk of M - M*b/(2B) tokens (all lengths differ)")
     return ap.parse_args()
 
 
@@ -317,16 +317,20 @@ def run_ours(args, rank, world, device):
     stream = torch.cuda.current_stream(device)
 
     caches = []
+    # ragged: sequence b starts at T - 1 - T*b/(2B) tokens (every length differs)
+    targets = [w.tokens - 1 - ((w.tokens * b) // (2 * w.batch) if args.ragged else 0) for b in range(w.batch)]
     for r in range(n_rep):
         c = KiviCache(cfg, device=device)
         kv = KVStream(w.with_(seed=w.seed + 100 * r), device=device)
-        t = 0
-        target = w.tokens - 1
-        while t < target:
-            n = min(4096, target - t)
-            k, v = kv.next(n)
-            c.append(k, v)
-            t += n
+        t = [0] * w.batch
+        while t != targets:
+            n = [min(4096, targets[b] - t[b]) for b in range(w.batch)]
+            k, v = kv.next(max(n))
+            if args.ragged:
+                c.append_ragged(k, v, n)
+            else:
+                c.append(k, v)
+            t = [t[b] + n[b] for b in range(w.batch)]
         caches.append((c, kv))
     # per-step inputs, resident before the timed region
     new_kv = [caches[s % n_rep][1].next(1) for s in range(total_steps)]
@@ -362,7 +366,7 @@ def run_ours(args, rank, world, device):
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize(device)
-    T_before = [caches[s % n_rep][0].tokens for s in range(n_rep)]   # tokens of each replica before the timed steps
+    T_before = [c.tokens_per_sequence() for c, _ in caches]   # tokens of each replica's sequences before the timed steps
     meta = [(c.layout()["n_slots"], c.layout()["block_bytes"]) for c, _ in caches]
 
     t0 = torch.cuda.Event(enable_timing=True)
@@ -387,19 +391,31 @@ def run_ours(args, rank, world, device):
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
     # bytes of the timed steps, from each replica's token count at each step
-    T_now = list(T_before)
+    T_now = [list(t) for t in T_before]
+    w1 = w.with_(batch=1)
     dec_bytes = app_bytes = launches = 0
     for i in range(args.steps):
         r = (args.warmup + i) % n_rep
         n_slots, block_bytes = meta[r]
-        app_bytes += append_bytes_at(w, T_now[r], block_bytes)
-        flush = state_at(w, T_now[r] + 1)[1] > state_at(w, T_now[r])[1]
-        T_now[r] += 1
-        dec_bytes += decode_bytes_at(w, T_now[r], n_slots)
-        launches += (2 if flush else 1) if fused else (2 if flush else 1) + 1
+        # the library's runs (consecutive sequences of equal length): one run is
+        # one decode launch (plus a flush launch when its token freezes a
+        # group); several runs share one ragged launch per 64 runs (plus one
+        # flush launch when any of them freezes a group)
+        runs = [b for b in range(w.batch) if b == 0 or T_now[r][b] != T_now[r][b - 1]]
+        freezes = [state_at(w, T_now[r][b0] + 1)[1] > state_at(w, T_now[r][b0])[1] for b0 in runs]
+        if not fused:   # kivi_append, one launch pair (flush, write) per run, then the decode
+            launches += sum(2 if f else 1 for f in freezes) + -(-len(runs) // 64)
+        else:
+            for i in range(0, len(runs), 64):
+                launches += 1 + (1 if any(freezes[i:i + 64]) else 0)
+        for b in range(w.batch):
+            app_bytes += append_bytes_at(w1, T_now[r][b], block_bytes)
+            T_now[r][b] += 1
+            dec_bytes += decode_bytes_at(w1, T_now[r][b], n_slots)
     for r, (c, _) in enumerate(caches):   # the byte count above is the library's own
-        assert c.tokens == T_now[r]
-        assert c.decode_bytes() == decode_bytes_at(w, T_now[r], meta[r][0]), "decode byte count mismatch"
+        assert c.tokens_per_sequence() == T_now[r]
+        assert c.decode_bytes() == sum(decode_bytes_at(w1, t, meta[r][0]) for t in T_now[r]), \
+            "decode byte count mismatch"
     ms_max, all_bytes = across_ranks(ms, dec_bytes + app_bytes, world, device)
     step_bytes = (dec_bytes + app_bytes) / args.steps
     value = all_bytes / (ms_max / 1e3) / 1e9
@@ -414,7 +430,7 @@ def run_ours(args, rank, world, device):
         "dec_bytes": dec_bytes / args.steps, "fused": fused, "step_bytes": step_bytes, "launches": launches,
         "clocks": clk, "app_tok_s": w.batch * args.steps / (ms / 1e3),
     }
-    if not args.no_e2e:
+    if not args.no_e2e and not args.ragged:
         res["e2e"] = run_e2e(args, caches, new_kv, w, device, stream)
     return res
 
@@ -728,7 +744,8 @@ def main():
         "config": workload_config(w, {"parallelism": f"replicas{world}",
                                       "l2": f"{r['n_rep']} rotating cache replicas x {r['per_cache'] / 1e6:.0f} MB "
                                             f"(> 4x 129 MB L2)",
-                                      "appended_per_sequence": -(-(args.steps + args.warmup) // r["n_rep"])}),
+                                      "appended_per_sequence": -(-(args.steps + args.warmup) // r["n_rep"]),
+                                      "ragged": bool(args.ragged)}),
         "roofline": {"bound": "hbm", "achieved": round(r["dec_gbs"], 1), "peak": peak, "unit": "GB/s",
                      "frac": round(r["dec_gbs"] / peak, 4), "traffic": traffic,
                      "kernel": "decode_mma_kernel (stream-K split-K, merge and fresh-token append in the same launch)", "peak_source": src,

@@ -195,9 +195,10 @@ int kivi_cache_tokens(const kivi_cache* cache, int64_t* tokens);
  * recent W tokens.  With T == 0 the output is all zeros.  The work is split
  * over the sequence (split-K) and merged in the same call; the workspace is
  * scratch.  Sequences of different lengths each attend over their own
- * tokens (one launch per run of consecutive sequences of equal length; the
- * same holds for every attention call below).  Errors: ENULL, EALIGN,
- * ECUDA. */
+ * tokens: the batch is cut into runs of consecutive sequences of equal
+ * length and one launch covers up to 64 runs (the runs' plans travel in the
+ * launch's parameters), so a ragged batch of up to 64 distinct lengths is
+ * still one launch.  Errors: ENULL, EALIGN, ECUDA. */
 int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_stream);
 
 /* One decode step in one call: appends one token to every sequence and
@@ -209,6 +210,9 @@ int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_str
  * straight from k_new / v_new and written into its sink or ring slot by the
  * decode launch itself, so a step is one launch; a step whose token freezes
  * a group (the ring is full) first runs that group's quantization launch.
+ * Sequences of different lengths: as kivi_decode_attn, one decode launch per
+ * 64 runs, preceded by one quantization launch over the sequences whose
+ * token freezes a group.
  *   k_new, v_new  device fp16 [B][h_kv][1][d], contiguous, 16-byte aligned.
  *   q, out        device fp16 [B][h_q][d], contiguous, 16-byte aligned.
  * Errors: ENULL, EALIGN, ECAPACITY, ECUDA (the token count is then left

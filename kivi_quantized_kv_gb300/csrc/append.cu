@@ -26,15 +26,14 @@ namespace {
 
 constexpr int kFlushThreads = 256;
 
-// Shared memory: keys [G][d] fp16, values [G][d] fp16, key codes [G][d] u8,
-// value codes [G][d] u8.
-__global__ void __launch_bounds__(kFlushThreads)
-flush_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
-             const __half* __restrict__ v_new, int64_t T_old, int64_t n_stride, int64_t g_begin) {
+// Group grp of unit (bb, h): the body of both flush kernels.  Shared memory:
+// keys [G][d] fp16, values [G][d] fp16, key codes [G][d] u8, value codes
+// [G][d] u8.
+__device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ arena,
+                                            const __half* __restrict__ k_new, const __half* __restrict__ v_new,
+                                            int64_t T_old, int64_t n_stride, int64_t grp, int h, int bb) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int G = g.G, d = g.d, b = g.bits;
-  const int64_t grp = g_begin + blockIdx.x;
-  const int h = blockIdx.y, bb = blockIdx.z;
   __half* kx = reinterpret_cast<__half*>(smem);
   __half* vx = kx + G * d;
   uint8_t* kc = reinterpret_cast<uint8_t*>(vx + G * d);
@@ -148,6 +147,27 @@ flush_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_ne
   }
 }
 
+__global__ void __launch_bounds__(kFlushThreads)
+flush_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
+             const __half* __restrict__ v_new, int64_t T_old, int64_t n_stride, int64_t g_begin) {
+  flush_group(g, arena, k_new, v_new, T_old, n_stride, g_begin + blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// The fused step over a ragged batch: block (h, b) freezes sequence b's next
+// group if its new token (position T_old of its run) reaches a full ring.
+__global__ void __launch_bounds__(kFlushThreads)
+flush_ragged_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
+                    const __half* __restrict__ v_new, const __grid_constant__ RunTable rt) {
+  const int bb = blockIdx.z;
+  int k = 0;
+  while (k < rt.n && bb >= rt.r[k].b0 + rt.r[k].nb) ++k;
+  if (k == rt.n || bb < rt.r[k].b0) return;   // not in this launch's runs (uniform per block)
+  const int64_t T_old = rt.r[k].fresh_pos;
+  const State s0 = state_at(g, T_old), s1 = state_at(g, T_old + 1);
+  if (s1.n_groups == s0.n_groups) return;   // uniform per block
+  flush_group(g, arena, k_new, v_new, T_old, 1, s0.n_groups, blockIdx.y, bb);
+}
+
 // One thread per 8 channels of one token of one unit.
 __global__ void write_kernel(Geo g, uint8_t* __restrict__ arena, const __half* __restrict__ k_new,
                              const __half* __restrict__ v_new, int64_t T_old, int64_t n_new,
@@ -212,6 +232,17 @@ cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, cons
     left -= n;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_flush_ragged(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
+                                const RunTable& runs, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(g.G) * g.d * (2 * sizeof(__half) + 2);
+  cudaError_t e = cudaFuncSetAttribute(flush_ragged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (injected_launch_failure()) return cudaErrorLaunchFailure;
+  flush_ragged_kernel<<<dim3(1, g.hkv, g.B), kFlushThreads, smem, stream>>>(g, arena, k_new, v_new, runs);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,

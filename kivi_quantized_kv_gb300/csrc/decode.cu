@@ -104,6 +104,48 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
   return mma::launch_b8(a, grid, threads, smem, stream);
 }
 
+cudaError_t launch_decode_ragged(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
+                                 const DecodePlan& plan, const RunTable& runs, float* partials, int32_t stride,
+                                 unsigned* counters, unsigned* error, cudaStream_t stream) {
+  if (plan.ctas < 1 || stride < 3 || runs.n < 1 || runs.n > kMaxRuns || runs.W < 1) return cudaErrorInvalidValue;
+  const DecodeShape sh = decode_shape(g);
+  mma::Args a{};
+  a.g = g;
+  a.arena = arena;
+  a.q = q;
+  a.out = out;
+  a.partials = partials;
+  a.counters = counters;
+  a.error = error;
+  a.plan = plan;
+  a.plan.nq = 1;
+  a.plan.q_rows = 1;
+  a.ns = sh.ns;
+  a.stage_bytes = sh.stage_bytes;
+  a.stride = stride;
+  a.npass = sh.npass;
+  a.units = g.B * g.hkv * sh.npass;
+  a.tc = 1;   // per run in the table
+  a.uw = 1;
+  int64_t ctas = plan.ctas;
+  if (ctas > runs.W) ctas = runs.W;
+  // a unit of w positions meets at most ceil(w P / W) + 1 of the P CTAs, which
+  // must not exceed the stride of partial records: units of different widths
+  // bound P by the widest one
+  int64_t uw_max = 1;
+  for (int k = 0; k < runs.n; ++k) uw_max = runs.r[k].uw > uw_max ? runs.r[k].uw : uw_max;
+  const int64_t cap = static_cast<int64_t>(stride - 2) * runs.W / uw_max;
+  if (cap < 1) return cudaErrorInvalidValue;
+  if (ctas > cap) ctas = cap;
+  const dim3 grid(static_cast<unsigned>(ctas));
+  if (injected_launch_failure()) return cudaErrorLaunchFailure;
+  const int threads = sh.nw * 32;
+  const int smem = decode_smem(sh, stride);
+  if (g.bits == 2) return mma::launch_rg_b2(a, runs, grid, threads, smem, stream);
+  if (g.bits == 4) return mma::launch_rg_b4(a, runs, grid, threads, smem, stream);
+  return mma::launch_rg_b8(a, runs, grid, threads, smem, stream);
+}
+
 cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,
                           const DecodePlan& plan, cudaStream_t stream) {
   return launch_decode_scratch(g, arena, q, out, plan, reinterpret_cast<float*>(arena + g.ws_partials),

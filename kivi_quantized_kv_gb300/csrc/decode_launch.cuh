@@ -9,7 +9,7 @@
 namespace kivi {
 namespace mma {
 
-template <int D, int BITS, int CH, bool MQ>
+template <int D, int BITS, int CH, bool MQ, bool RG>
 cudaError_t prepare() {
   // opt in to the largest dynamic shared memory once per instantiation
   static std::atomic<int> done{0};
@@ -20,18 +20,18 @@ cudaError_t prepare() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, decode_mma_kernel<D, BITS, CH, MQ>);
+  e = cudaFuncGetAttributes(&fa, decode_mma_kernel<D, BITS, CH, MQ, RG>);
   if (e != cudaSuccess) return e;
   // the opt-in limit covers static + dynamic shared memory
-  e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, CH, MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, CH, MQ, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            optin - static_cast<int>(fa.sharedSizeBytes));
   if (e == cudaSuccess) done.store(1, std::memory_order_release);
   return e;
 }
 
-template <int D, int BITS, int CH, bool MQ>
-cudaError_t launch_one(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
-  cudaError_t e = prepare<D, BITS, CH, MQ>();
+template <int D, int BITS, int CH, bool MQ, bool RG>
+cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
+  cudaError_t e = prepare<D, BITS, CH, MQ, RG>();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the CTAs may start (and set up their
   // shared memory) while the previous kernel in the stream drains; the kernel
@@ -46,51 +46,65 @@ cudaError_t launch_one(const Args& a, dim3 grid, int threads, int smem, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BITS, CH, MQ>, a);
+  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BITS, CH, MQ, RG>, a, rt);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D, int BITS, int CH, bool MQ>
+template <int D, int BITS, int CH, bool MQ, bool RG>
 int occupancy_one(int threads, int smem) {
-  if (prepare<D, BITS, CH, MQ>() != cudaSuccess) return 1;
+  if (prepare<D, BITS, CH, MQ, RG>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, BITS, CH, MQ>, threads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, BITS, CH, MQ, RG>, threads, smem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
 
-// one instantiation per (head dim, chunk of the group, several query tokens)
-template <int BITS, bool MQ>
-cudaError_t launch_mq(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+// one instantiation per (head dim, chunk of the group, several query tokens,
+// ragged)
+template <int BITS, bool MQ, bool RG>
+cudaError_t launch_mq(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
   const bool ch32 = (a.g.G % 32) == 0;
   if (a.g.d == 64)
-    return ch32 ? launch_one<64, BITS, 32, MQ>(a, grid, threads, smem, s)
-                : launch_one<64, BITS, 16, MQ>(a, grid, threads, smem, s);
-  return ch32 ? launch_one<128, BITS, 32, MQ>(a, grid, threads, smem, s)
-              : launch_one<128, BITS, 16, MQ>(a, grid, threads, smem, s);
+    return ch32 ? launch_one<64, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s)
+                : launch_one<64, BITS, 16, MQ, RG>(a, rt, grid, threads, smem, s);
+  return ch32 ? launch_one<128, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s)
+              : launch_one<128, BITS, 16, MQ, RG>(a, rt, grid, threads, smem, s);
 }
 
 template <int BITS>
 cudaError_t launch_bits(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+  const NoRuns none{0};
   // the single-query instantiation assumes one query token per sequence row
-  return a.plan.q_rows > 1 ? launch_mq<BITS, true>(a, grid, threads, smem, s)
-                       : launch_mq<BITS, false>(a, grid, threads, smem, s);
+  return a.plan.q_rows > 1 ? launch_mq<BITS, true, false>(a, none, grid, threads, smem, s)
+                           : launch_mq<BITS, false, false>(a, none, grid, threads, smem, s);
 }
 
-// the multi-query instantiations have the same launch bounds and shared memory
+// ragged launches: one query token per sequence (decode and the fused step)
+template <int BITS>
+cudaError_t launch_bits_ragged(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
+                               cudaStream_t s) {
+  return launch_mq<BITS, false, true>(a, rt, grid, threads, smem, s);
+}
+
+// the other instantiations have the same launch bounds and shared memory
 template <int BITS>
 int occupancy_bits(const Geo& g, int threads, int smem) {
   const bool ch32 = (g.G % 32) == 0;
   if (g.d == 64)
-    return ch32 ? occupancy_one<64, BITS, 32, false>(threads, smem) : occupancy_one<64, BITS, 16, false>(threads, smem);
-  return ch32 ? occupancy_one<128, BITS, 32, false>(threads, smem) : occupancy_one<128, BITS, 16, false>(threads, smem);
+    return ch32 ? occupancy_one<64, BITS, 32, false, false>(threads, smem)
+                : occupancy_one<64, BITS, 16, false, false>(threads, smem);
+  return ch32 ? occupancy_one<128, BITS, 32, false, false>(threads, smem)
+              : occupancy_one<128, BITS, 16, false, false>(threads, smem);
 }
 
 // defined in decode_b2.cu, decode_b4.cu, decode_b8.cu
 cudaError_t launch_b2(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
 cudaError_t launch_b4(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
 cudaError_t launch_b8(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_rg_b2(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_rg_b4(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_rg_b8(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem, cudaStream_t s);
 int occupancy_b2(const Geo& g, int threads, int smem);
 int occupancy_b4(const Geo& g, int threads, int smem);
 int occupancy_b8(const Geo& g, int threads, int smem);

@@ -60,6 +60,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 namespace kivi {
 namespace mma {
 
@@ -566,8 +568,14 @@ __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, 
   if (threadIdx.x == 0) a.counters[u] = 0u;
 }
 
-template <int D, int BITS, int CH, bool MQ>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mma_kernel(const Args a) {
+template <bool RG>
+using RunTableT = typename std::conditional<RG, RunTable, NoRuns>::type;
+
+// RG: a ragged launch; per-unit plan values come from the run table `rt`
+// (the unit's run) instead of the launch's plan.
+template <int D, int BITS, int CH, bool MQ, bool RG>
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
+    decode_mma_kernel(const Args a, const __grid_constant__ RunTableT<RG> rt) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   using WS = WarpSmem<D, CH>;
   constexpr int RK = D * BITS / 8;          // key row bytes
@@ -590,12 +598,41 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   const float qscale = kLog2e * rsqrtf(static_cast<float>(D));
   const int64_t n_vis = a.plan.n_vis_groups;
   const int64_t P = gridDim.x;
-  const int64_t W = static_cast<int64_t>(a.units) * a.uw;
+  int64_t W;
+  if constexpr (RG) W = rt.W; else W = static_cast<int64_t>(a.units) * a.uw;
   const int64_t c_start = (static_cast<int64_t>(blockIdx.x) * W) / P;
   const int64_t c_end = (static_cast<int64_t>(blockIdx.x + 1) * W) / P;
   if (c_start >= c_end) return;   // uniform; only when W < P, which the host avoids
-  const int u_first = static_cast<int>(c_start / a.uw);
-  const int u_last = static_cast<int>((c_end - 1) / a.uw);
+  // ragged launches: the run holding work position x, the run of unit u
+  // (searched upwards from a run k at or before it), a unit's first position
+  auto run_at = [&](int64_t x) -> int {
+    int k = 0;
+    if constexpr (RG) while (k + 1 < rt.n && rt.r[k + 1].pos0 <= x) ++k;
+    return k;
+  };
+  auto run_of = [&](int u, int k) -> int {
+    if constexpr (RG) while (k + 1 < rt.n && u >= rt.r[k + 1].ubase) ++k;
+    return k;
+  };
+  auto unit_start = [&](int u, int k) -> int64_t {
+    if constexpr (RG) return rt.r[k].pos0 + static_cast<int64_t>(u - rt.r[k].ubase) * rt.r[k].uw;
+    else return static_cast<int64_t>(u) * a.uw;
+  };
+  auto unit_width = [&](int k) -> int {
+    if constexpr (RG) return rt.r[k].uw;
+    else return static_cast<int>(a.uw);
+  };
+  int k_first = 0, k_last = 0;
+  int u_first, u_last;
+  if constexpr (RG) {
+    k_first = run_at(c_start);
+    k_last = run_at(c_end - 1);
+    u_first = rt.r[k_first].ubase + static_cast<int>((c_start - rt.r[k_first].pos0) / rt.r[k_first].uw);
+    u_last = rt.r[k_last].ubase + static_cast<int>((c_end - 1 - rt.r[k_last].pos0) / rt.r[k_last].uw);
+  } else {
+    u_first = static_cast<int>(c_start / a.uw);
+    u_last = static_cast<int>((c_end - 1) / a.uw);
+  }
 
   // shared memory: stages | q | slots | exchange | barriers | item rings (per warp, warp-major within each)
   uint8_t* stages = smem_raw;
@@ -657,6 +694,31 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   // visible groups never outnumber its slots
   const uint32_t slot0 = ring_slots ? static_cast<uint32_t>(a.plan.g_first % g.n_slots)
                                     : static_cast<uint32_t>(a.plan.g_first);
+  // per-unit plan values: the launch's (uniform) or the unit's run's (ragged)
+  auto f_nvis = [&](int k) -> int {
+    if constexpr (RG) return rt.r[k].n_vis; else return static_cast<int>(n_vis);
+  };
+  auto f_slot0 = [&](int k) -> uint32_t {
+    if constexpr (RG) return rt.r[k].slot0; else return slot0;
+  };
+  auto f_sink = [&](int k) -> int {
+    if constexpr (RG) return rt.r[k].n_sink; else return t_sink;
+  };
+  auto f_res = [&](int k) -> int {
+    if constexpr (RG) return rt.r[k].n_res; else return t_res;
+  };
+  auto f_rs0 = [&](int k) -> int {
+    if constexpr (RG) return rt.r[k].rs0; else return rs0;
+  };
+  auto f_gfirst = [&](int k) -> int64_t {
+    if constexpr (RG) return rt.r[k].g_first; else return a.plan.g_first;
+  };
+  auto f_qpos0 = [&](int k) -> int64_t {
+    if constexpr (RG) return rt.r[k].q_pos0; else return a.plan.q_pos0;
+  };
+  auto f_fresh_pos = [&](int k) -> int64_t {
+    if constexpr (RG) return rt.r[k].fresh_pos; else return a.plan.fresh_pos;
+  };
   int c_st = 0;                 // consumer: stage, phase parity
   uint32_t c_ph = 0;
   int inflight = 0;             // items issued and not yet consumed (warp-uniform)
@@ -668,14 +730,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   int p_rel = 0;
   int p_next = 0, p_left = 0;   // the warp's current claim: next position, positions left in it
   // end of unit p_u's positions, relative to c_start (negative or zero before the first claim)
-  int p_end = static_cast<int>(static_cast<int64_t>(u_first) * a.uw - c_start);
+  int p_end = static_cast<int>(unit_start(u_first, k_first) - c_start);
+  int p_k = k_first;            // run of unit p_u (ragged launches)
   const uint8_t* p_unit = nullptr;
   bool aborted = false;
   const uint32_t stages_s = smem_addr(my_stages);
   const uint32_t ring_s = smem_addr(ring_w);
   const uint32_t next_s = smem_addr(&s_next);
   const bool leader = lane == 0;
-  const int n_vis_i = static_cast<int>(n_vis);   // visible groups of one unit
   // the whole warp runs the bookkeeping on warp-uniform values; lane 0 alone
   // claims, notes the item and issues the copies (predicated, no branch)
   auto produce = [&]() {
@@ -693,7 +755,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         --p_left;
         p_have = true;
         if (p_rel >= p_end) {   // the position lies in a later unit (positions only grow)
-          do { ++p_u; p_end += a.uw; } while (p_rel >= p_end);
+          do {
+            ++p_u;
+            p_k = run_of(u_first + p_u, p_k);
+            p_end += unit_width(p_k);
+          } while (p_rel >= p_end);
           p_unit = unit_base(u_first + p_u);
           p_q = true;
         }
@@ -718,15 +784,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         ++inflight;
         continue;
       }
-      const int pos = p_rel - (p_end - static_cast<int>(a.uw));   // position inside unit p_u
+      const int pos = p_rel - (p_end - unit_width(p_k));   // position inside unit p_u
       bool issued = true;
-      if (pos < n_vis_i) {   // a frozen group block
-        uint32_t slot = slot0 + static_cast<uint32_t>(pos);
+      const int p_nvis = f_nvis(p_k);
+      if (pos < p_nvis) {   // a frozen group block
+        uint32_t slot = f_slot0(p_k) + static_cast<uint32_t>(pos);
         if (ring_slots && slot >= n_slots) slot -= n_slots;
         sts32_if(leader, ring_s + 4 * p_st, 2 * p_rel);
         bulk_load_if(leader, dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
       } else {                // a tail chunk: key rows then value rows
-        const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res, fresh);
+        const TailChunk tk = tail_chunk(pos - p_nvis, f_sink(p_k), f_res(p_k), fresh);
         if (tk.n == 0) {
           issued = false;     // nothing to copy or to attend to
         } else if (lane == 0) {
@@ -742,7 +809,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
             bulk_copy(dst, p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
             bulk_copy(dst + 16 * D, p_unit + g.sink_v + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
           } else {
-            int s0 = rs0 + tk.first;
+            int s0 = f_rs0(p_k) + tk.first;
             if (s0 >= g.R) s0 -= g.R;
             const int n1 = min(tk.n, g.R - s0), n2 = tk.n - n1;   // the ring may wrap
             bulk_arm(bar, static_cast<uint32_t>(tk.n) * D * 4);
@@ -824,17 +891,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
   // one query token (jq = 0, hi = T - 1) only a window masks anything, and
   // only in frozen groups (the ring and the sinks lie inside any window)
   int jq = 0;
+  int c_k = k_first;            // run of the open unit (ragged launches)
   auto masked = [&]() { return MQ || g.window > 0; };
-  auto col_hi = [&]() -> int64_t { return a.plan.q_pos0 + (MQ ? jq : 0); };
+  auto col_hi = [&]() -> int64_t { return f_qpos0(c_k) + (MQ ? jq : 0); };
   auto col_lo = [&](int64_t hi) { return g.window > 0 ? hi + 1 - g.window : static_cast<int64_t>(INT64_MIN); };
   auto open_unit = [&](int k) {
     const int u = u_first + k;
     nh = unit_rows<MQ>(a, u);
     if constexpr (MQ) jq = (4 * (u / (g.B * g.hkv)) + c) / rep;   // pass-slowest order
-    const int64_t u_base = static_cast<int64_t>(u) * a.uw;
+    c_k = run_of(u, c_k);
+    const int64_t u_base = unit_start(u, c_k);
     u_rel = static_cast<int>(u_base - c_start);
     const int first = owner_of(u_base, W, P);
-    total = owner_of(u_base + a.uw - 1, W, P) - first + 1;
+    total = owner_of(u_base + unit_width(c_k) - 1, W, P) - first + 1;
     cslot = static_cast<int>(blockIdx.x) - first;
     res_m = -INFINITY; res_l = 0.f; res_mn = 0.f;
     o_real = false;
@@ -921,9 +990,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       continue;
     }
     const int pos = (item >> 1) - u_rel;   // position inside the open unit
-    if (pos < n_vis_i) {
+    const int c_nvis = f_nvis(c_k);
+    if (pos < c_nvis) {
       // ------------------------------------------------------ a frozen group
-      const int64_t grp = a.plan.g_first + pos;
+      const int64_t grp = f_gfirst(c_k) + pos;
       const uint32_t blk = stages_s + c_st * a.stage_bytes;   // shared address of the block
 
       // (1) the query (natural pair order) and the folded B fragments:
@@ -1113,7 +1183,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       release();
     } else {
       // ------------------------------------------------------ a tail chunk
-      const TailChunk tk = tail_chunk(pos - n_vis_i, t_sink, t_res, fresh);
+      const TailChunk tk = tail_chunk(pos - c_nvis, f_sink(c_k), f_res(c_k), fresh);
       const uint8_t* kst = my_stages + c_st * a.stage_bytes;
       const uint8_t* vst = kst + 16 * D;
       if (!o_real) {   // from here on oacc holds real-scale values
@@ -1160,7 +1230,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
       float s = (r < tk.n) ? (acc0[0] + acc1[0]) * qscale : -INFINITY;
       if constexpr (MQ) {   // token r's position against column c's visible range
         const int64_t hi = col_hi(), lo = col_lo(hi);
-        const int64_t t = tk.fresh ? a.plan.fresh_pos
+        const int64_t t = tk.fresh ? f_fresh_pos(c_k)
                         : tk.sink  ? static_cast<int64_t>(tk.first) + r
                                    : g.S + a.plan.st.n_groups * g.G + tk.first + r;
         if (t > hi || (t >= g.S && t < lo)) s = -INFINITY;
@@ -1213,7 +1283,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mm
         // fused append: the token into its sink slot (widened to fp32) or its
         // ring slot; nothing this launch reads lives there
         uint8_t* base = const_cast<uint8_t*>(unit_base(u_first + cu));
-        const int64_t fp = a.plan.fresh_pos;
+        const int64_t fp = f_fresh_pos(c_k);
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
           for (int e = 4 * lane; e < D; e += 128) {

@@ -315,6 +315,102 @@ cudaError_t attn_run(const kivi_cache& c, const Run& r, const kivi::DecodePlan& 
                                      error, s);
 }
 float* ws_partials(const kivi_cache& c) { return reinterpret_cast<float*>(c.arena + c.g.ws_partials); }
+
+// The plans of runs [first, first + count) for one ragged launch (one query
+// token per sequence); fused: every sequence also attends to and appends one
+// new token taken from the inputs.
+kivi::RunTable run_table(const kivi_cache& c, const std::vector<Run>& runs, size_t first, size_t count,
+                         bool fused) {
+  const Geo& g = c.g;
+  const int64_t npass = (g.rep + 3) / 4;
+  kivi::RunTable t{};
+  t.n = static_cast<int32_t>(count);
+  int64_t pos = 0;
+  for (size_t i = 0; i < count; ++i) {
+    const Run& r = runs[first + i];
+    kivi::DecodePlan pl = plan_for(c, fused ? r.T + 1 : r.T, r.nb);
+    int64_t tc = pl.tc;
+    if (fused) {   // the fresh token is a tail chunk of its own, not read from the cache
+      if (r.T < g.S) pl.st.n_sink -= 1; else pl.st.n_res -= 1;
+      tc = (pl.st.n_sink + 3) / 4 + (pl.st.n_res + 7) / 8 + 1;
+    }
+    kivi::RunPlan& rp = t.r[i];
+    rp.pos0 = pos;
+    rp.g_first = pl.g_first;
+    rp.q_pos0 = pl.q_pos0;
+    rp.fresh_pos = r.T;
+    rp.ubase = static_cast<int32_t>(r.b0 * g.hkv * npass);
+    rp.n_vis = static_cast<int32_t>(pl.n_vis_groups);
+    rp.uw = static_cast<int32_t>(pl.n_vis_groups + tc);
+    rp.n_sink = static_cast<int32_t>(pl.st.n_sink);
+    rp.n_res = static_cast<int32_t>(pl.st.n_res);
+    rp.rs0 = static_cast<int32_t>((pl.st.n_groups * g.G) % g.R);
+    rp.slot0 = static_cast<uint32_t>(g.window > 0 ? pl.g_first % g.n_slots : pl.g_first);
+    rp.b0 = r.b0;
+    rp.nb = r.nb;
+    pos += static_cast<int64_t>(r.nb) * g.hkv * npass * rp.uw;
+  }
+  t.W = pos;
+  return t;
+}
+
+// Decode (fused: append one token from k_fresh / v_fresh first) over every
+// sequence: one launch when all lengths agree, else one ragged launch per
+// kMaxRuns runs (fused: preceded by one flush launch when a run freezes a
+// group).
+cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const __half* k_fresh,
+                       const __half* v_fresh, float* partials, int32_t stride, unsigned* counters,
+                       unsigned* error, cudaStream_t s) {
+  const Geo& g = c.g;
+  const bool fused = k_fresh != nullptr;
+  const std::vector<Run> runs = runs_of(c);
+  if (runs.size() == 1) {
+    const Run& r = runs[0];
+    if (fused) {
+      const State s0 = kivi::state_at(g, r.T), s1 = kivi::state_at(g, r.T + 1);
+      if (s1.n_groups > s0.n_groups) {
+        // the token reaches a full ring: its oldest G tokens freeze first, as
+        // in kivi_append (a launch of its own, before the decode reads them)
+        int64_t g_begin = s0.n_groups;
+        if (s1.n_groups - g.n_slots > g_begin) g_begin = s1.n_groups - g.n_slots;
+        const cudaError_t e = kivi::launch_flush(g, c.arena, k_fresh, v_fresh, r.T, 1, g_begin, s1.n_groups, s);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    kivi::DecodePlan pl = plan_for(c, fused ? r.T + 1 : r.T, r.nb);
+    if (fused) {
+      // the fresh token is attended straight from the inputs (and written into
+      // its sink or ring slot by the same launch), so the cache's own tail is
+      // one token shorter
+      if (r.T < g.S) pl.st.n_sink -= 1; else pl.st.n_res -= 1;
+      pl.tc = static_cast<int32_t>((pl.st.n_sink + 3) / 4 + (pl.st.n_res + 7) / 8 + 1);
+      pl.k_fresh = k_fresh;
+      pl.v_fresh = v_fresh;
+      pl.fresh_pos = r.T;
+    }
+    return attn_run(c, r, pl, q, out, partials, stride, counters, error, s);
+  }
+  for (size_t first = 0; first < runs.size(); first += kivi::kMaxRuns) {
+    const size_t count = runs.size() - first < static_cast<size_t>(kivi::kMaxRuns) ? runs.size() - first
+                                                                                     : kivi::kMaxRuns;
+    const kivi::RunTable t = run_table(c, runs, first, count, fused);
+    if (fused) {
+      bool freezes = false;
+      for (size_t i = first; i < first + count; ++i)
+        freezes = freezes || kivi::state_at(g, runs[i].T + 1).n_groups > kivi::state_at(g, runs[i].T).n_groups;
+      if (freezes) {
+        const cudaError_t e = kivi::launch_flush_ragged(g, c.arena, k_fresh, v_fresh, t, s);
+        if (e != cudaSuccess) return e;
+      }
+    }
+    kivi::DecodePlan pl = plan_for(c, runs[first].T, g.B);   // launch-wide fields: the grid
+    pl.k_fresh = k_fresh;
+    pl.v_fresh = v_fresh;
+    const cudaError_t e = kivi::launch_decode_ragged(g, c.arena, q, out, pl, t, partials, stride, counters, error, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 unsigned* ws_counters(const kivi_cache& c) { return reinterpret_cast<unsigned*>(c.arena + c.g.ws_counters); }
 unsigned* ws_error(const kivi_cache& c) { return reinterpret_cast<unsigned*>(c.arena + c.g.ws_error); }
 
@@ -366,14 +462,9 @@ int kivi_cache_tokens(const kivi_cache* c, int64_t* tokens) {
 int kivi_decode_attn(kivi_cache* c, const void* q, void* out, void* cuda_stream) {
   if (!c || !q || !out) return KIVI_ENULL;
   if (!aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  for (const Run& r : runs_of(*c)) {
-    const kivi::DecodePlan pl = plan_for(*c, r.T, r.nb);
-    const cudaError_t e = attn_run(*c, r, pl, static_cast<const __half*>(q), static_cast<__half*>(out),
-                                   ws_partials(*c), c->g.split_stride, ws_counters(*c), ws_error(*c), s);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
-  return KIVI_OK;
+  return cuda_status(decode_all(*c, static_cast<const __half*>(q), static_cast<__half*>(out), nullptr, nullptr,
+                                ws_partials(*c), c->g.split_stride, ws_counters(*c), ws_error(*c),
+                                static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int kivi_append_decode_attn(kivi_cache* c, const void* k_new, const void* v_new, const void* q, void* out,
@@ -382,36 +473,11 @@ int kivi_append_decode_attn(kivi_cache* c, const void* k_new, const void* v_new,
   if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
   const Geo& g = c->g;
   if (g.window == 0 && max_tokens_of(*c) + 1 > c->p.max_tokens) return KIVI_ECAPACITY;
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  const auto* kh = static_cast<const __half*>(k_new);
-  const auto* vh = static_cast<const __half*>(v_new);
-  for (const Run& r : runs_of(*c)) {
-    const Geo gs = sub_geo(g, r.nb);
-    const int64_t T_old = r.T, T_new = r.T + 1;
-    const int64_t in = static_cast<int64_t>(r.b0) * g.hkv * g.d;   // the run's first input row
-    const State s0 = kivi::state_at(g, T_old), s1 = kivi::state_at(g, T_new);
-    if (s1.n_groups > s0.n_groups) {
-      // the token reaches a full ring: its oldest G tokens freeze first, as in
-      // kivi_append (a launch of its own, before the decode reads the group)
-      int64_t g_begin = s0.n_groups;
-      if (s1.n_groups - g.n_slots > g_begin) g_begin = s1.n_groups - g.n_slots;
-      const cudaError_t e = kivi::launch_flush(gs, run_base(*c, r), kh + in, vh + in, T_old, 1, g_begin,
-                                               s1.n_groups, s);
-      if (e != cudaSuccess) return cuda_status(e);
-    }
-    kivi::DecodePlan pl = plan_for(*c, T_new, r.nb);
-    // the fresh token is attended straight from the inputs (and written into
-    // its sink or ring slot by the same launch), so the cache's own tail is
-    // one token shorter
-    if (T_old < g.S) pl.st.n_sink -= 1; else pl.st.n_res -= 1;
-    pl.tc = static_cast<int32_t>((pl.st.n_sink + 3) / 4 + (pl.st.n_res + 7) / 8 + 1);
-    pl.k_fresh = kh + in;
-    pl.v_fresh = vh + in;
-    pl.fresh_pos = T_old;
-    const cudaError_t e = attn_run(*c, r, pl, static_cast<const __half*>(q), static_cast<__half*>(out),
-                                   ws_partials(*c), g.split_stride, ws_counters(*c), ws_error(*c), s);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
+  const cudaError_t e = decode_all(*c, static_cast<const __half*>(q), static_cast<__half*>(out),
+                                   static_cast<const __half*>(k_new), static_cast<const __half*>(v_new),
+                                   ws_partials(*c), g.split_stride, ws_counters(*c), ws_error(*c),
+                                   static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_status(e);
   for (int64_t& t : c->T) t += 1;
   return KIVI_OK;
 }
@@ -516,15 +582,10 @@ int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda
   unsigned* counters = reinterpret_cast<unsigned*>(bytes + kAlign);
   float* partials = reinterpret_cast<float*>(bytes + head_bytes);
   if (cudaMemsetAsync(bytes, 0, static_cast<size_t>(head_bytes), s) != cudaSuccess) return KIVI_ECUDA;
-  // one launch per run of equal lengths; each leaves the counters zero, and
-  // the launch caps the CTAs so a unit's partials fit
-  for (const Run& r : runs_of(*c)) {
-    const kivi::DecodePlan pl = plan_for(*c, r.T, r.nb);
-    const cudaError_t e = attn_run(*c, r, pl, static_cast<const __half*>(q), static_cast<__half*>(out), partials,
-                                   static_cast<int32_t>(fit), counters, error, s);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
-  return KIVI_OK;
+  // each launch leaves the counters zero and caps its CTAs so a unit's
+  // partials fit
+  return cuda_status(decode_all(*c, static_cast<const __half*>(q), static_cast<__half*>(out), nullptr, nullptr,
+                                partials, static_cast<int32_t>(fit), counters, error, s));
 }
 
 int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {

@@ -32,7 +32,7 @@ struct State {
   int64_t T, n_sink, n_groups, n_res;
 };
 
-inline State state_at(const Geo& g, int64_t T) {
+__host__ __device__ inline State state_at(const Geo& g, int64_t T) {
   State s;
   s.T = T;
   s.n_sink = T < g.S ? T : g.S;
@@ -82,6 +82,38 @@ struct DecodePlan {
   int64_t q_pos0;
 };
 
+// Ragged launches: one decode launch over sequences of different lengths.
+// The batch is cut into runs of consecutive sequences of equal length; each
+// run's plan travels in the kernel's parameters (a grid constant, read with
+// constant loads).  Units keep the uniform numbering (sequence, kv head,
+// head pass), so run k holds units [ubase, ubase + nb * h_kv * npass); their
+// work positions start at pos0, uw per unit.
+struct RunPlan {
+  int64_t pos0;        // first work position of the run's units
+  int64_t g_first;     // first frozen group that can hold a visible token
+  int64_t q_pos0;      // position of the query (T - 1)
+  int64_t fresh_pos;   // fused step: position of the appended token
+  int32_t ubase;       // first unit of the run
+  int32_t uw;          // work positions per unit
+  int32_t n_vis;       // visible frozen groups per unit
+  int32_t n_sink;      // sink tokens read from the cache
+  int32_t n_res;       // ring tokens read from the cache
+  int32_t rs0;         // ring slot of the oldest ring token
+  uint32_t slot0;      // slot of the first visible group
+  int32_t b0, nb;      // the run's sequences
+  int32_t pad;
+};
+constexpr int kMaxRuns = 64;
+struct RunTable {
+  int32_t n;           // runs
+  int32_t pad;
+  int64_t W;           // work positions of the launch
+  RunPlan r[kMaxRuns];
+};
+struct NoRuns {
+  int32_t n;
+};
+
 // Decode launch shape: up to kDecodeWarps warps per CTA and kDecodeCtasPerSm
 // CTAs per SM (the kernel's launch bounds; registers per thread follow).
 constexpr int kDecodeWarps = 8;
@@ -112,5 +144,17 @@ cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half*
 cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
                                   const DecodePlan& plan, float* partials, int32_t stride,
                                   unsigned* counters, unsigned* error, cudaStream_t stream);
+// One decode launch over the runs of `runs` (plan: the launch-wide fields
+// nq = q_rows = 1, ctas, k_fresh / v_fresh for a fused step; runs: per-run
+// plans with pos0, ubase and W filled in by the caller).
+cudaError_t launch_decode_ragged(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
+                                 const DecodePlan& plan, const RunTable& runs, float* partials, int32_t stride,
+                                 unsigned* counters, unsigned* error, cudaStream_t stream);
+// The fused step's flush over a ragged batch: for each sequence b whose next
+// token (at position T_old[b], from the [B][h_kv][1][d] inputs) reaches a
+// full ring, the ring's oldest G tokens become its next frozen group; the
+// other sequences' blocks return at once.  T_old by run (b0, nb, fresh_pos).
+cudaError_t launch_flush_ragged(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
+                                const RunTable& runs, cudaStream_t stream);
 
 }  // namespace kivi

@@ -166,3 +166,19 @@ def test_ragged_argument_errors():
                                       sc.numel(), None) == _abi.KIVI_OK
     assert L.kivi_prefill_bytes(c._h, 4) == -1 and L.kivi_prefill_bytes(c._h, 3) > 0
     torch.cuda.synchronize()
+
+
+def test_more_runs_than_one_ragged_launch_holds():
+    """70 sequences of 70 different lengths: more runs than one ragged launch
+    takes (64), so the decode and the fused step are split over two."""
+    from kivi_quantized_kv_gb300 import KiviConfig
+    cfg = KiviConfig(bits=4, group=16, residual=32, sinks=2, h_q=2, h_kv=1, head_dim=64, batch=70, max_tokens=200)
+    r = Ragged(cfg)
+    r.append([b + 1 for b in range(70)])                  # lengths 1 .. 70
+    r.append([(37 * b) % 61 for b in range(70)])          # ragged again, some zeros
+    assert len(set(r.pos)) > 64
+    for i in range(3):
+        assert r.decode_err(q_of(cfg, 300 + i)) <= TOL
+        assert r.fused_err(q_of(cfg, 400 + i)) <= TOL
+    assert r.bytes_equal()
+    assert r.gpu.read_error() == 0
