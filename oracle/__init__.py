@@ -130,7 +130,7 @@ def pack_row(codes, bits: int) -> np.ndarray:
     out = np.zeros(codes.size * bits // 8, dtype=np.uint8)
     rc = lib().ko_pack_row(_ptr(codes, ctypes.c_uint8), codes.size, bits, _ptr(out, ctypes.c_uint8))
     if rc != 0:
-        raise ValueError("row length * bits must be a multiple of 32")
+        raise ValueError("row length * bits must be a multiple of 32 (b in 2, 4, 8) or 8 (other b)")
     return out
 
 
@@ -139,7 +139,7 @@ def unpack_row(packed, L: int, bits: int) -> np.ndarray:
     out = np.zeros(L, dtype=np.uint8)
     rc = lib().ko_unpack_row(_ptr(packed, ctypes.c_uint8), L, bits, _ptr(out, ctypes.c_uint8))
     if rc != 0:
-        raise ValueError("row length * bits must be a multiple of 32")
+        raise ValueError("row length * bits must be a multiple of 32 (b in 2, 4, 8) or 8 (other b)")
     return out
 
 

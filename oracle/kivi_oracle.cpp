@@ -138,12 +138,45 @@ void quantize(const uint16_t* x, int n, int64_t stride, int bits, uint8_t* codes
 
 // ---------------------------------------------------------------------------
 // Packing of one row of L codes of b bits (the pages fix only "packed u8").
-// Reading: the row is cut into little-endian 32-bit words of 32/b codes; in
-// each word, row element j (0-based inside the word) sits in the low 16-bit
-// half when j is even and in the high half when j is odd, at bit offset
-// b * floor(j/2) inside its half, least significant first.
+// Reading for b in {2, 4, 8}: the row is cut into little-endian 32-bit words
+// of 32/b codes; in each word, row element j (0-based inside the word) sits
+// in the low 16-bit half when j is even and in the high half when j is odd,
+// at bit offset b * floor(j/2) inside its half, least significant first.
+// Reading for the other widths (b in {1, 3, 5, 6, 7}; tract #2329 allows
+// 1..16 bits, kvquant++ recommends 3): a plain bit stream, element j at bits
+// [b j, b j + b) of the row counted from the least significant bit of byte 0,
+// so codes cross byte boundaries and no bit is left empty.
 // ---------------------------------------------------------------------------
+bool word_rule(int bits) { return bits == 2 || bits == 4 || bits == 8; }
+
+int pack_stream(const uint8_t* codes, int L, int bits, uint8_t* out) {
+  if ((static_cast<int64_t>(L) * bits) % 8 != 0) return kInvalid;
+  const int64_t nbytes = static_cast<int64_t>(L) * bits / 8;
+  for (int64_t i = 0; i < nbytes; ++i) out[i] = 0;
+  for (int j = 0; j < L; ++j) {
+    for (int k = 0; k < bits; ++k) {
+      const int64_t bit = static_cast<int64_t>(j) * bits + k;
+      if ((codes[j] >> k) & 1) out[bit / 8] = static_cast<uint8_t>(out[bit / 8] | (1u << (bit % 8)));
+    }
+  }
+  return kOk;
+}
+
+int unpack_stream(const uint8_t* packed, int L, int bits, uint8_t* codes) {
+  if ((static_cast<int64_t>(L) * bits) % 8 != 0) return kInvalid;
+  for (int j = 0; j < L; ++j) {
+    int c = 0;
+    for (int k = 0; k < bits; ++k) {
+      const int64_t bit = static_cast<int64_t>(j) * bits + k;
+      c |= ((packed[bit / 8] >> (bit % 8)) & 1) << k;
+    }
+    codes[j] = static_cast<uint8_t>(c);
+  }
+  return kOk;
+}
+
 int pack_row(const uint8_t* codes, int L, int bits, uint8_t* out) {
+  if (!word_rule(bits)) return pack_stream(codes, L, bits, out);
   if ((static_cast<int64_t>(L) * bits) % 32 != 0) return kInvalid;
   const int per = 32 / bits;
   for (int w = 0; w < L / per; ++w) {
@@ -159,6 +192,7 @@ int pack_row(const uint8_t* codes, int L, int bits, uint8_t* out) {
 }
 
 int unpack_row(const uint8_t* packed, int L, int bits, uint8_t* codes) {
+  if (!word_rule(bits)) return unpack_stream(packed, L, bits, codes);
   if ((static_cast<int64_t>(L) * bits) % 32 != 0) return kInvalid;
   const int per = 32 / bits;
   const uint32_t mask = (1u << bits) - 1u;
@@ -177,7 +211,7 @@ int unpack_row(const uint8_t* packed, int L, int bits, uint8_t* codes) {
 // Parameters, state and layout.
 // ---------------------------------------------------------------------------
 int validate(const ko_params& p) {
-  if (!(p.bits == 2 || p.bits == 4 || p.bits == 8)) return kInvalid;
+  if (p.bits < 1 || p.bits > 8) return kInvalid;   // codes are bytes here; wider codes are out of scope
   if (!(p.head_dim == 64 || p.head_dim == 128)) return kInvalid;
   if (p.group < 16 || p.group > 256 || p.group % 16 != 0) return kInvalid;
   if (p.residual < p.group || p.residual % p.group != 0) return kInvalid;
@@ -461,11 +495,11 @@ void ko_quantize(const uint16_t* x, int32_t n, int64_t stride, int32_t bits, uin
 }
 
 int ko_pack_row(const uint8_t* codes, int32_t L, int32_t bits, uint8_t* out) {
-  if (!(bits == 2 || bits == 4 || bits == 8)) return kInvalid;
+  if (bits < 1 || bits > 8) return kInvalid;
   return pack_row(codes, L, bits, out);
 }
 int ko_unpack_row(const uint8_t* packed, int32_t L, int32_t bits, uint8_t* codes) {
-  if (!(bits == 2 || bits == 4 || bits == 8)) return kInvalid;
+  if (bits < 1 || bits > 8) return kInvalid;
   return unpack_row(packed, L, bits, codes);
 }
 

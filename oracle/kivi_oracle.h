@@ -34,7 +34,7 @@ extern "C" {
 #endif
 
 typedef struct ko_params {
-  int32_t bits;      /* b in {2,4,8} */
+  int32_t bits;      /* b in 1..8 (2, 4, 8: word rule; others: bit stream) */
   int32_t group;     /* G: tokens per frozen key group */
   int32_t residual;  /* R: capacity of the fp16 residual ring */
   int32_t sinks;     /* S: leading tokens kept in fp32 */

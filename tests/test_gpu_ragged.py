@@ -182,3 +182,25 @@ def test_more_runs_than_one_ragged_launch_holds():
         assert r.fused_err(q_of(cfg, 400 + i)) <= TOL
     assert r.bytes_equal()
     assert r.gpu.read_error() == 0
+
+
+def test_ragged_decode_at_the_mha7b_shape():
+    """B 8, 32 heads, d 128, 4-bit, G 32, R 128, S 4 with lengths 4095 - 256 b
+    (eight runs, one ragged launch): every sequence's decode and fused steps
+    against its own oracle cache."""
+    from kivi_quantized_kv_gb300 import KiviConfig
+    cfg = KiviConfig(bits=4, group=32, residual=128, sinks=4, h_q=32, h_kv=32, head_dim=128, batch=8,
+                     max_tokens=4200)
+    r = Ragged.__new__(Ragged)
+    from kivi_quantized_kv_gb300 import KiviCache
+    r.cfg = cfg
+    r.gpu = KiviCache(cfg)
+    r.ref = [oracle.Cache(oparams(cfg, batch=1)) for _ in range(cfg.batch)]
+    r.streams = [random_stream(oparams(cfg, batch=1), 4200, seed=700 + b) for b in range(cfg.batch)]
+    r.pos = [0] * cfg.batch
+    r.append([4095 - 256 * b for b in range(8)])
+    assert r.decode_err(q_of(cfg, 1)) <= TOL
+    for i in range(40):   # crosses group freezes of several sequences at different steps
+        assert r.fused_err(q_of(cfg, 10 + i)) <= TOL
+    assert r.bytes_equal()
+    assert r.gpu.read_error() == 0

@@ -54,7 +54,7 @@ def test_unquantized_prefix_is_textbook_attention(oracle_lib, T):
             assert np.allclose(out[b, hq], ref, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 8])
 @pytest.mark.parametrize("window", [0, 48])
 @pytest.mark.parametrize("T", [37, 100, 257])
 def test_matches_bruteforce_on_dequantized(oracle_lib, bits, window, T):

@@ -132,6 +132,9 @@ def test_sinks_and_ring_hold_inputs(oracle_lib):
 
 # --- an independent, test-side decoder of the documented byte layout -------
 def _unpack(packed, L, bits):
+    if bits not in (2, 4, 8):   # bit stream: element j at bits [b j, b j + b), LSB first
+        flat = np.unpackbits(packed, bitorder="little")[:L * bits].reshape(L, bits).astype(np.int64)
+        return (flat << np.arange(bits)[None, :]).sum(axis=1)
     words = packed.view("<u4")
     per = 32 // bits
     j = np.arange(per)
@@ -171,7 +174,7 @@ def decode_unit_numpy(arena_unit, p, L, T, n_groups):
     return K, V
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("G,d", [(16, 64), (32, 128)])
 def test_independent_decoder_agrees(oracle_lib, bits, G, d):
     p = P(oracle_lib, bits=bits, group=G, residual=2 * G, head_dim=d, batch=1, h_kv=2, h_q=2, max_tokens=200)
@@ -245,7 +248,7 @@ def test_capacity_and_validation(oracle_lib):
     before = c.arena()
     assert c.append(k[:, :, 40:41], v[:, :, 40:41]) == 3
     assert c.T == 40 and np.array_equal(before, c.arena())
-    bad = [dict(bits=3), dict(bits=1), dict(head_dim=96), dict(group=8), dict(group=24),
+    bad = [dict(bits=0), dict(bits=9), dict(head_dim=96), dict(group=8), dict(group=24),
            dict(residual=16), dict(residual=48), dict(sinks=-1), dict(h_q=3), dict(window=16),
            dict(window=-1), dict(batch=0)]
     for kw in bad:
