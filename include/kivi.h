@@ -57,7 +57,11 @@ typedef enum kivi_status {
 } kivi_status;
 
 /* Cache parameters.
- *   bits       b in {2, 4, 8}: code width.
+ *   bits       b in 1..8: code width (tract #2329: configurable width;
+ *              kvquant++ README: 3 bits recommended).  b in {2, 4, 8} decode
+ *              on tensor cores; the other widths pack as a bit stream and
+ *              decode on CUDA cores, need G <= 64 and have no multi-query
+ *              (prefill) attention.
  *   group      G: tokens per frozen key group; a multiple of 16 in [16, 256].
  *   residual   R: capacity of the fp16 residual ring; R >= G and R % G == 0.
  *   sinks      S in [0, 1024]: leading tokens kept in fp32.
@@ -97,9 +101,11 @@ typedef struct kivi_params {
  *     blk_ks  fp16 key Δ[d] then key min[d] (one pair per channel)
  *     blk_vq  value codes, channel-major: d rows of G*b/8 bytes
  *     blk_vs  fp16 (Δ, min) per token, G pairs
- *   A row of codes is cut into little-endian 32-bit words of 32/b codes;
- *   element j of a word sits in the low 16-bit half when j is even, the high
- *   half when j is odd, at bit b*floor(j/2) of its half.
+ *   b in {2, 4, 8}: a row of codes is cut into little-endian 32-bit words
+ *   of 32/b codes; element j of a word sits in the low 16-bit half when j is
+ *   even, the high half when j is odd, at bit b*floor(j/2) of its half.
+ *   Other b: a bit stream, element j at bits [b j, b j + b) of the row from
+ *   the least significant bit of byte 0 (codes cross byte boundaries).
  * The workspace (workspace_offset, workspace_bytes) holds split-K partial
  * results and per-unit counters; its contents are scratch. */
 typedef struct kivi_layout {
@@ -257,8 +263,8 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  * oldest part of its first queries' windows).  The newest query's row equals
  * kivi_decode_attn's output for it.  Work: as kivi_decode_attn with n_queries
  * times the query rows per kv head, each row masked to its own positions.
- * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536), EALIGN, ENOSPC
- * (scratch too small), ECUDA. */
+ * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, or b outside
+ * {2, 4, 8}), EALIGN, ENOSPC (scratch too small), ECUDA. */
 int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream);
 

@@ -125,6 +125,32 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
   }
   __syncthreads();
 
+  if (!(b == 2 || b == 4 || b == 8)) {
+    // the other widths: a bit stream per row, code j at bits [b j, b j + b);
+    // one thread per output byte
+    const int krow = d * b / 8, vrow = G * b / 8;
+    uint8_t* kq8 = blk + g.blk_kq;
+    for (int i = threadIdx.x; i < G * krow; i += blockDim.x) {
+      const int t = i / krow, byte = i % krow;
+      uint32_t v = 0;
+      for (int k = 0; k < 8; ++k) {
+        const int bit = 8 * byte + k, j = bit / b;
+        v |= ((static_cast<uint32_t>(kc[t * d + j]) >> (bit - j * b)) & 1u) << k;
+      }
+      kq8[i] = static_cast<uint8_t>(v);
+    }
+    uint8_t* vq8 = blk + g.blk_vq;
+    for (int i = threadIdx.x; i < d * vrow; i += blockDim.x) {
+      const int c = i / vrow, byte = i % vrow;
+      uint32_t v = 0;
+      for (int k = 0; k < 8; ++k) {
+        const int bit = 8 * byte + k, j = bit / b;
+        v |= ((static_cast<uint32_t>(vc[j * d + c]) >> (bit - j * b)) & 1u) << k;
+      }
+      vq8[i] = static_cast<uint8_t>(v);
+    }
+    return;
+  }
   // pack: element j of a 32-bit word goes to half (j & 1), bit b * (j >> 1)
   const int per = 32 / b;
   uint32_t* kq = reinterpret_cast<uint32_t*>(blk + g.blk_kq);

@@ -9,6 +9,13 @@
 namespace kivi {
 namespace mma {
 
+// the kernel of an instantiation
+template <int D, int BITS, int CH, bool MQ, bool RG>
+constexpr auto kernel_of() {
+  if constexpr (RG) return decode_mma_ragged_kernel<D, BITS, CH, MQ>;
+  else return decode_mma_kernel<D, BITS, CH, MQ, false>;
+}
+
 template <int D, int BITS, int CH, bool MQ, bool RG>
 cudaError_t prepare() {
   // opt in to the largest dynamic shared memory once per instantiation
@@ -20,10 +27,10 @@ cudaError_t prepare() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, decode_mma_kernel<D, BITS, CH, MQ, RG>);
+  e = cudaFuncGetAttributes(&fa, kernel_of<D, BITS, CH, MQ, RG>());
   if (e != cudaSuccess) return e;
   // the opt-in limit covers static + dynamic shared memory
-  e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, CH, MQ, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(kernel_of<D, BITS, CH, MQ, RG>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            optin - static_cast<int>(fa.sharedSizeBytes));
   if (e == cudaSuccess) done.store(1, std::memory_order_release);
   return e;
@@ -46,7 +53,8 @@ cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int th
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BITS, CH, MQ, RG>, a, rt);
+  if constexpr (RG) e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG>(), a, rt);
+  else e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG>(), a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -55,7 +63,7 @@ template <int D, int BITS, int CH, bool MQ, bool RG>
 int occupancy_one(int threads, int smem) {
   if (prepare<D, BITS, CH, MQ, RG>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, BITS, CH, MQ, RG>, threads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_of<D, BITS, CH, MQ, RG>(), threads, smem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }

@@ -571,11 +571,10 @@ __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, 
 template <bool RG>
 using RunTableT = typename std::conditional<RG, RunTable, NoRuns>::type;
 
-// RG: a ragged launch; per-unit plan values come from the run table `rt`
-// (the unit's run) instead of the launch's plan.
+// The kernel body.  RG: a ragged launch; per-unit plan values come from the
+// run table `rt` (the unit's run) instead of the launch's plan.
 template <int D, int BITS, int CH, bool MQ, bool RG>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
-    decode_mma_kernel(const Args a, const __grid_constant__ RunTableT<RG> rt) {
+__device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& rt) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   using WS = WarpSmem<D, CH>;
   constexpr int RK = D * BITS / 8;          // key row bytes
@@ -1317,6 +1316,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
       if (++c_st == a.ns) { c_st = 0; c_ph ^= 1u; }
     }
   }
+}
+
+// Uniform launches: the plan is the launch's own (one kernel parameter).
+template <int D, int BITS, int CH, bool MQ, bool RG>
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mma_kernel(const Args a) {
+  const NoRuns none{0};
+  decode_body<D, BITS, CH, MQ, false>(a, none);
+}
+
+// Ragged launches: the runs' plans travel as a grid constant.
+template <int D, int BITS, int CH, bool MQ>
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
+    decode_mma_ragged_kernel(const Args a, const __grid_constant__ RunTable rt) {
+  decode_body<D, BITS, CH, MQ, true>(a, rt);
 }
 
 }  // namespace mma

@@ -49,7 +49,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int validate(const kivi_params* p) {
   if (!p) return KIVI_ENULL;
-  if (!(p->bits == 2 || p->bits == 4 || p->bits == 8)) return KIVI_EINVAL;
+  if (p->bits < 1 || p->bits > 8) return KIVI_EINVAL;
+  // the bit-stream widths decode on CUDA cores with a frozen group in one
+  // warp's shared memory
+  if (!kivi::word_rule(p->bits) && p->group > 64) return KIVI_EINVAL;
   if (!(p->head_dim == 64 || p->head_dim == 128)) return KIVI_EINVAL;
   if (p->group < 16 || p->group > 256 || p->group % 16 != 0) return KIVI_EINVAL;
   if (p->residual < p->group || p->residual % p->group != 0) return KIVI_EINVAL;
@@ -364,6 +367,23 @@ cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const 
   const Geo& g = c.g;
   const bool fused = k_fresh != nullptr;
   const std::vector<Run> runs = runs_of(c);
+  if (!kivi::word_rule(g.bits)) {
+    // bit-stream widths: per run, the new token's append (fused step) and a
+    // CUDA-core decode
+    for (const Run& r : runs) {
+      if (fused) {
+        const cudaError_t e = append_run(c, r, k_fresh, v_fresh, 1, 1, s);
+        if (e != cudaSuccess) return e;
+      }
+      const kivi::DecodePlan pl = plan_for(c, fused ? r.T + 1 : r.T, r.nb);
+      const Geo gs = sub_geo(g, r.nb);
+      const int64_t row0 = static_cast<int64_t>(r.b0) * g.hq * g.d;
+      const cudaError_t e = kivi::launch_decode_simt(gs, run_base(c, r), q + row0, out + row0, pl, partials, stride,
+                                                     counters, c.num_sms * 4, s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   if (runs.size() == 1) {
     const Run& r = runs[0];
     if (fused) {
@@ -697,6 +717,7 @@ size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
 int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch) return KIVI_ENULL;
+  if (!kivi::word_rule(c->g.bits)) return KIVI_EINVAL;   // multi-query attention: b in {2, 4, 8}
   if (n_queries > min_tokens_of(*c) || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
   if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(c->g, n_queries)) return KIVI_ENOSPC;
@@ -707,6 +728,7 @@ int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries
 int kivi_prefill_attn_ragged(kivi_cache* c, const void* q, void* out, const int64_t* n_queries, int64_t m_max,
                              void* scratch, size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch || !n_queries) return KIVI_ENULL;
+  if (!kivi::word_rule(c->g.bits)) return KIVI_EINVAL;
   if (!prefill_count_ok(c->g, m_max)) return KIVI_EINVAL;
   for (int32_t b = 0; b < c->g.B; ++b)
     if (n_queries[b] < 0 || n_queries[b] > m_max || n_queries[b] > c->T[b]) return KIVI_EINVAL;
