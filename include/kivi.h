@@ -60,8 +60,8 @@ typedef enum kivi_status {
  *   bits       b in 1..8: code width (tract #2329: configurable width;
  *              kvquant++ README: 3 bits recommended).  b in {2, 4, 8} decode
  *              on tensor cores; the other widths pack as a bit stream and
- *              decode on CUDA cores, need G <= 64 and have no multi-query
- *              (prefill) attention.
+ *              decode on CUDA cores, need G in {32, 64} and have no
+ *              multi-query (prefill) attention.
  *   group      G: tokens per frozen key group; a multiple of 16 in [16, 256].
  *   residual   R: capacity of the fp16 residual ring; R >= G and R % G == 0.
  *   sinks      S in [0, 1024]: leading tokens kept in fp32.

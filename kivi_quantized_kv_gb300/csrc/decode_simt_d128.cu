@@ -1,0 +1,14 @@
+// decode_simt_d128.cu — the head-dim-128 instantiations of the CUDA-core decode
+// kernel (decode_simt.cuh), one translation unit per head dim so they build
+// in parallel.
+#include "decode_simt.cuh"
+
+namespace kivi {
+namespace simt {
+
+cudaError_t launch_d128(const Args& a, int ctas, int smem, cudaStream_t s, int* resident) {
+  return launch_d<128>(a, ctas, smem, s, resident);
+}
+
+}  // namespace simt
+}  // namespace kivi

@@ -50,9 +50,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int validate(const kivi_params* p) {
   if (!p) return KIVI_ENULL;
   if (p->bits < 1 || p->bits > 8) return KIVI_EINVAL;
-  // the bit-stream widths decode on CUDA cores with a frozen group in one
-  // warp's shared memory
-  if (!kivi::word_rule(p->bits) && p->group > 64) return KIVI_EINVAL;
+  // the bit-stream widths decode on CUDA cores, a frozen group in one warp's
+  // shared memory and its value rows whole 32-bit words
+  if (!kivi::word_rule(p->bits) && p->group != 32 && p->group != 64) return KIVI_EINVAL;
   if (!(p->head_dim == 64 || p->head_dim == 128)) return KIVI_EINVAL;
   if (p->group < 16 || p->group > 256 || p->group % 16 != 0) return KIVI_EINVAL;
   if (p->residual < p->group || p->residual % p->group != 0) return KIVI_EINVAL;
@@ -379,7 +379,7 @@ cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const 
       const Geo gs = sub_geo(g, r.nb);
       const int64_t row0 = static_cast<int64_t>(r.b0) * g.hq * g.d;
       const cudaError_t e = kivi::launch_decode_simt(gs, run_base(c, r), q + row0, out + row0, pl, partials, stride,
-                                                     counters, c.num_sms * 4, s);
+                                                     counters, c.num_sms, s);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -54,7 +54,7 @@ def test_cache_bytes_covers_the_oracle_layout(abi, oracle_lib):
         assert nb - lay["cache_bytes"] <= 8 * 1024 * 1024 + lay["cache_bytes"] // 100
 
 
-@pytest.mark.parametrize("kw", [dict(bits=0), dict(bits=9), dict(bits=16), dict(bits=3, group=128, residual=128), dict(head_dim=96), dict(group=8), dict(group=40),
+@pytest.mark.parametrize("kw", [dict(bits=0), dict(bits=9), dict(bits=16), dict(bits=3, group=128, residual=128), dict(bits=5, group=16, residual=32), dict(head_dim=96), dict(group=8), dict(group=40),
                                 dict(residual=16), dict(residual=48), dict(sinks=-1), dict(h_q=6),
                                 dict(h_q=36, h_kv=4), dict(window=16, max_tokens=0), dict(window=-1),
                                 dict(batch=0), dict(max_tokens=-1)])

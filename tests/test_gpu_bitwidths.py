@@ -25,9 +25,9 @@ def _built():
 
 CASES = [
     dict(bits=3, group=32, residual=64, sinks=4, h_q=8, h_kv=2, head_dim=128, batch=2, max_tokens=600),
-    dict(bits=1, group=16, residual=32, sinks=1, h_q=4, h_kv=4, head_dim=64, batch=2, max_tokens=600),
+    dict(bits=1, group=32, residual=32, sinks=1, h_q=4, h_kv=4, head_dim=64, batch=2, max_tokens=600),
     dict(bits=5, group=64, residual=64, sinks=0, h_q=16, h_kv=2, head_dim=128, batch=1, max_tokens=600),
-    dict(bits=6, group=16, residual=32, sinks=3, h_q=6, h_kv=2, head_dim=64, batch=2, max_tokens=600),
+    dict(bits=6, group=32, residual=64, sinks=3, h_q=6, h_kv=2, head_dim=64, batch=2, max_tokens=600),
     dict(bits=7, group=32, residual=32, sinks=2, h_q=4, h_kv=1, head_dim=128, batch=3, max_tokens=0, window=96),
 ]
 
