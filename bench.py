@@ -773,7 +773,8 @@ def main():
 
 
 DECODE_SOURCES = ("kivi_internal.cuh", "decode_mma.cuh", "decode_launch.cuh", "decode.cu",
-                  "decode_b2.cu", "decode_b4.cu", "decode_b8.cu")
+                  "decode_b2.cu", "decode_b4.cu", "decode_b8.cu", "decode_simt.cuh", "decode_simt.cu",
+                  "decode_simt_d64.cu", "decode_simt_d128.cu")
 
 
 def decode_sources_sha():
