@@ -403,7 +403,7 @@ def run_ours(args, rank, world, device):
         # flush launch when any of them freezes a group)
         runs = [b for b in range(w.batch) if b == 0 or T_now[r][b] != T_now[r][b - 1]]
         freezes = [state_at(w, T_now[r][b0] + 1)[1] > state_at(w, T_now[r][b0])[1] for b0 in runs]
-        if w.bits not in (2, 4, 8):   # bit-stream widths: per run, the append (flush, write) and a decode
+        if w.bits not in (2, 4, 8) and w.head_dim != 128:   # CUDA-core widths: per run, append (flush, write) + decode
             launches += sum((2 if f else 1) + 1 for f in freezes)
         elif not fused:   # kivi_append, one launch pair (flush, write) per run, then the decode
             launches += sum(2 if f else 1 for f in freezes) + -(-len(runs) // 64)

@@ -52,7 +52,8 @@ int decode_ctas_per_sm(const Geo& g) {
   const int smem = decode_smem(sh, g.split_stride);
   if (g.bits == 2) return mma::occupancy_b2(g, threads, smem);
   if (g.bits == 4) return mma::occupancy_b4(g, threads, smem);
-  return mma::occupancy_b8(g, threads, smem);
+  if (g.bits == 8) return mma::occupancy_b8(g, threads, smem);
+  return mma::occupancy_stream_b(g.bits, g, threads, smem);
 }
 
 cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
@@ -101,7 +102,8 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
   const int smem = decode_smem(sh, stride);
   if (g.bits == 2) return mma::launch_b2(a, grid, threads, smem, stream);
   if (g.bits == 4) return mma::launch_b4(a, grid, threads, smem, stream);
-  return mma::launch_b8(a, grid, threads, smem, stream);
+  if (g.bits == 8) return mma::launch_b8(a, grid, threads, smem, stream);
+  return mma::launch_stream_b(g.bits, a, grid, threads, smem, stream);
 }
 
 cudaError_t launch_decode_ragged(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
@@ -143,7 +145,8 @@ cudaError_t launch_decode_ragged(const Geo& g, const uint8_t* arena, const __hal
   const int smem = decode_smem(sh, stride);
   if (g.bits == 2) return mma::launch_rg_b2(a, runs, grid, threads, smem, stream);
   if (g.bits == 4) return mma::launch_rg_b4(a, runs, grid, threads, smem, stream);
-  return mma::launch_rg_b8(a, runs, grid, threads, smem, stream);
+  if (g.bits == 8) return mma::launch_rg_b8(a, runs, grid, threads, smem, stream);
+  return mma::launch_rg_stream_b(g.bits, a, runs, grid, threads, smem, stream);
 }
 
 cudaError_t launch_decode(const Geo& g, uint8_t* arena, const __half* q, __half* out,

@@ -80,30 +80,48 @@ cudaError_t launch_mq(const Args& a, const RunTableT<RG>& rt, dim3 grid, int thr
               : launch_one<128, BITS, 16, MQ, RG>(a, rt, grid, threads, smem, s);
 }
 
+// bit-stream widths: head dim 128 and 32-token chunks only (a lane's quarter
+// of a key row, and its 8 codes of a value row, start on 32-bit words)
+template <int BITS, bool MQ, bool RG>
+cudaError_t launch_stream(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
+  if (a.g.d != 128 || (a.g.G % 32) != 0) return cudaErrorInvalidValue;
+  return launch_one<128, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s);
+}
+
 template <int BITS>
 cudaError_t launch_bits(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
   const NoRuns none{0};
   // the single-query instantiation assumes one query token per sequence row
-  return a.plan.q_rows > 1 ? launch_mq<BITS, true, false>(a, none, grid, threads, smem, s)
-                           : launch_mq<BITS, false, false>(a, none, grid, threads, smem, s);
+  if constexpr (stream_bits<BITS>()) {
+    return a.plan.q_rows > 1 ? launch_stream<BITS, true, false>(a, none, grid, threads, smem, s)
+                             : launch_stream<BITS, false, false>(a, none, grid, threads, smem, s);
+  } else {
+    return a.plan.q_rows > 1 ? launch_mq<BITS, true, false>(a, none, grid, threads, smem, s)
+                             : launch_mq<BITS, false, false>(a, none, grid, threads, smem, s);
+  }
 }
 
 // ragged launches: one query token per sequence (decode and the fused step)
 template <int BITS>
 cudaError_t launch_bits_ragged(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
                                cudaStream_t s) {
-  return launch_mq<BITS, false, true>(a, rt, grid, threads, smem, s);
+  if constexpr (stream_bits<BITS>()) return launch_stream<BITS, false, true>(a, rt, grid, threads, smem, s);
+  else return launch_mq<BITS, false, true>(a, rt, grid, threads, smem, s);
 }
 
 // the other instantiations have the same launch bounds and shared memory
 template <int BITS>
 int occupancy_bits(const Geo& g, int threads, int smem) {
-  const bool ch32 = (g.G % 32) == 0;
-  if (g.d == 64)
-    return ch32 ? occupancy_one<64, BITS, 32, false, false>(threads, smem)
-                : occupancy_one<64, BITS, 16, false, false>(threads, smem);
-  return ch32 ? occupancy_one<128, BITS, 32, false, false>(threads, smem)
-              : occupancy_one<128, BITS, 16, false, false>(threads, smem);
+  if constexpr (stream_bits<BITS>()) {
+    return occupancy_one<128, BITS, 32, false, false>(threads, smem);
+  } else {
+    const bool ch32 = (g.G % 32) == 0;
+    if (g.d == 64)
+      return ch32 ? occupancy_one<64, BITS, 32, false, false>(threads, smem)
+                  : occupancy_one<64, BITS, 16, false, false>(threads, smem);
+    return ch32 ? occupancy_one<128, BITS, 32, false, false>(threads, smem)
+                : occupancy_one<128, BITS, 16, false, false>(threads, smem);
+  }
 }
 
 // defined in decode_b2.cu, decode_b4.cu, decode_b8.cu
@@ -113,6 +131,11 @@ cudaError_t launch_b8(const Args& a, dim3 grid, int threads, int smem, cudaStrea
 cudaError_t launch_rg_b2(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem, cudaStream_t s);
 cudaError_t launch_rg_b4(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem, cudaStream_t s);
 cudaError_t launch_rg_b8(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem, cudaStream_t s);
+// the bit-stream widths (decode_b1.cu, decode_b3.cu, decode_b5.cu, decode_b6.cu, decode_b7.cu)
+cudaError_t launch_stream_b(int bits, const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_rg_stream_b(int bits, const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
+                               cudaStream_t s);
+int occupancy_stream_b(int bits, const Geo& g, int threads, int smem);
 int occupancy_b2(const Geo& g, int threads, int smem);
 int occupancy_b4(const Geo& g, int threads, int smem);
 int occupancy_b8(const Geo& g, int threads, int smem);

@@ -292,10 +292,22 @@ __host__ __device__ constexpr bool pair_hi(int p) {  // codes in bits 8..15
   return BITS * (p % (16 / BITS)) >= 8;
 }
 
+// Widths packed as a bit stream (b outside {2, 4, 8}): element j of a slice
+// at bit b j of its words taken as one little-endian bit string.
+template <int BITS>
+__host__ __device__ constexpr bool stream_bits() { return !(BITS == 2 || BITS == 4 || BITS == 8); }
+
 // fp16x2 of pair p as exact subnormals: low half = element 2p, high half =
-// element 2p + 1, each code * 2^(pair_kb(p) - 24).
+// element 2p + 1, each code * 2^(pair_kb(p) - 24) (bit-stream widths: both
+// codes moved to bit 0 of their halves, class 0).
 template <int BITS>
 __device__ __forceinline__ uint32_t code_pair(const uint32_t* w, int p) {
+  if constexpr (stream_bits<BITS>()) {
+    constexpr uint32_t M = (1u << BITS) - 1u;
+    const int bit = 2 * BITS * p, wi = bit >> 5, sh = bit & 31;
+    const uint32_t t = (sh + 2 * BITS <= 32) ? (w[wi] >> sh) : __funnelshift_r(w[wi], w[wi + 1], sh);
+    return (t & M) | ((t << (16 - BITS)) & (M << 16));
+  }
   const uint32_t x = w[p / (16 / BITS)];
   if constexpr (BITS == 8) {
     return pair_hi<BITS>(p) ? prmt(x, 0u, 0x4341u) : (x & 0x00FF00FFu);
@@ -310,7 +322,9 @@ __device__ __forceinline__ uint32_t code_pair(const uint32_t* w, int p) {
 // list of the NP pairs.
 template <int BITS, int NP>
 __host__ __device__ constexpr int ord_pair(int n) {
-  if constexpr (BITS == 4) {
+  if constexpr (stream_bits<BITS>()) {
+    return n;
+  } else if constexpr (BITS == 4) {
     const int cls = n / (NP / 2), k = n % (NP / 2);
     return 4 * (k / 2) + 2 * (k % 2) + cls;
   } else if constexpr (BITS == 2) {
@@ -321,15 +335,17 @@ __host__ __device__ constexpr int ord_pair(int n) {
   }
 }
 template <int BITS>
-__host__ __device__ constexpr int n_acc() { return BITS == 2 ? 4 : 2; }
+__host__ __device__ constexpr int n_acc() { return stream_bits<BITS>() ? 1 : BITS == 2 ? 4 : 2; }
 // accumulator of the score MMA that takes sorted pairs 2j, 2j + 1
 template <int BITS, int NP>
 __host__ __device__ constexpr int acc_of(int j) {
+  if constexpr (stream_bits<BITS>()) return 0;
   return BITS == 8 ? (j & 1) : pair_kb<BITS>(ord_pair<BITS, NP>(2 * j)) / (BITS == 4 ? 4 : 2);
 }
 // 2^-k of accumulator a
 template <int BITS>
 __host__ __device__ constexpr float acc_scale(int a) {
+  if constexpr (stream_bits<BITS>()) return 1.f;
   return BITS == 8 ? 1.f : BITS == 4 ? (a ? 0.0625f : 1.f) : (a == 0 ? 1.f : a == 1 ? 0.25f : a == 2 ? 0.0625f : 0.015625f);
 }
 
@@ -853,7 +869,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
 #pragma unroll
   for (int i = 0; i < TPL; ++i) {
     const int l = (TPL * r + i) % (CH / 4);
-    const int kb = (BITS * ((l / 2) % (16 / BITS))) % 8;
+    const int kb = stream_bits<BITS>() ? 0 : (BITS * ((l / 2) % (16 / (stream_bits<BITS>() ? 1 : BITS)))) % 8;
     vscl[i] = __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);
   }
   const float sc_scale = qscale * kTwo24;
@@ -867,8 +883,14 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   const uint32_t o_vs = static_cast<uint32_t>(g.blk_vs) + TPL * r * 4;   // value (Δ, min) of token TPL*r
   const uint32_t vrow = static_cast<uint32_t>(g.G) * BITS / 8;           // bytes of one value-code row
   const uint32_t vrow8 = 8 * vrow, vrow16 = 16 * vrow;
-  const uint32_t o_vq = static_cast<uint32_t>(g.blk_vq) + r * vrow + (QV >= 32 ? c * (QV / 8) : ((c * QV) / 32) * 4);
-  const int vsh = QV >= 32 ? 0 : ((c * QV) % 32) / 2;   // the lane's codes within their word
+  // bit streams: the lane's 8 codes of a 32-token chunk start at bit 8 c b
+  // of the chunk; the word holding that bit and the shift inside it
+  constexpr bool kStream = stream_bits<BITS>();
+  const uint32_t o_vq = kStream ? static_cast<uint32_t>(g.blk_vq) + r * vrow + 4 * ((8 * c * BITS) >> 5)
+                                : static_cast<uint32_t>(g.blk_vq) + r * vrow +
+                                      (QV >= 32 ? c * (QV / 8) : ((c * QV) / 32) * 4);
+  const int vsh = kStream ? (8 * c * BITS) & 31
+                          : (QV >= 32 ? 0 : ((c * QV) % 32) / 2);   // the lane's codes within their word
 
   // ------------------------------------------------------------ consumer
   const int nunits = u_last - u_first + 1;
@@ -1038,7 +1060,13 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
           // two rows of a shared-memory phase fall in different bank halves
           const uint32_t row0 = blk + o_k0 + (s0 + 2 * v2) * RK;
           const uint32_t row1 = blk + o_k1 + (s0 + 2 * v2) * RK;
-          if constexpr (KW >= 4) {
+          if constexpr (kStream) {   // a quarter of b words, 4-byte aligned
+#pragma unroll
+            for (int i = 0; i < KW; ++i) {
+              w0[i] = lds32(row0 + 4 * i);
+              w1[i] = lds32(row1 + 4 * i);
+            }
+          } else if constexpr (KW >= 4) {
 #pragma unroll
             for (int i = 0; i < KW; i += 4) {
               const uint4 x = lds128(row0 + 4 * i);
@@ -1158,10 +1186,15 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         const uint32_t vq = blk + o_vq + s0 * BITS / 8;
 #pragma unroll
         for (int ct = 0; ct < NCT; ++ct) {
-          uint32_t v0[VW], v1[VW];
+          uint32_t v0[kStream ? 2 : VW], v1[kStream ? 2 : VW];
           const uint32_t rowa = vq + ct * vrow16;
           const uint32_t rowb = rowa + vrow8;
-          if constexpr (VW == 2) {
+          if constexpr (kStream) {   // the lane's 8 codes: a 64-bit window from three words
+            const uint32_t a0 = lds32(rowa), a1 = lds32(rowa + 4), a2 = lds32(rowa + 8);
+            const uint32_t b0 = lds32(rowb), b1 = lds32(rowb + 4), b2 = lds32(rowb + 8);
+            v0[0] = __funnelshift_r(a0, a1, vsh); v0[1] = __funnelshift_r(a1, a2, vsh);
+            v1[0] = __funnelshift_r(b0, b1, vsh); v1[1] = __funnelshift_r(b1, b2, vsh);
+          } else if constexpr (VW == 2) {
             const uint2 x = lds64(rowa), y = lds64(rowb);
             v0[0] = x.x; v0[1] = x.y; v1[0] = y.x; v1[1] = y.y;
           } else if constexpr (QV >= 32) {

@@ -319,6 +319,10 @@ cudaError_t attn_run(const kivi_cache& c, const Run& r, const kivi::DecodePlan& 
 }
 float* ws_partials(const kivi_cache& c) { return reinterpret_cast<float*>(c.arena + c.g.ws_partials); }
 
+// Bit-stream widths decode on tensor cores at head dim 128 (a lane's quarter
+// of a key row is whole 32-bit words) and on CUDA cores at head dim 64.
+bool simt_path(const Geo& g) { return !kivi::word_rule(g.bits) && g.d != 128; }
+
 // The plans of runs [first, first + count) for one ragged launch (one query
 // token per sequence); fused: every sequence also attends to and appends one
 // new token taken from the inputs.
@@ -367,9 +371,9 @@ cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const 
   const Geo& g = c.g;
   const bool fused = k_fresh != nullptr;
   const std::vector<Run> runs = runs_of(c);
-  if (!kivi::word_rule(g.bits)) {
-    // bit-stream widths: per run, the new token's append (fused step) and a
-    // CUDA-core decode
+  if (simt_path(g)) {
+    // bit-stream widths at head dim 64: per run, the new token's append
+    // (fused step) and a CUDA-core decode
     for (const Run& r : runs) {
       if (fused) {
         const cudaError_t e = append_run(c, r, k_fresh, v_fresh, 1, 1, s);
@@ -717,7 +721,7 @@ size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
 int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch) return KIVI_ENULL;
-  if (!kivi::word_rule(c->g.bits)) return KIVI_EINVAL;   // multi-query attention: b in {2, 4, 8}
+  if (simt_path(c->g)) return KIVI_EINVAL;   // multi-query attention: the tensor-core path
   if (n_queries > min_tokens_of(*c) || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
   if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(c->g, n_queries)) return KIVI_ENOSPC;
@@ -728,7 +732,7 @@ int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries
 int kivi_prefill_attn_ragged(kivi_cache* c, const void* q, void* out, const int64_t* n_queries, int64_t m_max,
                              void* scratch, size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch || !n_queries) return KIVI_ENULL;
-  if (!kivi::word_rule(c->g.bits)) return KIVI_EINVAL;
+  if (simt_path(c->g)) return KIVI_EINVAL;
   if (!prefill_count_ok(c->g, m_max)) return KIVI_EINVAL;
   for (int32_t b = 0; b < c->g.B; ++b)
     if (n_queries[b] < 0 || n_queries[b] > m_max || n_queries[b] > c->T[b]) return KIVI_EINVAL;

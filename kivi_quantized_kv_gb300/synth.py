@@ -72,11 +72,14 @@ WORKLOADS = {
     "swa_mistral": Workload("swa_mistral", batch=32, h_q=32, h_kv=8, head_dim=128, tokens=16384,
                             bits=8, group=64, residual=64, sinks=4, window=4096, rope=True),
     # the mha7b and gqa8b shapes at 3 bits (kvquant++'s recommended width),
-    # packed as a bit stream and decoded on CUDA cores
+    # packed as a bit stream
     "mha7b_b3": Workload("mha7b_b3", batch=8, h_q=32, h_kv=32, head_dim=128, tokens=4096, bits=3,
                          group=32, residual=128, sinks=4),
     "gqa8b_b3": Workload("gqa8b_b3", batch=4, h_q=32, h_kv=8, head_dim=128, tokens=32768, bits=3,
                          group=32, residual=128, sinks=4, rope=True),
+    # head dim 64 at 3 bits: the CUDA-core decode of the bit-stream widths
+    "mha_d64_b3": Workload("mha_d64_b3", batch=8, h_q=32, h_kv=32, head_dim=64, tokens=4096, bits=3,
+                           group=32, residual=128, sinks=4),
 }
 
 

@@ -1,8 +1,9 @@
 """Code widths outside {2, 4, 8} (tract #2329: configurable 1..16 bits; the
 kvquant++ README recommends 3) against the oracle, through the C ABI.
 
-These widths pack as a plain bit stream and decode on CUDA cores
-(decode_simt.cu).  Bytes must equal the oracle's; decode and fused steps
+These widths pack as a plain bit stream and decode on the tensor cores at
+head dim 128 (two codes unpacked into one fp16x2 operand register) and on
+CUDA cores at head dim 64 (decode_simt.cuh).  Bytes must equal the oracle's; decode and fused steps
 within 2e-3.  Streams cross sinks, the filling ring, group freezes, a wrapping
 window and ragged lengths.
 """
@@ -57,7 +58,10 @@ def test_bit_stream_widths_match_oracle(shape):
     assert p.gpu.read_error() == 0
 
 
-def test_three_bits_ragged_and_prefill_refusal():
+def test_three_bits_ragged_and_prefill():
+    """3 bits at head dim 128 (the tensor-core path): a ragged batch decodes
+    per sequence and chunked prefill matches the oracle; at head dim 64 (the
+    CUDA-core path) multi-query attention is refused."""
     import ctypes
     from kivi_quantized_kv_gb300 import KiviCache, KiviConfig, _abi
     import oracle
@@ -74,8 +78,18 @@ def test_three_bits_ragged_and_prefill_refusal():
     out = c.decode(q.cuda()).float().cpu().numpy()
     for b in range(3):
         assert row_rel_err(out[b:b + 1], refs[b].decode_attn(q[b:b + 1].numpy())) <= TOL
-    sc = torch.empty(c.prefill_scratch_bytes(4), dtype=torch.uint8, device="cuda")
-    qq = torch.zeros((3, 4, 4, 128), dtype=torch.float16, device="cuda")
+    g = torch.Generator().manual_seed(9)
+    qq = torch.randn((3, 7, 4, 128), generator=g).half()
+    pout = c.prefill_ragged(qq.cuda(), [7, 7, 7]).float().cpu().numpy()
+    for b in range(3):
+        assert row_rel_err(pout[b:b + 1], refs[b].prefill_attn(qq[b:b + 1].numpy())) <= TOL
+    assert c.read_error() == 0
+    small = KiviConfig(bits=3, group=32, residual=64, sinks=4, h_q=4, h_kv=4, head_dim=64, batch=1, max_tokens=64)
+    c64 = KiviCache(small)
+    z = torch.zeros((1, 4, 8, 64), dtype=torch.float16, device="cuda")
+    c64.append(z, z)
+    sc = torch.empty(c64.prefill_scratch_bytes(4), dtype=torch.uint8, device="cuda")
+    q4 = torch.zeros((1, 4, 4, 64), dtype=torch.float16, device="cuda")
     vp = ctypes.c_void_p
-    assert _abi.lib().kivi_prefill_attn(c._h, vp(qq.data_ptr()), vp(qq.data_ptr()), 4, vp(sc.data_ptr()),
+    assert _abi.lib().kivi_prefill_attn(c64._h, vp(q4.data_ptr()), vp(q4.data_ptr()), 4, vp(sc.data_ptr()),
                                         sc.numel(), None) == _abi.KIVI_EINVAL

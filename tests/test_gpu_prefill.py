@@ -48,6 +48,9 @@ CASES = [
     # GQA rep 3: a pass of four rows spans two query tokens; 8-bit, no sinks
     (dict(bits=8, group=32, residual=32, sinks=0, h_q=6, h_kv=2, head_dim=128, batch=2, max_tokens=400),
      [7, 64, 50, 90]),
+    # 5 bits (bit-stream packing) at head dim 128, GQA rep 4
+    (dict(bits=5, group=32, residual=64, sinks=2, h_q=8, h_kv=2, head_dim=128, batch=2, max_tokens=400),
+     [9, 70, 33]),
     # sliding window, ring of group slots wrapping; the 150-token chunk loses
     # the evicted start of its first queries' windows
     (dict(bits=4, group=16, residual=32, sinks=2, h_q=8, h_kv=2, head_dim=128, batch=2, max_tokens=0, window=48),
