@@ -58,10 +58,12 @@ typedef enum kivi_status {
 
 /* Cache parameters.
  *   bits       b in 1..8: code width (tract #2329: configurable width;
- *              kvquant++ README: 3 bits recommended).  b in {2, 4, 8} decode
- *              on tensor cores; the other widths pack as a bit stream and
- *              decode on CUDA cores, need G in {32, 64} and have no
- *              multi-query (prefill) attention.
+ *              kvquant++ README: 3 bits recommended).  b in {2, 4, 8} pack
+ *              by the word rule below; the other widths pack as a bit
+ *              stream and need G in {32, 64}.  Every width decodes on
+ *              tensor cores at head dim 128; the bit-stream widths at head
+ *              dim 64 decode on CUDA cores and have no multi-query
+ *              (prefill) attention.
  *   group      G: tokens per frozen key group; a multiple of 16 in [16, 256].
  *   residual   R: capacity of the fp16 residual ring; R >= G and R % G == 0.
  *   sinks      S in [0, 1024]: leading tokens kept in fp32.
@@ -263,8 +265,8 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  * oldest part of its first queries' windows).  The newest query's row equals
  * kivi_decode_attn's output for it.  Work: as kivi_decode_attn with n_queries
  * times the query rows per kv head, each row masked to its own positions.
- * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, or b outside
- * {2, 4, 8}), EALIGN, ENOSPC (scratch too small), ECUDA. */
+ * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, or a bit-stream
+ * width at head dim 64), EALIGN, ENOSPC (scratch too small), ECUDA. */
 int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream);
 

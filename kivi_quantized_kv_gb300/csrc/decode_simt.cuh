@@ -1,12 +1,11 @@
 // decode_simt.cuh — split-K decode attention on CUDA cores for the code widths
 // packed as a plain bit stream (b in {1, 3, 5, 6, 7}; tract #2329 makes the
-// width configurable, the kvquant++ README recommends 3 bits).
+// width configurable, the kvquant++ README recommends 3 bits) at head dim 64.
 //
-// The tensor-core kernel (decode_mma.cuh) turns codes into MMA operands with
-// one AND per code pair, which needs the word-rule packing of b in {2, 4, 8}
-// (both codes of a pair at the same bit of the two halves of a word).  A bit
-// stream puts codes at arbitrary bit offsets, so this kernel dequantizes on
-// CUDA cores instead, in fp32:
+// The tensor-core kernel (decode_mma.cuh) reads a lane's quarter of a key
+// row as whole 32-bit words; at head dim 64 a quarter of a bit-stream row is
+// 16 b bits, which does not start on a word for odd b.  These shapes
+// dequantize on CUDA cores instead, each lane owning whole rows, in fp32:
 //   s_t = Σ_c (q_c Δ_c) code_tc + Σ_c q_c min_c      (keys, per channel)
 //   o_c = Σ_t (p_t Δ_t) code_ct + Σ_t p_t min_t      (values, per token)
 // with the same online softmax (log2 units) and split-K merge as the
