@@ -33,13 +33,14 @@ class KoParams(ctypes.Structure):
         ("sinks", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("max_tokens", ctypes.c_int64), ("window", ctypes.c_int64),
+        ("outlier_permille", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
 class KoLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "n_slots", "sink_k", "sink_v", "res_k", "res_v", "groups", "block_bytes",
-        "blk_kq", "blk_ks", "blk_vq", "blk_vs", "unit_bytes", "cache_bytes")]
+        "blk_kq", "blk_ks", "blk_vq", "blk_vs", "blk_ko", "blk_vo", "n_outliers", "unit_bytes", "cache_bytes")]
 
 
 def lib():
@@ -156,10 +157,11 @@ class Params:
     batch: int
     max_tokens: int = 0
     window: int = 0
+    outlier_permille: int = 0
 
     def c(self) -> KoParams:
         return KoParams(self.bits, self.group, self.residual, self.sinks, self.h_q, self.h_kv,
-                        self.head_dim, self.batch, self.max_tokens, self.window)
+                        self.head_dim, self.batch, self.max_tokens, self.window, self.outlier_permille, 0)
 
 
 def validate(p: Params) -> int:

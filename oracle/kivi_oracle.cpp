@@ -107,15 +107,20 @@ float f16_to_f32(uint16_t h) {
 //   * when the stored Δ is zero (a constant vector) every code is 0.
 // The zero point is the fp16 min itself (exact, because min is an fp16 value).
 // ---------------------------------------------------------------------------
+// skip (may be null): elements kept exactly in an outlier table; they take
+// no part in min and max and get code 0.  A vector whose every element is
+// skipped gets min = 0, Δ = 0.
 void quantize(const uint16_t* x, int n, int64_t stride, int bits, uint8_t* codes,
-              uint16_t* d16_out, uint16_t* mn16_out) {
+              uint16_t* d16_out, uint16_t* mn16_out, const uint8_t* skip = nullptr) {
   float mn = std::numeric_limits<float>::infinity();
   float mx = -std::numeric_limits<float>::infinity();
   for (int i = 0; i < n; ++i) {
+    if (skip && skip[i * stride]) continue;
     const float v = f16_to_f32(x[i * stride]);
     if (v < mn) mn = v;
     if (v > mx) mx = v;
   }
+  if (mn > mx) { mn = 0.0f; mx = 0.0f; }   // every element is an outlier
   mn = mn + 0.0f;
   mx = mx + 0.0f;
   const int top = (1 << bits) - 1;
@@ -124,7 +129,7 @@ void quantize(const uint16_t* x, int n, int64_t stride, int bits, uint8_t* codes
   const float dq = f16_to_f32(d16);
   for (int i = 0; i < n; ++i) {
     int code = 0;
-    if (dq != 0.0f) {
+    if (dq != 0.0f && !(skip && skip[i * stride])) {
       const float v = f16_to_f32(x[i * stride]);
       const float t = (v - mn) / dq;
       const float r = std::nearbyint(t);          // default mode: nearest, ties to even
@@ -220,6 +225,7 @@ int validate(const ko_params& p) {
   if (p.batch < 1) return kInvalid;
   if (p.window < 0 || p.max_tokens < 0) return kInvalid;
   if (p.window > 0 && p.window < p.residual) return kInvalid;
+  if (p.outlier_permille < 0 || p.outlier_permille > 50) return kInvalid;
   return kOk;
 }
 
@@ -259,7 +265,15 @@ ko_layout layout_of(const ko_params& p) {
   L.blk_ks = L.blk_kq + G * d * b / 8;
   L.blk_vq = L.blk_ks + 2 * d * 2;
   L.blk_vs = L.blk_vq + d * G * b / 8;
-  L.block_bytes = L.blk_vs + G * 2 * 2;
+  // dense-and-sparse outliers (pigeon guide, "KVQuant adds": a small share
+  // of the values, around one in a hundred, kept in fp16 beside the codes):
+  // per block a key table and a value table of n_outliers 4-byte entries,
+  // each padded to 16 bytes
+  L.n_outliers = (static_cast<int64_t>(p.outlier_permille) * G * d + 999) / 1000;
+  const int64_t table = (4 * L.n_outliers + 15) / 16 * 16;
+  L.blk_ko = L.blk_vs + G * 2 * 2;
+  L.blk_vo = L.blk_ko + table;
+  L.block_bytes = L.blk_vo + table;
   L.unit_bytes = L.groups + L.n_slots * L.block_bytes;
   L.cache_bytes = static_cast<int64_t>(p.batch) * p.h_kv * L.unit_bytes;
   return L;
@@ -294,6 +308,31 @@ const uint8_t* unit_ptr(const ko_cache& c, int64_t b, int64_t h) {
   return c.arena.data() + (b * c.p.h_kv + h) * c.L.unit_bytes;
 }
 
+// The n largest |x| of x[0..len) (fp16; magnitude order is the order of the
+// bit patterns without the sign), ties to the smaller index, flagged in skip.
+void select_outliers(const uint16_t* x, int len, int64_t n, uint8_t* skip) {
+  if (n <= 0) return;
+  std::vector<int> idx(len);
+  for (int i = 0; i < len; ++i) idx[i] = i;
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return (x[a] & 0x7FFF) > (x[b] & 0x7FFF); });
+  for (int64_t k = 0; k < n && k < len; ++k) skip[idx[k]] = 1;
+}
+
+// The flagged values of a [G][d] block as {u8 t, u8 ch, fp16 x} entries in
+// flat-index (t d + ch) order.
+void write_table(const uint16_t* x, const uint8_t* skip, int G, int d, uint8_t* out) {
+  int64_t e = 0;
+  for (int t = 0; t < G; ++t) {
+    for (int ch = 0; ch < d; ++ch) {
+      if (!skip[t * d + ch]) continue;
+      out[4 * e] = static_cast<uint8_t>(t);
+      out[4 * e + 1] = static_cast<uint8_t>(ch);
+      put_u16(out + 4 * e + 2, x[t * d + ch]);
+      ++e;
+    }
+  }
+}
+
 // Flush: the ring's oldest G tokens (absolute positions a0 .. a0+G-1) become
 // frozen group g.  Keys: one (Δ, min) per channel over the G tokens; values:
 // one (Δ, min) per token over the d channels.
@@ -312,12 +351,21 @@ void flush_group(ko_cache& c, uint8_t* unit, int64_t g) {
       vx[t * d + ch] = get_u16(unit + c.L.res_v + (ring_slot * d + ch) * 2);
     }
   }
+  // outliers (dense-and-sparse): per block the n_outliers values of largest
+  // magnitude, ties to the smaller flat index t d + ch, stored exactly in
+  // index order and left out of the dense quantization
+  const int64_t no = c.L.n_outliers;
+  std::vector<uint8_t> kskip(static_cast<size_t>(G) * d, 0), vskip(static_cast<size_t>(G) * d, 0);
+  select_outliers(kx.data(), G * d, no, kskip.data());
+  select_outliers(vx.data(), G * d, no, vskip.data());
+  write_table(kx.data(), kskip.data(), G, d, blk + c.L.blk_ko);
+  write_table(vx.data(), vskip.data(), G, d, blk + c.L.blk_vo);
   // keys, per channel over the group's tokens
   std::vector<uint8_t> kcodes(static_cast<size_t>(G) * d);
   std::vector<uint8_t> col(G);
   for (int ch = 0; ch < d; ++ch) {
     uint16_t d16, mn16;
-    quantize(&kx[ch], G, d, b, col.data(), &d16, &mn16);
+    quantize(&kx[ch], G, d, b, col.data(), &d16, &mn16, no ? &kskip[ch] : nullptr);
     for (int t = 0; t < G; ++t) kcodes[t * d + ch] = col[t];
     put_u16(blk + c.L.blk_ks + ch * 2, d16);
     put_u16(blk + c.L.blk_ks + (d + ch) * 2, mn16);
@@ -328,7 +376,7 @@ void flush_group(ko_cache& c, uint8_t* unit, int64_t g) {
   std::vector<uint8_t> vcodes(static_cast<size_t>(G) * d);
   for (int t = 0; t < G; ++t) {
     uint16_t d16, mn16;
-    quantize(&vx[t * d], d, 1, b, &vcodes[t * d], &d16, &mn16);
+    quantize(&vx[t * d], d, 1, b, &vcodes[t * d], &d16, &mn16, no ? &vskip[t * d] : nullptr);
     put_u16(blk + c.L.blk_vs + (t * 2 + 0) * 2, d16);
     put_u16(blk + c.L.blk_vs + (t * 2 + 1) * 2, mn16);
   }
@@ -378,6 +426,13 @@ void dequant_resident(const ko_cache& c, int64_t b_idx, int64_t h, double* K, do
       for (int ch = 0; ch < d; ++ch) {
         unpack_row(blk + c.L.blk_vq + static_cast<int64_t>(ch) * G * b / 8, G, b, row.data());
         vr[ch] = vmn + static_cast<double>(row[t]) * vdq;
+      }
+      // outliers are exact (dense-and-sparse)
+      for (int64_t e = 0; e < c.L.n_outliers; ++e) {
+        const uint8_t* ke = blk + c.L.blk_ko + 4 * e;
+        if (ke[0] == t) kr[ke[1]] = f16_to_f32(get_u16(ke + 2));
+        const uint8_t* ve = blk + c.L.blk_vo + 4 * e;
+        if (ve[0] == t) vr[ve[1]] = f16_to_f32(get_u16(ve + 2));
       }
     } else {   // residual ring, fp16
       const int64_t ring_slot = (a - S) % R;
@@ -613,7 +668,9 @@ int ko_prefill_attn(const ko_cache* c, const uint16_t* q, int64_t n_queries, dou
 // Bytes a decode pass must move, per unit: packed codes of the visible
 // quantized tokens (keys and values), the key (Δ, min) rows of every group
 // touched, the value (Δ, min) of every visible quantized token, the fp16
-// residual keys and values, the fp32 sinks; plus q and out (fp16) per head.
+// residual keys and values, the fp32 sinks, the key and value outlier tables
+// (n_outliers 4-byte entries each) of every group touched; plus q and out
+// (fp16) per head.
 int64_t ko_decode_bytes(const ko_cache* c) {
   const ko_params& p = c->p;
   const int64_t d = p.head_dim, G = p.group, b = p.bits, S = p.sinks, T = c->T;
@@ -626,7 +683,8 @@ int64_t ko_decode_bytes(const ko_cache* c) {
     if (vis > 0) { tq += vis; touched += 1; }
   }
   const int64_t ns = std::min(T, S);
-  const int64_t per_unit = 2 * tq * d * b / 8 + 4 * d * touched + 4 * tq + 4 * d * c->n_res + 8 * d * ns;
+  const int64_t per_unit = 2 * tq * d * b / 8 + 4 * d * touched + 4 * tq + 4 * d * c->n_res + 8 * d * ns +
+                          8 * c->L.n_outliers * touched;
   return per_unit * p.batch * p.h_kv + 4 * d * static_cast<int64_t>(p.batch) * p.h_q;
 }
 

@@ -44,6 +44,10 @@ typedef struct ko_params {
   int32_t batch;     /* B */
   int64_t max_tokens;/* capacity T_max when window == 0 */
   int64_t window;    /* W: 0 = attend to everything; > 0 = sinks + last W tokens */
+  int32_t outlier_permille; /* dense-and-sparse: per frozen key block and value
+                               block, ceil(permille * G * d / 1000) values kept
+                               exactly in a side table; 0 = none */
+  int32_t reserved;
 } ko_params;
 
 /* Byte layout of one (batch, kv-head) unit and of one frozen group block. */
@@ -54,6 +58,9 @@ typedef struct ko_layout {
   int64_t groups;         /* first group block */
   int64_t block_bytes;    /* one group block */
   int64_t blk_kq, blk_ks, blk_vq, blk_vs; /* offsets inside a block */
+  int64_t blk_ko, blk_vo; /* key and value outlier tables: n_outliers entries
+                             of {u8 token, u8 channel, fp16 value} each */
+  int64_t n_outliers;     /* entries per table (0 without outliers) */
   int64_t unit_bytes;     /* one (b, h_kv) unit */
   int64_t cache_bytes;    /* B * H_kv * unit_bytes */
 } ko_layout;
