@@ -234,7 +234,10 @@ def decode_bytes_at(w, T, n_slots):
             tq += vis
             touched += 1
     d = w.head_dim
-    per_unit = 2 * tq * d * w.bits // 8 + 4 * d * touched + 4 * tq + 4 * d * n_res + 8 * d * n_sink
+    n_out = -(-getattr(w, "outlier_permille", 0) * w.group * d // 1000)   # outlier table entries
+    tables = 2 * (2 * (w.group + 1) + 4 * n_out) if n_out else 0          # row pointers + entries, K and V
+    per_unit = (2 * tq * d * w.bits // 8 + 4 * d * touched + 4 * tq + 4 * d * n_res + 8 * d * n_sink +
+                tables * touched)
     return per_unit * w.batch * w.h_kv + 4 * d * w.batch * w.h_q
 
 
@@ -257,7 +260,10 @@ def prefill_bytes_at(w, T, m, n_slots):
             tq += vis
             touched += 1
     d = w.head_dim
-    per_unit = 2 * tq * d * w.bits // 8 + 4 * d * touched + 4 * tq + 4 * d * n_res + 8 * d * n_sink
+    n_out = -(-getattr(w, "outlier_permille", 0) * w.group * d // 1000)   # outlier table entries
+    tables = 2 * (2 * (w.group + 1) + 4 * n_out) if n_out else 0          # row pointers + entries, K and V
+    per_unit = (2 * tq * d * w.bits // 8 + 4 * d * touched + 4 * tq + 4 * d * n_res + 8 * d * n_sink +
+                tables * touched)
     return per_unit * w.batch * w.h_kv + 4 * d * w.batch * m * w.h_q
 
 
@@ -650,7 +656,7 @@ def oracle_sample(w, units_max, seed=0, extra=4096):
     ws = w.with_(batch=bs, h_kv=hk, h_q=hk * rep)
     p = oracle.Params(bits=w.bits, group=w.group, residual=w.residual, sinks=w.sinks, h_q=ws.h_q, h_kv=ws.h_kv,
                       head_dim=w.head_dim, batch=ws.batch, max_tokens=0 if w.window else w.tokens + extra,
-                      window=w.window)
+                      window=w.window, outlier_permille=w.outlier_permille)
     c = oracle.Cache(p)
     kv = KVStream(ws, device="cpu")
     t = 0
@@ -774,7 +780,8 @@ def main():
 
 DECODE_SOURCES = ("kivi_internal.cuh", "decode_mma.cuh", "decode_launch.cuh", "decode.cu",
                   "decode_b2.cu", "decode_b4.cu", "decode_b8.cu", "decode_simt.cuh", "decode_simt.cu",
-                  "decode_simt_d64.cu", "decode_simt_d128.cu")
+                  "decode_simt_d64.cu", "decode_simt_d128.cu", "decode_outl.cuh", "decode_outl.cu",
+                  "decode_outl_b2.cu", "decode_outl_b3.cu", "decode_outl_b4.cu")
 
 
 def decode_sources_sha():

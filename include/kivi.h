@@ -88,6 +88,14 @@ typedef struct kivi_params {
   int32_t batch;
   int64_t max_tokens;
   int64_t window;
+  int32_t outlier_permille;   /* dense-and-sparse outliers: 0 = none, else
+                                 1..50 per mille of each frozen key block and
+                                 value block kept exactly (see the layout
+                                 below); needs bits 2..4, group a multiple of
+                                 32 and, at 3 bits, head_dim 128.  Decode and
+                                 the fused step add the corrections; the
+                                 multi-query attention refuses such a cache */
+  int32_t reserved;           /* 0 */
 } kivi_params;
 
 /* Byte layout of the arena and current state (all offsets in bytes).
@@ -103,6 +111,17 @@ typedef struct kivi_params {
  *     blk_ks  fp16 key Δ[d] then key min[d] (one pair per channel)
  *     blk_vq  value codes, channel-major: d rows of G*b/8 bytes
  *     blk_vs  fp16 (Δ, min) per token, G pairs
+ *     blk_ko, blk_vo  (outlier_permille > 0) key and value outlier tables,
+ *             rows by token: u16 row pointers [G + 1] (the entries of
+ *             token t are [ptr[t], ptr[t+1])), then from out_entries the
+ *             n_outliers = ceil(outlier_permille * G * d / 1000) entries
+ *             of 4 bytes {u8 token t, u8 channel c, fp16 value}, in
+ *             increasing t * d + c; each table padded to 16 bytes.  The
+ *             outliers of a block are its n_outliers values of largest
+ *             magnitude (ties to the smaller t * d + c); they are left out
+ *             of the dense min and max, take code 0 and read back exactly
+ *             (KV-cache quantization guide (pigeon), "KVQuant adds": a
+ *             small share of values kept in fp16 beside the codes).
  *   b in {2, 4, 8}: a row of codes is cut into little-endian 32-bit words
  *   of 32/b codes; element j of a word sits in the low 16-bit half when j is
  *   even, the high half when j is odd, at bit b*floor(j/2) of its half.
@@ -124,6 +143,9 @@ typedef struct kivi_layout {
   int64_t n_res;      /* tokens live in the ring */
   int32_t max_splits; /* CTAs that may share one unit's work */
   int32_t reserved;
+  int64_t blk_ko, blk_vo;   /* outlier tables inside a block */
+  int64_t n_outliers;       /* entries per table (0 without outliers) */
+  int64_t out_entries;      /* offset of the entries inside a table */
 } kivi_layout;
 
 typedef struct kivi_cache kivi_cache;
@@ -265,8 +287,9 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  * oldest part of its first queries' windows).  The newest query's row equals
  * kivi_decode_attn's output for it.  Work: as kivi_decode_attn with n_queries
  * times the query rows per kv head, each row masked to its own positions.
- * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, or a bit-stream
- * width at head dim 64), EALIGN, ENOSPC (scratch too small), ECUDA. */
+ * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, a bit-stream width
+ * at head dim 64, or a cache with outlier tables), EALIGN, ENOSPC (scratch
+ * too small), ECUDA. */
 int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream);
 
@@ -278,7 +301,7 @@ int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_que
  *           sequence are not read (q) and not written (out).
  *   scratch at least kivi_prefill_scratch_bytes(cache, m_max) bytes.
  * One launch per run of consecutive sequences with equal (length, count).
- * Errors: ENULL, EINVAL, EALIGN, ENOSPC, ECUDA. */
+ * Errors: ENULL, EINVAL (as kivi_prefill_attn), EALIGN, ENOSPC, ECUDA. */
 int kivi_prefill_attn_ragged(kivi_cache* cache, const void* q, void* out, const int64_t* n_queries,
                              int64_t m_max, void* scratch, size_t scratch_bytes, void* cuda_stream);
 

@@ -30,6 +30,7 @@ class KiviParams(ctypes.Structure):
         ("sinks", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("max_tokens", ctypes.c_int64), ("window", ctypes.c_int64),
+        ("outlier_permille", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -38,7 +39,8 @@ class KiviLayout(ctypes.Structure):
         "n_slots", "sink_k", "sink_v", "res_k", "res_v", "groups",
         "block_bytes", "blk_kq", "blk_ks", "blk_vq", "blk_vs",
         "unit_bytes", "cache_bytes", "workspace_offset", "workspace_bytes", "arena_bytes",
-        "tokens", "n_sink", "n_groups", "n_res")] + [("max_splits", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+        "tokens", "n_sink", "n_groups", "n_res")] + [("max_splits", ctypes.c_int32), ("reserved", ctypes.c_int32)] + [
+        (n, ctypes.c_int64) for n in ("blk_ko", "blk_vo", "n_outliers", "out_entries")]
 
 
 class KiviError(RuntimeError):

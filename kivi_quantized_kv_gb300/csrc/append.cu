@@ -15,6 +15,17 @@
 // __float2half_rn; "round" is rintf (half to even).  min and max are
 // canonicalised with + 0.0f so -0 and +0 give the same bytes.
 //
+// Dense-and-sparse outliers (when the cache keeps them; pigeon guide, "KVQuant
+// adds"): before the quantizer, the n_out values of largest magnitude of the
+// key block and of the value block are found by n_out rounds of a block-wide
+// maximum over a unique 32-bit key per element, (|x| bits << 16) | (0xFFFF -
+// flat index), each round taking the largest key below the previous round's
+// (so ties go to the smaller flat index).  They are flagged in a bitmask,
+// left out of the min and max, given code 0, and written to the block's
+// table as rows by token: row pointers (entries of the tokens before t),
+// then the entries in flat-index order (an entry's place is the number of
+// selected indices below its own).
+//
 // write_kernel: widens new sink tokens to fp32 (tract #2458, sink commit) and
 // copies new tokens into the fp16 ring at slot (a - S) mod R (pigeon guide,
 // step 4).  It runs after flush_kernel on the same stream, because a flush can
@@ -28,7 +39,70 @@ constexpr int kFlushThreads = 256;
 
 // Group grp of unit (bb, h): the body of both flush kernels.  Shared memory:
 // keys [G][d] fp16, values [G][d] fp16, key codes [G][d] u8, value codes
-// [G][d] u8.
+// [G][d] u8; with outliers also the key and value flag bitmasks (G d / 32
+// words each), the selected flat indices of keys and values (n_out each) and
+// the round maxima (2 x 8 words).
+size_t flush_smem(const Geo& g) {
+  const size_t gd = static_cast<size_t>(g.G) * g.d;
+  size_t s = gd * (2 * sizeof(__half) + 2);
+  if (g.n_out > 0) s += 2 * (gd / 32) * 4 + 2 * static_cast<size_t>(g.n_out) * 4 + 16 * 4;
+  return s;
+}
+
+// the largest key below prev over the block's n elements of x; every thread
+// gets it (one barrier per call; red alternates between two halves by round)
+__device__ __forceinline__ uint32_t block_next_key(const __half* x, int n, uint32_t prev, uint32_t* red, int round) {
+  uint32_t best = 0u;
+  const unsigned short* xb = reinterpret_cast<const unsigned short*>(x);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t k = (static_cast<uint32_t>(xb[i] & 0x7FFFu) << 16) | (0xFFFFu - static_cast<uint32_t>(i));
+    if (k < prev && k > best) best = k;
+  }
+  best = __reduce_max_sync(0xffffffffu, best);
+  uint32_t* rr = red + 8 * (round & 1);
+  if ((threadIdx.x & 31) == 0) rr[threadIdx.x >> 5] = best;
+  __syncthreads();
+  uint32_t m = 0u;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = rr[w] > m ? rr[w] : m;
+  return m;
+}
+
+// selects the n_out outliers of a [G][d] block x: flags them in f (zeroed
+// here) and writes the table at out: row pointers by token, then from
+// out_ent the entries in flat-index order; sel is scratch for n_out indices.
+// Ends with a barrier: the flags are then visible to all.
+__device__ __forceinline__ void select_outliers(const __half* x, int G, int d, int n_out, int out_ent, uint32_t* f,
+                                                int* sel, uint32_t* red, uint8_t* out) {
+  const int n = G * d;
+  for (int w = threadIdx.x; w < n / 32; w += blockDim.x) f[w] = 0u;
+  uint32_t prev = 0xFFFFFFFFu;
+  for (int r = 0; r < n_out; ++r) {
+    prev = block_next_key(x, n, prev, red, r);
+    if (threadIdx.x == 0) sel[r] = static_cast<int>(0xFFFFu - (prev & 0xFFFFu));
+  }
+  __syncthreads();
+  const unsigned short* xb = reinterpret_cast<const unsigned short*>(x);
+  uint32_t* table = reinterpret_cast<uint32_t*>(out + out_ent);
+  uint16_t* ptr = reinterpret_cast<uint16_t*>(out);
+  for (int t = threadIdx.x; t <= G; t += blockDim.x) {   // entries of the tokens before t
+    int cnt = 0;
+    for (int j = 0; j < n_out; ++j) cnt += sel[j] < t * d ? 1 : 0;
+    ptr[t] = static_cast<uint16_t>(cnt);
+  }
+  for (int e = threadIdx.x; e < n_out; e += blockDim.x) {
+    const int i = sel[e];
+    int rank = 0;
+    for (int j = 0; j < n_out; ++j) rank += sel[j] < i ? 1 : 0;
+    atomicOr(&f[i >> 5], 1u << (i & 31));
+    // {u8 t, u8 c, fp16 x}, little-endian
+    table[rank] = static_cast<uint32_t>(i / d) | (static_cast<uint32_t>(i % d) << 8) |
+                  (static_cast<uint32_t>(xb[i]) << 16);
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ bool flagged(const uint32_t* f, int i) { return (f[i >> 5] >> (i & 31)) & 1u; }
+
 __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ arena,
                                             const __half* __restrict__ k_new, const __half* __restrict__ v_new,
                                             int64_t T_old, int64_t n_stride, int64_t grp, int h, int bb) {
@@ -68,21 +142,34 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
   __half* ks_out = reinterpret_cast<__half*>(blk + g.blk_ks);
   __half* vs_out = reinterpret_cast<__half*>(blk + g.blk_vs);
 
-  // keys: one (Δ, min) per channel over the group's tokens
+  // outliers: flags (bit t d + c) of the key and value blocks
+  const bool outl = g.n_out > 0;
+  uint32_t* kf = reinterpret_cast<uint32_t*>(vc + G * d);
+  uint32_t* vf = kf + G * d / 32;
+  if (outl) {
+    int* sel = reinterpret_cast<int*>(vf + G * d / 32);
+    uint32_t* red = reinterpret_cast<uint32_t*>(sel + g.n_out);
+    select_outliers(kx, G, d, g.n_out, g.out_ent, kf, sel, red, blk + g.blk_ko);
+    select_outliers(vx, G, d, g.n_out, g.out_ent, vf, sel, red, blk + g.blk_vo);
+  }
+
+  // keys: one (Δ, min) per channel over the group's tokens (its dense values)
   for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float mn = __half2float(kx[c]), mx = mn;
-    for (int t = 1; t < G; ++t) {
+    float mn = INFINITY, mx = -INFINITY;
+    for (int t = 0; t < G; ++t) {
+      if (outl && flagged(kf, t * d + c)) continue;
       const float v = __half2float(kx[t * d + c]);
       mn = fminf(mn, v);
       mx = fmaxf(mx, v);
     }
+    if (mn > mx) { mn = 0.0f; mx = 0.0f; }   // every value an outlier
     mn = __fadd_rn(mn, 0.0f);
     mx = __fadd_rn(mx, 0.0f);
     const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), top));
     const float dq = __half2float(d16);
     for (int t = 0; t < G; ++t) {
       int code = 0;
-      if (dq != 0.0f) {
+      if (dq != 0.0f && !(outl && flagged(kf, t * d + c))) {
         const float r = rintf(__fdiv_rn(__fsub_rn(__half2float(kx[t * d + c]), mn), dq));
         code = static_cast<int>(fminf(fmaxf(r, 0.0f), top));
       }
@@ -95,8 +182,9 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
   // values: one (Δ, min) per token over the channels; one warp per token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   for (int t = warp; t < G; t += nwarps) {
-    float mn = __half2float(vx[t * d + lane]), mx = mn;
-    for (int c = lane + 32; c < d; c += 32) {
+    float mn = INFINITY, mx = -INFINITY;
+    for (int c = lane; c < d; c += 32) {
+      if (outl && flagged(vf, t * d + c)) continue;
       const float v = __half2float(vx[t * d + c]);
       mn = fminf(mn, v);
       mx = fmaxf(mx, v);
@@ -106,13 +194,14 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
+    if (mn > mx) { mn = 0.0f; mx = 0.0f; }
     mn = __fadd_rn(mn, 0.0f);
     mx = __fadd_rn(mx, 0.0f);
     const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), top));
     const float dq = __half2float(d16);
     for (int c = lane; c < d; c += 32) {
       int code = 0;
-      if (dq != 0.0f) {
+      if (dq != 0.0f && !(outl && flagged(vf, t * d + c))) {
         const float r = rintf(__fdiv_rn(__fsub_rn(__half2float(vx[t * d + c]), mn), dq));
         code = static_cast<int>(fminf(fmaxf(r, 0.0f), top));
       }
@@ -241,7 +330,7 @@ cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, cons
                          int64_t T_old, int64_t n_stride, int64_t g_begin, int64_t g_end,
                          cudaStream_t stream) {
   if (g_end <= g_begin) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(g.G) * g.d * (2 * sizeof(__half) + 2);
+  const size_t smem = flush_smem(g);
   cudaError_t e = cudaFuncSetAttribute(flush_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -262,7 +351,7 @@ cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, cons
 
 cudaError_t launch_flush_ragged(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
                                 const RunTable& runs, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(g.G) * g.d * (2 * sizeof(__half) + 2);
+  const size_t smem = flush_smem(g);
   cudaError_t e = cudaFuncSetAttribute(flush_ragged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -10,13 +10,13 @@ namespace kivi {
 namespace mma {
 
 // the kernel of an instantiation
-template <int D, int BITS, int CH, bool MQ, bool RG>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
 constexpr auto kernel_of() {
-  if constexpr (RG) return decode_mma_ragged_kernel<D, BITS, CH, MQ>;
-  else return decode_mma_kernel<D, BITS, CH, MQ, false>;
+  if constexpr (RG) return decode_mma_ragged_kernel<D, BITS, CH, MQ, OUTL>;
+  else return decode_mma_kernel<D, BITS, CH, MQ, false, OUTL>;
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
 cudaError_t prepare() {
   // opt in to the largest dynamic shared memory once per instantiation
   static std::atomic<int> done{0};
@@ -27,18 +27,18 @@ cudaError_t prepare() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, kernel_of<D, BITS, CH, MQ, RG>());
+  e = cudaFuncGetAttributes(&fa, kernel_of<D, BITS, CH, MQ, RG, OUTL>());
   if (e != cudaSuccess) return e;
   // the opt-in limit covers static + dynamic shared memory
-  e = cudaFuncSetAttribute(kernel_of<D, BITS, CH, MQ, RG>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(kernel_of<D, BITS, CH, MQ, RG, OUTL>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            optin - static_cast<int>(fa.sharedSizeBytes));
   if (e == cudaSuccess) done.store(1, std::memory_order_release);
   return e;
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
 cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
-  cudaError_t e = prepare<D, BITS, CH, MQ, RG>();
+  cudaError_t e = prepare<D, BITS, CH, MQ, RG, OUTL>();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the CTAs may start (and set up their
   // shared memory) while the previous kernel in the stream drains; the kernel
@@ -53,17 +53,17 @@ cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int th
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if constexpr (RG) e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG>(), a, rt);
-  else e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG>(), a);
+  if constexpr (RG) e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL>(), a, rt);
+  else e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL>(), a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
 int occupancy_one(int threads, int smem) {
-  if (prepare<D, BITS, CH, MQ, RG>() != cudaSuccess) return 1;
+  if (prepare<D, BITS, CH, MQ, RG, OUTL>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_of<D, BITS, CH, MQ, RG>(), threads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_of<D, BITS, CH, MQ, RG, OUTL>(), threads, smem) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
@@ -137,6 +137,12 @@ cudaError_t launch_rg_stream_b(int bits, const Args& a, const RunTable& rt, dim3
                                cudaStream_t s);
 int occupancy_stream_b(int bits, const Geo& g, int threads, int smem);
 int occupancy_b2(const Geo& g, int threads, int smem);
+// with outlier tables (decode_outl.cu): 2 to 4 bits, 32-token chunks, one
+// query token per sequence
+cudaError_t launch_outl_b(int bits, const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_rg_outl_b(int bits, const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
+                             cudaStream_t s);
+int occupancy_outl_b(int bits, const Geo& g, int threads, int smem);
 int occupancy_b4(const Geo& g, int threads, int smem);
 int occupancy_b8(const Geo& g, int threads, int smem);
 

@@ -54,6 +54,21 @@
 // Tails go through the same tensor-core path: the fp16 ring rows are A
 // operands as they are (values transposed by ldmatrix), and the fp32 sink
 // rows are narrowed to fp16 exactly (they were fp16 when appended).
+//
+// Outlier tables (the OUTL instantiations; KV-cache quantization guide
+// (pigeon), "KVQuant adds": a small share of values kept in fp16 beside the
+// codes).  An outlier's code is 0, so the dense path above reads it as the
+// min of its vector; the kernel adds the difference.  The tables travel
+// with the block in the same bulk copy.  Keys: a score lane walks the
+// table's rows of its own TPL tokens and adds q_c (x - min_c) scaled to log2
+// units; key outliers sit in fixed channels and spread over the tokens, so
+// this takes no barrier and no atomic.  Values: outliers bunch in the few
+// tokens of large scale, so the lanes take the chunk's entries in turn
+// (entry-parallel) and add p_h,t (x - min_t) for the four heads into a
+// per-warp fp32 [4][D] buffer with shared atomics; p comes from the score
+// lanes through a per-warp [4][CH] exchange.  The buffer is at the running
+// max: its owner lanes (the lane that holds that output channel) rescale it
+// with the accumulators and add it to their output at the close of a unit.
 #pragma once
 
 #include "kivi_internal.cuh"
@@ -589,10 +604,13 @@ using RunTableT = typename std::conditional<RG, RunTable, NoRuns>::type;
 
 // The kernel body.  RG: a ragged launch; per-unit plan values come from the
 // run table `rt` (the unit's run) instead of the launch's plan.
-template <int D, int BITS, int CH, bool MQ, bool RG>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL>
 __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& rt) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   using WS = WarpSmem<D, CH>;
+  // outlier corrections (OUTL): per warp a [4][CH] fp32 exchange of the
+  // chunk's p and the [4][D] fp32 value corrections
+  constexpr int kCorr = OUTL ? 16 * (CH + D) : 0;
   constexpr int RK = D * BITS / 8;          // key row bytes
   constexpr int KW = RK / 16;               // 32-bit words of a lane's key quarter
   constexpr int QD = D / 4;                 // channels of a lane's quarter
@@ -654,7 +672,8 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   uint8_t* q_all = stages + static_cast<size_t>(nw) * a.ns * a.stage_bytes;
   float* slots = reinterpret_cast<float*>(q_all + nw * WS::kQ);
   uint8_t* xch_all = reinterpret_cast<uint8_t*>(slots) + nw * WS::kSlot;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xch_all + nw * WS::kXch);
+  float* corr_all = reinterpret_cast<float*>(xch_all + nw * WS::kXch);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(corr_all) + nw * kCorr);
   __shared__ unsigned s_arrive;   // warps signed in for the current combine
   __shared__ unsigned s_done;     // combines completed
   __shared__ unsigned s_flag;     // this CTA merges its last unit
@@ -663,6 +682,8 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   uint8_t* my_stages = stages + static_cast<size_t>(warp) * a.ns * a.stage_bytes;
   uint8_t* qw = q_all + warp * WS::kQ;
   uint8_t* xw = xch_all + warp * WS::kXch;
+  float* pbuf = corr_all + warp * (kCorr / 4);   // [4][CH]: p of (head, token) of the open chunk
+  float* ocorr = pbuf + 4 * CH;                  // [4][D], real scale, at the running max
   const uint32_t xw_s = smem_addr(xw);
   const uint32_t bar0 = smem_addr(bars + warp * a.ns);
   int* ring_w = reinterpret_cast<int*>(bars + nw * a.ns) + warp * a.ns;   // this warp's item ring
@@ -904,6 +925,15 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   for (int i = 0; i < NCT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
   const uint8_t* qlane = qw + hh_col * WS::kQRow + c * WS::kQS;
   const uint32_t q_s = smem_addr(qlane);
+  // q of row hh, channel ch from the q area (16-byte chunks of 4 pairs, stored
+  // in pair order 0, 2, 1, 3; quarters padded)
+  auto q_at = [&](int hh, int ch) -> float {
+    const int idx = ch >> 3, w = (ch >> 1) & 3;
+    const int slot = (w == 1) ? 2 : (w == 2) ? 1 : w;
+    const __half* p = reinterpret_cast<const __half*>(qw + hh * WS::kQRow + (idx / (QD / 8)) * WS::kQS +
+                                                      (idx % (QD / 8)) * 16 + slot * 4);
+    return __half2float(p[ch & 1]);
+  };
 
   // token masks, needed with a window or with several query tokens: this
   // lane's score column c is query row 4 pass + c of the open unit, i.e.
@@ -930,6 +960,16 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
     o_real = false;
 #pragma unroll
     for (int i = 0; i < NCT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    if constexpr (OUTL) {   // this lane's entries: head c, channels 16 ct + r (+ 8)
+#pragma unroll
+      for (int ct = 0; ct < NCT; ++ct) { ocorr[c * D + 16 * ct + r] = 0.f; ocorr[c * D + 16 * ct + r + 8] = 0.f; }
+    }
+  };
+  auto rescale_corr = [&](float corr) {
+    if constexpr (OUTL) {
+#pragma unroll
+      for (int ct = 0; ct < NCT; ++ct) { ocorr[c * D + 16 * ct + r] *= corr; ocorr[c * D + 16 * ct + r + 8] *= corr; }
+    }
   };
   // the warp's state of unit cu into its slot, then the sign-in: the last warp
   // combines a unit that is not the CTA's last while the others stream on; the
@@ -959,6 +999,10 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
       for (int ct = 0; ct < NCT; ++ct) {
         so[16 * ct + r] = fmaf(oacc[ct][0] + oacc[ct][1], osc, mh);
         so[16 * ct + r + 8] = fmaf(oacc[ct][2] + oacc[ct][3], osc, mh);
+        if constexpr (OUTL) {
+          so[16 * ct + r] += ocorr[c * D + 16 * ct + r];
+          so[16 * ct + r + 8] += ocorr[c * D + 16 * ct + r + 8];
+        }
       }
     }
     if (cu != nunits - 1) {
@@ -1103,6 +1147,28 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
           sv[2 * v2] = sw ? s_b : s_a;
           sv[2 * v2 + 1] = sw ? s_a : s_b;
         }
+        if constexpr (OUTL) {
+          // key outliers of the lane's tokens (rows s0 + TPL r .. of the
+          // table): score += q_c (x - min_c) for an entry (t, c, x), whose
+          // dense part dequantized to min_c (code 0).  Key outliers sit in
+          // fixed channels, so they spread over the tokens and the lanes;
+          // this takes no barrier and no atomic
+          const uint8_t* stg = my_stages + c_st * a.stage_bytes;
+          const uint16_t* kp = reinterpret_cast<const uint16_t*>(stg + g.blk_ko);
+          const uint32_t* ke = reinterpret_cast<const uint32_t*>(stg + g.blk_ko + g.out_ent);
+          const __half* kmin = reinterpret_cast<const __half*>(stg + g.blk_ks) + D;
+          const int t_lo = s0 + TPL * r;
+          const int e1 = kp[t_lo + TPL];
+          for (int e = kp[t_lo]; e < e1; ++e) {
+            const uint32_t ent = ke[e];
+            const int i = static_cast<int>(ent & 0xFFu) - t_lo;
+            const int ch = static_cast<int>((ent >> 8) & 0xFFu);
+            const float ds = (__half2float(__ushort_as_half(static_cast<unsigned short>(ent >> 16))) -
+                              __half2float(kmin[ch])) * (qscale * q_at(c, ch));
+#pragma unroll
+            for (int j = 0; j < TPL; ++j) sv[j] += (j == i) ? ds : 0.f;
+          }
+        }
         if (masked()) {   // tokens outside [lo, hi] are invisible to column c
           const int64_t hi = col_hi(), lo = col_lo(hi);
 #pragma unroll
@@ -1126,6 +1192,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
             res_mn *= corr;
 #pragma unroll
             for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
+            rescale_corr(corr);
           }
         }
         const float mref = (res_m == -INFINITY) ? 0.f : res_m;   // every score so far -inf: p = 0
@@ -1152,6 +1219,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
             res_l += p;
             res_mn = fmaf(p, dm[2 * i + 1], res_mn);
             pd[i] = p * dm[2 * i] * vscl[i];
+            if constexpr (OUTL) pbuf[c * CH + TPL * r + i] = p;
           }
         }
         // (5) P' hi/lo into the exchange buffer (head c, tokens TPL*r ..)
@@ -1174,6 +1242,27 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
           }
         }
         __syncwarp();
+        if constexpr (OUTL) {
+          // value outliers of the chunk, spread over the lanes by entry (they
+          // bunch in the few tokens of large scale): o_h += p_h,t (x - min_t)
+          // for an entry (t, c, x), whose dense part dequantized to the
+          // token's min.  The owners rescaled their entries and wrote p
+          // before the barrier above.
+          const uint8_t* stg = my_stages + c_st * a.stage_bytes;
+          const uint16_t* vp = reinterpret_cast<const uint16_t*>(stg + g.blk_vo);
+          const uint32_t* ve = reinterpret_cast<const uint32_t*>(stg + g.blk_vo + g.out_ent);
+          const __half* vdm = reinterpret_cast<const __half*>(stg + g.blk_vs);
+          const int e1 = vp[s0 + CH];
+          for (int e = vp[s0] + lane; e < e1; e += 32) {
+            const uint32_t ent = ve[e];
+            const int t = static_cast<int>(ent & 0xFFu);
+            const int ch = static_cast<int>((ent >> 8) & 0xFFu);
+            const float dx = __half2float(__ushort_as_half(static_cast<unsigned short>(ent >> 16))) -
+                             __half2float(vdm[2 * t + 1]);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) atomicAdd(&ocorr[hh * D + ch], pbuf[hh * CH + t - s0] * dx);
+          }
+        }
         // (6) Oᵀ += Vᵀ P': B = P' of tokens c*CH/4 + 4kcn + {0,1 | 2,3} in column r
         uint32_t bp[NKT][2];
         if constexpr (NKT == 2) {
@@ -1275,6 +1364,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         res_mn *= corr;
 #pragma unroll
         for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
+        rescale_corr(corr);
       }
       const float p = (MQ && s == -INFINITY) ? 0.f : ex2(s - res_m);
       res_l += p;
@@ -1352,17 +1442,17 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
 }
 
 // Uniform launches: the plan is the launch's own (one kernel parameter).
-template <int D, int BITS, int CH, bool MQ, bool RG>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mma_kernel(const Args a) {
   const NoRuns none{0};
-  decode_body<D, BITS, CH, MQ, false>(a, none);
+  decode_body<D, BITS, CH, MQ, false, OUTL>(a, none);
 }
 
 // Ragged launches: the runs' plans travel as a grid constant.
-template <int D, int BITS, int CH, bool MQ>
+template <int D, int BITS, int CH, bool MQ, bool OUTL = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     decode_mma_ragged_kernel(const Args a, const __grid_constant__ RunTable rt) {
-  decode_body<D, BITS, CH, MQ, true>(a, rt);
+  decode_body<D, BITS, CH, MQ, true, OUTL>(a, rt);
 }
 
 }  // namespace mma

@@ -64,6 +64,12 @@ int validate(const kivi_params* p) {
   if (static_cast<int64_t>(p->h_kv) * ((p->h_q / p->h_kv + 3) / 4) > 65535) return KIVI_EINVAL;
   if (p->window < 0 || p->max_tokens < 0) return KIVI_EINVAL;
   if (p->window > 0 && p->window < p->residual) return KIVI_EINVAL;
+  if (p->outlier_permille < 0 || p->outlier_permille > 50 || p->reserved != 0) return KIVI_EINVAL;
+  // the outlier corrections are built into the tensor-core decode at 2 to 4
+  // bits (3 at head dim 128) with 32-token chunks
+  if (p->outlier_permille > 0 &&
+      (p->bits < 2 || p->bits > 4 || p->group % 32 != 0 || (p->bits == 3 && p->head_dim != 128)))
+    return KIVI_EINVAL;
   return KIVI_OK;
 }
 
@@ -97,7 +103,12 @@ Geo geometry(const kivi_params& p) {
   g.blk_ks = g.blk_kq + G * d * b / 8;
   g.blk_vq = g.blk_ks + 2 * d * 2;
   g.blk_vs = g.blk_vq + d * G * b / 8;
-  g.block_bytes = g.blk_vs + G * 2 * 2;
+  g.n_out = static_cast<int32_t>((static_cast<int64_t>(p.outlier_permille) * G * d + 999) / 1000);
+  g.out_ent = g.n_out ? static_cast<int32_t>(((G + 1) * 2 + 3) / 4 * 4) : 0;
+  const int64_t table = g.n_out ? (g.out_ent + 4 * static_cast<int64_t>(g.n_out) + 15) / 16 * 16 : 0;
+  g.blk_ko = g.blk_vs + G * 2 * 2;
+  g.blk_vo = g.blk_ko + table;
+  g.block_bytes = g.blk_vo + table;
   g.unit_bytes = g.groups + g.n_slots * g.block_bytes;
   g.cache_bytes = static_cast<int64_t>(p.batch) * p.h_kv * g.unit_bytes;
   g.max_splits = max_splits_for(p);
@@ -629,6 +640,7 @@ int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
   L.n_slots = g.n_slots;
   L.sink_k = g.sink_k; L.sink_v = g.sink_v; L.res_k = g.res_k; L.res_v = g.res_v; L.groups = g.groups;
   L.block_bytes = g.block_bytes; L.blk_kq = g.blk_kq; L.blk_ks = g.blk_ks; L.blk_vq = g.blk_vq; L.blk_vs = g.blk_vs;
+  L.blk_ko = g.blk_ko; L.blk_vo = g.blk_vo; L.n_outliers = g.n_out; L.out_entries = g.out_ent;
   L.unit_bytes = g.unit_bytes; L.cache_bytes = g.cache_bytes;
   L.workspace_offset = g.ws_partials;
   L.arena_bytes = arena_bytes_of(g);
@@ -657,7 +669,8 @@ int64_t attn_bytes(const kivi_cache& c, const Run& r, int64_t nq) {
     if (vis > 0) { tq += vis; touched += 1; }
   }
   const int64_t per_unit = 2 * tq * d * g.bits / 8 + 4 * d * touched + 4 * tq + 4 * d * pl.st.n_res +
-                           8 * d * pl.st.n_sink;
+                           8 * d * pl.st.n_sink +
+                           (g.n_out ? 2 * (2 * (g.G + 1) + 4 * static_cast<int64_t>(g.n_out)) * touched : 0);
   return per_unit * r.nb * g.hkv + 4 * d * static_cast<int64_t>(r.nb) * nq * g.hq;
 }
 
@@ -721,7 +734,8 @@ size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
 int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch) return KIVI_ENULL;
-  if (simt_path(c->g)) return KIVI_EINVAL;   // multi-query attention: the tensor-core path
+  // multi-query attention: the tensor-core path, without outlier tables
+  if (simt_path(c->g) || c->g.n_out > 0) return KIVI_EINVAL;
   if (n_queries > min_tokens_of(*c) || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
   if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(c->g, n_queries)) return KIVI_ENOSPC;
@@ -732,7 +746,7 @@ int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries
 int kivi_prefill_attn_ragged(kivi_cache* c, const void* q, void* out, const int64_t* n_queries, int64_t m_max,
                              void* scratch, size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch || !n_queries) return KIVI_ENULL;
-  if (simt_path(c->g)) return KIVI_EINVAL;
+  if (simt_path(c->g) || c->g.n_out > 0) return KIVI_EINVAL;
   if (!prefill_count_ok(c->g, m_max)) return KIVI_EINVAL;
   for (int32_t b = 0; b < c->g.B; ++b)
     if (n_queries[b] < 0 || n_queries[b] > m_max || n_queries[b] > c->T[b]) return KIVI_EINVAL;

@@ -16,6 +16,10 @@ struct Geo {
   int64_t window, n_slots;
   int64_t unit_bytes, sink_k, sink_v, res_k, res_v, groups;
   int64_t block_bytes, blk_kq, blk_ks, blk_vq, blk_vs;
+  int64_t blk_ko, blk_vo;  // outlier tables of a block: u16 row pointers [G + 1] by token,
+                           // then from out_ent the 4-byte entries {u8 t, u8 c, fp16 x}
+  int32_t n_out;           // entries per table; 0 without outliers
+  int32_t out_ent;         // offset of the entries inside a table
   int64_t cache_bytes;
   int64_t ws_partials;   // arena offset of the split-K partials
   int64_t ws_counters;   // arena offset of the per-unit merge counters

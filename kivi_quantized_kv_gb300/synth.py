@@ -49,6 +49,7 @@ class Workload:
     rope: bool = False
     v_lognormal: bool = True
     seed: int = 0
+    outlier_permille: int = 0   # dense-and-sparse: values per thousand kept exactly in the side tables
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -77,6 +78,12 @@ WORKLOADS = {
                          group=32, residual=128, sinks=4),
     "gqa8b_b3": Workload("gqa8b_b3", batch=4, h_q=32, h_kv=8, head_dim=128, tokens=32768, bits=3,
                          group=32, residual=128, sinks=4, rope=True),
+    # dense-and-sparse: the mha7b shape with 1 % of each key and value block
+    # kept exactly in the outlier tables (KVQuant's pairing of 3 bits and 1 %)
+    "mha7b_o10": Workload("mha7b_o10", batch=8, h_q=32, h_kv=32, head_dim=128, tokens=4096, bits=4,
+                          group=32, residual=128, sinks=4, outlier_permille=10),
+    "mha7b_b3_o10": Workload("mha7b_b3_o10", batch=8, h_q=32, h_kv=32, head_dim=128, tokens=4096, bits=3,
+                             group=32, residual=128, sinks=4, outlier_permille=10),
     # head dim 64 at 3 bits: the CUDA-core decode of the bit-stream widths
     "mha_d64_b3": Workload("mha_d64_b3", batch=8, h_q=32, h_kv=32, head_dim=64, tokens=4096, bits=3,
                            group=32, residual=128, sinks=4),

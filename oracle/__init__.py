@@ -40,7 +40,7 @@ class KoParams(ctypes.Structure):
 class KoLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "n_slots", "sink_k", "sink_v", "res_k", "res_v", "groups", "block_bytes",
-        "blk_kq", "blk_ks", "blk_vq", "blk_vs", "blk_ko", "blk_vo", "n_outliers", "unit_bytes", "cache_bytes")]
+        "blk_kq", "blk_ks", "blk_vq", "blk_vs", "blk_ko", "blk_vo", "n_outliers", "out_entries", "unit_bytes", "cache_bytes")]
 
 
 def lib():

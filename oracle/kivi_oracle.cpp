@@ -267,10 +267,13 @@ ko_layout layout_of(const ko_params& p) {
   L.blk_vs = L.blk_vq + d * G * b / 8;
   // dense-and-sparse outliers (pigeon guide, "KVQuant adds": a small share
   // of the values, around one in a hundred, kept in fp16 beside the codes):
-  // per block a key table and a value table of n_outliers 4-byte entries,
-  // each padded to 16 bytes
+  // per block a key table and a value table in compressed sparse rows by
+  // token: G + 1 u16 row pointers (entries of token t are [ptr[t], ptr[t+1])),
+  // then n_outliers 4-byte entries from a 4-byte boundary, each table padded
+  // to 16 bytes
   L.n_outliers = (static_cast<int64_t>(p.outlier_permille) * G * d + 999) / 1000;
-  const int64_t table = (4 * L.n_outliers + 15) / 16 * 16;
+  L.out_entries = L.n_outliers ? ((G + 1) * 2 + 3) / 4 * 4 : 0;
+  const int64_t table = L.n_outliers ? (L.out_entries + 4 * L.n_outliers + 15) / 16 * 16 : 0;
   L.blk_ko = L.blk_vs + G * 2 * 2;
   L.blk_vo = L.blk_ko + table;
   L.block_bytes = L.blk_vo + table;
@@ -318,19 +321,24 @@ void select_outliers(const uint16_t* x, int len, int64_t n, uint8_t* skip) {
   for (int64_t k = 0; k < n && k < len; ++k) skip[idx[k]] = 1;
 }
 
-// The flagged values of a [G][d] block as {u8 t, u8 ch, fp16 x} entries in
-// flat-index (t d + ch) order.
-void write_table(const uint16_t* x, const uint8_t* skip, int G, int d, uint8_t* out) {
+// The flagged values of a [G][d] block as a table of rows by token: row
+// pointers ptr[0..G] (ptr[t] = entries of tokens before t), then at
+// entries_off the {u8 t, u8 ch, fp16 x} entries in flat-index (t d + ch)
+// order.
+void write_table(const uint16_t* x, const uint8_t* skip, int G, int d, int64_t entries_off, uint8_t* out) {
   int64_t e = 0;
   for (int t = 0; t < G; ++t) {
+    put_u16(out + 2 * t, static_cast<uint16_t>(e));
     for (int ch = 0; ch < d; ++ch) {
       if (!skip[t * d + ch]) continue;
-      out[4 * e] = static_cast<uint8_t>(t);
-      out[4 * e + 1] = static_cast<uint8_t>(ch);
-      put_u16(out + 4 * e + 2, x[t * d + ch]);
+      uint8_t* en = out + entries_off + 4 * e;
+      en[0] = static_cast<uint8_t>(t);
+      en[1] = static_cast<uint8_t>(ch);
+      put_u16(en + 2, x[t * d + ch]);
       ++e;
     }
   }
+  put_u16(out + 2 * G, static_cast<uint16_t>(e));
 }
 
 // Flush: the ring's oldest G tokens (absolute positions a0 .. a0+G-1) become
@@ -358,8 +366,10 @@ void flush_group(ko_cache& c, uint8_t* unit, int64_t g) {
   std::vector<uint8_t> kskip(static_cast<size_t>(G) * d, 0), vskip(static_cast<size_t>(G) * d, 0);
   select_outliers(kx.data(), G * d, no, kskip.data());
   select_outliers(vx.data(), G * d, no, vskip.data());
-  write_table(kx.data(), kskip.data(), G, d, blk + c.L.blk_ko);
-  write_table(vx.data(), vskip.data(), G, d, blk + c.L.blk_vo);
+  if (no) {
+    write_table(kx.data(), kskip.data(), G, d, c.L.out_entries, blk + c.L.blk_ko);
+    write_table(vx.data(), vskip.data(), G, d, c.L.out_entries, blk + c.L.blk_vo);
+  }
   // keys, per channel over the group's tokens
   std::vector<uint8_t> kcodes(static_cast<size_t>(G) * d);
   std::vector<uint8_t> col(G);
@@ -429,9 +439,9 @@ void dequant_resident(const ko_cache& c, int64_t b_idx, int64_t h, double* K, do
       }
       // outliers are exact (dense-and-sparse)
       for (int64_t e = 0; e < c.L.n_outliers; ++e) {
-        const uint8_t* ke = blk + c.L.blk_ko + 4 * e;
+        const uint8_t* ke = blk + c.L.blk_ko + c.L.out_entries + 4 * e;
         if (ke[0] == t) kr[ke[1]] = f16_to_f32(get_u16(ke + 2));
-        const uint8_t* ve = blk + c.L.blk_vo + 4 * e;
+        const uint8_t* ve = blk + c.L.blk_vo + c.L.out_entries + 4 * e;
         if (ve[0] == t) vr[ve[1]] = f16_to_f32(get_u16(ve + 2));
       }
     } else {   // residual ring, fp16
@@ -669,8 +679,8 @@ int ko_prefill_attn(const ko_cache* c, const uint16_t* q, int64_t n_queries, dou
 // quantized tokens (keys and values), the key (Δ, min) rows of every group
 // touched, the value (Δ, min) of every visible quantized token, the fp16
 // residual keys and values, the fp32 sinks, the key and value outlier tables
-// (n_outliers 4-byte entries each) of every group touched; plus q and out
-// (fp16) per head.
+// (G + 1 u16 row pointers and n_outliers 4-byte entries each) of every group
+// touched; plus q and out (fp16) per head.
 int64_t ko_decode_bytes(const ko_cache* c) {
   const ko_params& p = c->p;
   const int64_t d = p.head_dim, G = p.group, b = p.bits, S = p.sinks, T = c->T;
@@ -684,7 +694,7 @@ int64_t ko_decode_bytes(const ko_cache* c) {
   }
   const int64_t ns = std::min(T, S);
   const int64_t per_unit = 2 * tq * d * b / 8 + 4 * d * touched + 4 * tq + 4 * d * c->n_res + 8 * d * ns +
-                          8 * c->L.n_outliers * touched;
+                          (c->L.n_outliers ? 2 * (2 * (G + 1) + 4 * c->L.n_outliers) * touched : 0);
   return per_unit * p.batch * p.h_kv + 4 * d * static_cast<int64_t>(p.batch) * p.h_q;
 }
 

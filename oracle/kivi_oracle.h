@@ -58,9 +58,12 @@ typedef struct ko_layout {
   int64_t groups;         /* first group block */
   int64_t block_bytes;    /* one group block */
   int64_t blk_kq, blk_ks, blk_vq, blk_vs; /* offsets inside a block */
-  int64_t blk_ko, blk_vo; /* key and value outlier tables: n_outliers entries
-                             of {u8 token, u8 channel, fp16 value} each */
+  int64_t blk_ko, blk_vo; /* key and value outlier tables (CSR by token):
+                             u16 row pointers [G + 1], then, from
+                             out_entries, n_outliers entries of
+                             {u8 token, u8 channel, fp16 value} */
   int64_t n_outliers;     /* entries per table (0 without outliers) */
+  int64_t out_entries;    /* offset of the entries inside a table */
   int64_t unit_bytes;     /* one (b, h_kv) unit */
   int64_t cache_bytes;    /* B * H_kv * unit_bytes */
 } ko_layout;

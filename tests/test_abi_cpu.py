@@ -45,7 +45,9 @@ def test_cache_bytes_covers_the_oracle_layout(abi, oracle_lib):
     from kivi_quantized_kv_gb300 import cache_bytes
     for kw in (dict(), dict(bits=2, head_dim=128, batch=8, h_q=32, h_kv=32, max_tokens=4096),
                dict(bits=8, group=64, residual=64, window=4096, max_tokens=0, h_q=32, h_kv=8, batch=32,
-                    head_dim=128)):
+                    head_dim=128),
+               dict(bits=3, head_dim=128, outlier_permille=10), dict(bits=2, group=64, residual=64,
+                                                                      outlier_permille=50)):
         cfg = params(**kw)
         lay = oracle_lib.layout(oracle_lib.Params(**cfg.__dict__))
         nb = cache_bytes(cfg)
@@ -57,7 +59,13 @@ def test_cache_bytes_covers_the_oracle_layout(abi, oracle_lib):
 @pytest.mark.parametrize("kw", [dict(bits=0), dict(bits=9), dict(bits=16), dict(bits=3, group=128, residual=128), dict(bits=5, group=16, residual=32), dict(head_dim=96), dict(group=8), dict(group=40),
                                 dict(residual=16), dict(residual=48), dict(sinks=-1), dict(h_q=6),
                                 dict(h_q=36, h_kv=4), dict(window=16, max_tokens=0), dict(window=-1),
-                                dict(batch=0), dict(max_tokens=-1)])
+                                dict(batch=0), dict(max_tokens=-1),
+                                # outlier tables: 0..50 per mille, 2 to 4 bits, G a multiple of 32,
+                                # 3 bits at head dim 128 only
+                                dict(outlier_permille=-1), dict(outlier_permille=51),
+                                dict(outlier_permille=10, bits=8), dict(outlier_permille=10, bits=1),
+                                dict(outlier_permille=10, group=16, residual=32),
+                                dict(outlier_permille=10, bits=3)])
 def test_invalid_parameters_are_rejected(abi, kw):
     from kivi_quantized_kv_gb300 import cache_bytes
     cfg = params(**kw)

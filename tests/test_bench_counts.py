@@ -22,13 +22,14 @@ def W(**kw):
 def n_slots(oracle_lib, w, T):
     p = oracle_lib.Params(bits=w.bits, group=w.group, residual=w.residual, sinks=w.sinks, h_q=w.h_q,
                           h_kv=w.h_kv, head_dim=w.head_dim, batch=w.batch, max_tokens=0 if w.window else T,
-                          window=w.window)
+                          window=w.window, outlier_permille=w.outlier_permille)
     return oracle_lib.layout(p)["n_slots"], p
 
 
-@pytest.mark.parametrize("window,T", [(0, 1), (0, 3), (0, 35), (0, 300), (48, 300), (48, 1000), (64, 77)])
-def test_decode_bytes_match_the_oracle(oracle_lib, window, T):
-    w = W(window=window)
+@pytest.mark.parametrize("window,T,pm", [(0, 1, 0), (0, 3, 0), (0, 35, 0), (0, 300, 0), (48, 300, 0), (48, 1000, 0),
+                                         (64, 77, 0), (0, 300, 10), (48, 1000, 37)])
+def test_decode_bytes_match_the_oracle(oracle_lib, window, T, pm):
+    w = W(window=window, group=32, outlier_permille=pm) if pm else W(window=window)
     ns, p = n_slots(oracle_lib, w, T)
     c = oracle_lib.Cache(p)
     rng = np.random.default_rng(T)

@@ -5,8 +5,9 @@ of the values (about one in a hundred) is kept in fp16 in a sparse table
 beside the low-bit codes.  The readings fixed here: per frozen key block and
 value block the n = ceil(permille G d / 1000) values of largest magnitude are
 outliers (ties to the smaller flat index t d + c); they take no part in the
-dense min and max, get code 0, are stored as {u8 t, u8 c, fp16 x} in flat
-order, and dequantize to x exactly.
+dense min and max, get code 0, are stored as rows by token (u16 row
+pointers, then {u8 t, u8 c, fp16 x} entries in flat order), and dequantize
+to x exactly.
 
 The pins do not restate the quantizer: blocks whose dense part lies on a
 2-bit grid reconstruct exactly only if the selection, the exclusion from the
@@ -64,13 +65,20 @@ def stream_with(p, blocks, rng, tail):
     return K[None, None].astype(np.float16), V[None, None].astype(np.float16)
 
 
-def table(c, slot, which):
+def table(c, slot, which, G=16):
+    """The entries of a block's table; its row pointers are checked against
+    them (row t holds exactly the entries of token t)."""
     L = c.layout
     blk = c.unit(0, 0)[L["groups"] + slot * L["block_bytes"]:][:L["block_bytes"]]
     off = L["blk_ko"] if which == "k" else L["blk_vo"]
-    raw = blk[off:off + 4 * L["n_outliers"]].reshape(-1, 4)
+    ptr = blk[off:off + 2 * (G + 1)].copy().view(np.uint16)
+    raw = blk[off + L["out_entries"]:off + L["out_entries"] + 4 * L["n_outliers"]].reshape(-1, 4)
     vals = raw[:, 2:].copy().view(np.float16)[:, 0]
-    return [(int(t), int(ch), float(x)) for (t, ch), x in zip(raw[:, :2], vals)]
+    ent = [(int(t), int(ch), float(x)) for (t, ch), x in zip(raw[:, :2], vals)]
+    assert ptr[0] == 0 and ptr[G] == len(ent)
+    for t in range(G):
+        assert all(e[0] == t for e in ent[ptr[t]:ptr[t + 1]]), (t, ptr)
+    return ent
 
 
 def test_entry_count_and_layout(oracle_lib):
@@ -79,8 +87,9 @@ def test_entry_count_and_layout(oracle_lib):
     assert L0["n_outliers"] == 0 and L0["blk_ko"] == L0["blk_vo"] == L0["block_bytes"]
     assert L["n_outliers"] == 11                          # ceil(10 * 16 * 64 / 1000) = ceil(10.24)
     assert L["blk_ko"] == L0["block_bytes"]               # tables after the value scales
-    assert L["blk_vo"] - L["blk_ko"] == 48                # 44 bytes, padded to 16
-    assert L["block_bytes"] == L0["block_bytes"] + 96
+    assert L["out_entries"] == 36                         # 17 u16 row pointers, to a 4-byte boundary
+    assert L["blk_vo"] - L["blk_ko"] == 80                # 36 + 44 bytes, padded to 16
+    assert L["block_bytes"] == L0["block_bytes"] + 160
     assert oracle_lib.layout(P(oracle_lib, group=32, head_dim=128, outlier_permille=1))["n_outliers"] == 5
     assert oracle_lib.validate(P(oracle_lib, outlier_permille=50)) == 0
     for bad in (-1, 51):
@@ -139,6 +148,10 @@ def test_ties_go_to_the_smaller_flat_index(oracle_lib):
     assert c.append(k, v) == 0 and c.n_groups == 1
     want = [(0, ch, K[0, ch]) for ch in range(8)] + [(5, 7, -2.0), (9, 0, 2.0), (12, 63, 2.0)]
     assert table(c, 0, "k") == want
+    # row pointers worked by hand: 8 entries in row 0, one each in rows 5, 9, 12
+    L = c.layout
+    ptr = c.unit(0, 0)[L["groups"] + L["blk_ko"]:][:34].copy().view(np.uint16)
+    assert ptr.tolist() == [0] + [8] * 5 + [9] * 4 + [10] * 3 + [11] * 4
 
 
 def test_a_channel_of_outliers_only_gets_zero_scales(oracle_lib):
