@@ -34,6 +34,7 @@ class KoParams(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("max_tokens", ctypes.c_int64), ("window", ctypes.c_int64),
         ("outlier_permille", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("rope_base", ctypes.c_double),
     ]
 
 
@@ -158,10 +159,12 @@ class Params:
     max_tokens: int = 0
     window: int = 0
     outlier_permille: int = 0
+    rope_base: float = 0.0
 
     def c(self) -> KoParams:
         return KoParams(self.bits, self.group, self.residual, self.sinks, self.h_q, self.h_kv,
-                        self.head_dim, self.batch, self.max_tokens, self.window, self.outlier_permille, 0)
+                        self.head_dim, self.batch, self.max_tokens, self.window, self.outlier_permille, 0,
+                        self.rope_base)
 
 
 def validate(p: Params) -> int:

@@ -226,6 +226,7 @@ int validate(const ko_params& p) {
   if (p.window < 0 || p.max_tokens < 0) return kInvalid;
   if (p.window > 0 && p.window < p.residual) return kInvalid;
   if (p.outlier_permille < 0 || p.outlier_permille > 50) return kInvalid;
+  if (!(p.rope_base == 0.0 || (p.rope_base > 1.0 && p.rope_base <= 1e7))) return kInvalid;
   return kOk;
 }
 
@@ -465,6 +466,27 @@ void dequant_unit(const ko_cache& c, int64_t b_idx, int64_t h, double* K, double
     if (a < lo) vis[a] = 0;
 }
 
+// Pre-RoPE keys (pigeon guide, "KVQuant adds": keys quantized before the
+// rotary embedding, which would otherwise mix channel pairs): the rows K[a]
+// of positions a = 0 .. T-1, as dequantized, rotated in place by RoPE at
+// their own positions.  Reading: the rotate-half pairing, channel i with
+// i + d/2, angle a * base^(-2i/d); the query arrives already rotated at its
+// own position, so the scores are q . R(a) k_a.
+void rope_rotate(const ko_params& p, double* K, int64_t T) {
+  if (p.rope_base == 0.0) return;
+  const int d = p.head_dim, h = d / 2;
+  for (int i = 0; i < h; ++i) {
+    const double theta = std::pow(p.rope_base, -2.0 * i / d);
+    for (int64_t a = 0; a < T; ++a) {
+      const double phi = static_cast<double>(a) * theta;
+      const double cs = std::cos(phi), sn = std::sin(phi);
+      const double x = K[a * d + i], y = K[a * d + i + h];
+      K[a * d + i] = x * cs - y * sn;
+      K[a * d + i + h] = y * cs + x * sn;
+    }
+  }
+}
+
 // softmax(q Kᵀ / sqrt(d)) V of one query row over the visible tokens, two
 // passes in fp64 (scores and their max, then the weights); all zero when no
 // token is visible.
@@ -501,6 +523,7 @@ void attend_unit(const ko_cache& c, int64_t b_idx, int64_t h, const uint16_t* q,
   std::vector<double> K(static_cast<size_t>(T) * d), V(static_cast<size_t>(T) * d);
   std::vector<uint8_t> vis(static_cast<size_t>(T));
   dequant_unit(c, b_idx, h, K.data(), V.data(), vis.data());
+  rope_rotate(p, K.data(), T);
   std::vector<double> qd(d);
   for (int r = 0; r < rep; ++r) {
     const int64_t hq = h * rep + r;
@@ -528,6 +551,7 @@ void attend_unit_causal(const ko_cache& c, int64_t b_idx, int64_t h, const uint1
   std::vector<double> K(static_cast<size_t>(T) * d), V(static_cast<size_t>(T) * d);
   std::vector<uint8_t> res(static_cast<size_t>(T)), vis(static_cast<size_t>(T));
   dequant_resident(c, b_idx, h, K.data(), V.data(), res.data());
+  rope_rotate(p, K.data(), T);
   std::vector<double> qd(d);
   for (int64_t j = 0; j < M; ++j) {
     const int64_t P = T - M + j;

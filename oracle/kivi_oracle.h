@@ -48,6 +48,10 @@ typedef struct ko_params {
                                block, ceil(permille * G * d / 1000) values kept
                                exactly in a side table; 0 = none */
   int32_t reserved;
+  double rope_base;  /* 0: keys arrive rotated (post-RoPE).  > 1: keys arrive
+                        and are stored before RoPE; attention rotates each
+                        dequantized key at its position (rotate-half pairs
+                        (i, i + d/2), angle position * base^(-2i/d)) */
 } ko_params;
 
 /* Byte layout of one (batch, kv-head) unit and of one frozen group block. */
