@@ -409,7 +409,9 @@ def run_ours(args, rank, world, device):
         # flush launch when any of them freezes a group)
         runs = [b for b in range(w.batch) if b == 0 or T_now[r][b] != T_now[r][b - 1]]
         freezes = [state_at(w, T_now[r][b0] + 1)[1] > state_at(w, T_now[r][b0])[1] for b0 in runs]
-        if w.bits not in (2, 4, 8) and w.head_dim != 128:   # CUDA-core widths: per run, append (flush, write) + decode
+        if (w.bits not in (2, 4, 8) and w.head_dim != 128) or w.rope_base:
+            # the CUDA-core decode (bit-stream widths at head dim 64, pre-RoPE
+            # keys): per run, append (flush, write) + decode
             launches += sum((2 if f else 1) + 1 for f in freezes)
         elif not fused:   # kivi_append, one launch pair (flush, write) per run, then the decode
             launches += sum(2 if f else 1 for f in freezes) + -(-len(runs) // 64)
@@ -756,7 +758,10 @@ def main():
                                       "ragged": bool(args.ragged)}),
         "roofline": {"bound": "hbm", "achieved": round(r["dec_gbs"], 1), "peak": peak, "unit": "GB/s",
                      "frac": round(r["dec_gbs"] / peak, 4), "traffic": traffic,
-                     "kernel": "decode_mma_kernel (stream-K split-K, merge and fresh-token append in the same launch)", "peak_source": src,
+                     "kernel": ("decode_simt_kernel (CUDA cores, per-run append then decode)"
+                                if (w.bits not in (2, 4, 8) and w.head_dim != 128) or w.rope_base else
+                                "decode_mma_kernel (stream-K split-K, merge and fresh-token append in the same launch)"),
+                     "peak_source": src,
                      "bytes_per_launch": int(r["dec_bytes"])},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
@@ -780,7 +785,8 @@ def main():
 
 DECODE_SOURCES = ("kivi_internal.cuh", "decode_mma.cuh", "decode_launch.cuh", "decode.cu",
                   "decode_b2.cu", "decode_b4.cu", "decode_b8.cu", "decode_simt.cuh", "decode_simt.cu",
-                  "decode_simt_d64.cu", "decode_simt_d128.cu", "decode_outl.cuh", "decode_outl.cu",
+                  "decode_simt_d64.cu", "decode_simt_d128.cu", "decode_simt_rope_d64.cu", "decode_simt_rope_d128.cu",
+                  "decode_outl.cuh", "decode_outl.cu",
                   "decode_outl_b2.cu", "decode_outl_b3.cu", "decode_outl_b4.cu")
 
 

@@ -96,6 +96,18 @@ typedef struct kivi_params {
                                  the fused step add the corrections; the
                                  multi-query attention refuses such a cache */
   int32_t reserved;           /* 0 */
+  double rope_base;           /* 0: keys arrive rotated (post-RoPE, or no
+                                 RoPE).  > 1 (at most 1e7): pre-RoPE keys
+                                 (KV-cache quantization guide (pigeon),
+                                 "KVQuant adds"): keys are stored and
+                                 quantized as they arrive, before the rotary
+                                 embedding, and attention rotates each
+                                 dequantized key at its own position a:
+                                 channels (i, i + d/2) by the angle
+                                 a * rope_base^(-2i/d); q arrives rotated.
+                                 Needs group 32 or 64 and no outlier tables;
+                                 decodes on CUDA cores; the multi-query
+                                 attention refuses such a cache */
 } kivi_params;
 
 /* Byte layout of the arena and current state (all offsets in bytes).

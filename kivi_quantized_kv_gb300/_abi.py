@@ -31,6 +31,7 @@ class KiviParams(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("max_tokens", ctypes.c_int64), ("window", ctypes.c_int64),
         ("outlier_permille", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("rope_base", ctypes.c_double),
     ]
 
 

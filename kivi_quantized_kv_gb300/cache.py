@@ -27,16 +27,19 @@ class KiviConfig:
     max_tokens: int = 0
     window: int = 0
     outlier_permille: int = 0
+    rope_base: float = 0.0
 
     def c(self) -> _abi.KiviParams:
         return _abi.KiviParams(self.bits, self.group, self.residual, self.sinks, self.h_q, self.h_kv,
-                               self.head_dim, self.batch, self.max_tokens, self.window, self.outlier_permille, 0)
+                               self.head_dim, self.batch, self.max_tokens, self.window, self.outlier_permille, 0,
+                               self.rope_base)
 
     @staticmethod
     def from_workload(w) -> "KiviConfig":
         return KiviConfig(bits=w.bits, group=w.group, residual=w.residual, sinks=w.sinks, h_q=w.h_q,
                           h_kv=w.h_kv, head_dim=w.head_dim, batch=w.batch, max_tokens=w.max_tokens,
-                          window=w.window, outlier_permille=getattr(w, "outlier_permille", 0))
+                          window=w.window, outlier_permille=getattr(w, "outlier_permille", 0),
+                          rope_base=getattr(w, "rope_base", 0.0))
 
 
 def cache_bytes(cfg: KiviConfig) -> int:

@@ -23,7 +23,8 @@ cudaError_t launch_decode_simt(const Geo& g, const uint8_t* arena, const __half*
             static_cast<int32_t>((plan.st.n_res + simt::kTail - 1) / simt::kTail);
   if (a.items < 1) a.items = 1;
   const int64_t units = static_cast<int64_t>(g.B) * g.hkv;
-  const int smem = simt::kWarps * (g.d == 64 ? simt::Smem<64>::bytes(g) : simt::Smem<128>::bytes(g));
+  const int smem = simt::kWarps * (g.d == 64 ? simt::Smem<64>::bytes(g) : simt::Smem<128>::bytes(g)) +
+                   simt::rope_bytes(g);
   // many short CTAs (about eight per resident slot) so that the waves end
   // evenly, within the partial records a unit has
   int resident = 1;

@@ -22,6 +22,20 @@
 // All query heads of the kv head share each block read.  The warps' (m, l, o)
 // are combined in shared memory; a unit split over several CTAs leaves
 // partial records and the last CTA (an atomic count) merges them.
+//
+// Pre-RoPE keys (ROPE; pigeon guide, "KVQuant adds": keys quantized before
+// the rotary embedding, which would otherwise mix channel pairs): the codes
+// hold the unrotated keys, and every dequantized key is rotated at its own
+// position a before the dot product, pairs (i, i + D/2) by the angle
+// a θ_i, θ_i = base^(-2i/D); the query arrives rotated.  A per-token
+// rotation does not fold into one operand shared by a group's tokens, so
+// these caches decode here, at every code width.  cos and sin of a θ_i:
+//   * frozen groups, a = a0 + t: angle addition of the group's base a0 θ_i
+//     (one per pair and group, from a double-precision angle reduced mod 2π)
+//     and the offset t θ_i (a per-CTA table [D/2][G], built once);
+//   * sinks and ring tokens: the double-precision angle of each token.
+// The score of token t for a head, with k_i = min_i + code_i Δ_i:
+//   s = Σ_i cos (k_i q_i + k_{i+D/2} q_{i+D/2}) + sin (k_i q_{i+D/2} - k_{i+D/2} q_i).
 #pragma once
 
 #include "kivi_internal.cuh"
@@ -63,20 +77,61 @@ struct Smem {
   }
 };
 
-// 32 codes of BITS bits held in BITS consecutive 32-bit words (code j at bit
-// BITS j of the words taken as one little-endian bit string), as floats.
+// 32 codes of BITS bits held in BITS consecutive 32-bit words, as floats.
+// Bit-stream widths: code j at bit BITS j of the words taken as one
+// little-endian bit string.  Widths 2, 4, 8 (the word rule): word j / (32 /
+// BITS) holds code j at bit 16 (e & 1) + BITS (e >> 1), e = j mod (32 / BITS).
 // Every shift is a compile-time constant.
 template <int BITS>
 __device__ __forceinline__ void unpack32(const uint32_t (&w)[BITS], float (&f)[32]) {
   constexpr uint32_t M = (1u << BITS) - 1u;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const int bit = BITS * j, wi = bit >> 5, sh = bit & 31;
     uint32_t v;
-    if (sh + BITS <= 32) v = (w[wi] >> sh) & M;
-    else v = __funnelshift_r(w[wi], w[wi + 1], sh) & M;
+    if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
+      constexpr int per = 32 / BITS;
+      const int e = j % per;
+      v = (w[j / per] >> (16 * (e & 1) + BITS * (e >> 1))) & M;
+    } else {
+      const int bit = BITS * j, wi = bit >> 5, sh = bit & 31;
+      if (sh + BITS <= 32) v = (w[wi] >> sh) & M;
+      else v = __funnelshift_r(w[wi], w[wi + 1], sh) & M;
+    }
     f[j] = static_cast<float>(v);
   }
+}
+
+// code j of a packed row (the same packing as unpack32), with run-time shifts
+template <int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint32_t* row, int j) {
+  constexpr uint32_t M = (1u << BITS) - 1u;
+  if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
+    constexpr int per = 32 / BITS;
+    const int e = j % per;
+    return (row[j / per] >> (16 * (e & 1) + BITS * (e >> 1))) & M;
+  } else {
+    const int bit = BITS * j, wi = bit >> 5, sh = bit & 31;
+    uint32_t v = row[wi] >> sh;
+    if (sh + BITS > 32) v |= row[wi + 1] << (32 - sh);
+    return v & M;
+  }
+}
+
+// cos and sin of a double-precision angle, reduced mod 2π in double first
+// (positions times θ reach 10^5 rad), then taken in single precision
+__device__ __forceinline__ float2 rope_cs(double ang) {
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  const double r = ang - kTwoPi * rint(ang * (1.0 / kTwoPi));
+  float sn, cs;
+  sincosf(static_cast<float>(r), &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+// shared memory of the RoPE tables of one CTA: θ (double) [D/2], the offset
+// table [D/2][G] and one base row [D/2] per warp (float2)
+__host__ __device__ inline int rope_bytes(const Geo& g) {
+  const int h = g.d / 2;
+  return g.rope_l2b != 0.0 ? h * 8 + h * g.G * 8 + kWarps * h * 8 : 0;
 }
 
 // 16-byte asynchronous copies global -> shared (Ampere-style cp.async; the
@@ -89,9 +144,10 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
-template <int D, int BITS>
+template <int D, int BITS, bool ROPE>
 __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) {
   extern __shared__ __align__(16) uint8_t smem[];
+  constexpr int H2 = D / 2;
   const Geo& g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rep = g.rep;
@@ -114,6 +170,18 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) 
     qs[i] = __half2float(a.q[(static_cast<int64_t>(bb) * g.hq + hk * rep + h) * D + c]) * qscale;
   }
   __syncwarp();
+
+  // RoPE tables: θ_i, the offsets' cos / sin, this warp's base row
+  double* theta = reinterpret_cast<double*>(smem + kWarps * Smem<D>::bytes(g));
+  float2* offs = reinterpret_cast<float2*>(theta + H2);          // [H2][G]
+  float2* wbase = offs + H2 * g.G + warp * H2;                   // [H2]
+  if constexpr (ROPE) {
+    for (int i = threadIdx.x; i < H2; i += blockDim.x) theta[i] = exp2(-(2.0 * i / D) * g.rope_l2b);
+    __syncthreads();
+    for (int x = threadIdx.x; x < H2 * g.G; x += blockDim.x)
+      offs[x] = rope_cs(static_cast<double>(x % g.G) * theta[x / g.G]);
+    __syncthreads();
+  }
 
   float m[kMaxRep], l[kMaxRep], o[kMaxRep][CPL];
 #pragma unroll
@@ -182,11 +250,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) 
       const int64_t grp = a.plan.g_first + it;
       const __half* ks = reinterpret_cast<const __half*>(blk + g.blk_ks);   // Δ[D], min[D]
       const __half* vs = reinterpret_cast<const __half*>(blk + g.blk_vs);   // (Δ, min) per token
-      // q Δ per head and channel; Σ q min per head
+      // q Δ per head and channel; Σ q min per head (without RoPE)
       float cmin[kMaxRep];
 #pragma unroll
       for (int h = 0; h < kMaxRep; ++h) cmin[h] = 0.f;
-      for (int c = lane; c < D; c += 32) {
+      for (int c = lane; c < (ROPE ? 0 : D); c += 32) {
         const float dq = __half2float(ks[c]), mn = __half2float(ks[D + c]);
 #pragma unroll
         for (int h = 0; h < kMaxRep; ++h) {
@@ -205,6 +273,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) 
       __syncwarp();
       const int64_t a0 = g.S + grp * G;
       const int ns = G / 32;   // tokens per lane (G in {32, 64})
+      if constexpr (ROPE) {   // the group's base angles a0 θ_i
+        for (int i = lane; i < H2; i += 32) wbase[i] = rope_cs(static_cast<double>(a0) * theta[i]);
+        __syncwarp();
+      }
       // scores: lane = token t = lane + 32 i; each 32-channel chunk of its
       // row is unpacked once and used by every head
       float s[2][kMaxRep];
@@ -214,6 +286,28 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) 
         const int t = lane + 32 * i;
         const uint32_t* row = reinterpret_cast<const uint32_t*>(blk + g.blk_kq + t * (D * BITS / 8));
         float acc[kMaxRep];
+        if constexpr (ROPE) {
+          // the pairs (i, i + D/2): codes read one at a time (a rolled loop
+          // keeps the registers and the code small), dequantized, rotated at
+          // position a0 + t, dotted with every head's q
+#pragma unroll
+          for (int h = 0; h < kMaxRep; ++h) acc[h] = 0.f;
+#pragma unroll 2
+          for (int ci = 0; ci < H2; ++ci) {
+            const float k1 = fmaf(static_cast<float>(code_at<BITS>(row, ci)), __half2float(ks[ci]),
+                                  __half2float(ks[D + ci]));
+            const float k2 = fmaf(static_cast<float>(code_at<BITS>(row, ci + H2)), __half2float(ks[ci + H2]),
+                                  __half2float(ks[D + ci + H2]));
+            const float2 b = wbase[ci], o = offs[ci * G + t];
+            const float cs = b.x * o.x - b.y * o.y, sn = b.y * o.x + b.x * o.y;
+            const float r1 = k1 * cs - k2 * sn, r2 = k2 * cs + k1 * sn;
+#pragma unroll
+            for (int h = 0; h < kMaxRep; ++h) {
+              if (h >= rep) break;
+              acc[h] = fmaf(qs[h * D + ci], r1, fmaf(qs[h * D + ci + H2], r2, acc[h]));
+            }
+          }
+        } else {
 #pragma unroll
         for (int h = 0; h < kMaxRep; ++h) acc[h] = cmin[h];
 #pragma unroll
@@ -236,6 +330,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) 
               acc[h] = fmaf(qv.w, f[4 * x + 3], acc[h]);
             }
           }
+        }
         }
         const bool vis = a0 + t >= lo_pos;
 #pragma unroll
@@ -323,6 +418,17 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) 
         float kr[CPL];
 #pragma unroll
         for (int jj = 0; jj < CPL; ++jj) kr[jj] = kval(u, lane + 32 * jj);
+        if constexpr (ROPE) {   // channels lane + 32 jj and their partners + D/2, at the token's position
+          const int64_t pos = sink ? static_cast<int64_t>(first + u)
+                                   : g.S + a.plan.st.n_groups * g.G + first + u;
+#pragma unroll
+          for (int jj = 0; jj < CPL / 2; ++jj) {
+            const float2 r = rope_cs(static_cast<double>(pos) * theta[lane + 32 * jj]);
+            const float x = kr[jj], y = kr[jj + CPL / 2];
+            kr[jj] = x * r.x - y * r.y;
+            kr[jj + CPL / 2] = y * r.x + x * r.y;
+          }
+        }
 #pragma unroll
         for (int h = 0; h < kMaxRep; ++h) {
           if (h >= rep) break;
@@ -425,23 +531,46 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const Args a) 
 
 // Launches a.splits CTAs per unit; with `resident` non-null it only reports
 // the CTAs of this instantiation one SM holds at `smem`.
-template <int D, int BITS>
+template <int D, int BITS, bool ROPE>
 cudaError_t launch_one(const Args& a, int ctas, int smem, cudaStream_t s, int* resident) {
-  cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<D, BITS, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
   if (e != cudaSuccess) return e;
-  if (resident) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(resident, decode_simt_kernel<D, BITS>, kWarps * 32, smem);
-  decode_simt_kernel<D, BITS><<<ctas, kWarps * 32, smem, s>>>(a);
+  if (resident)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(resident, decode_simt_kernel<D, BITS, ROPE>, kWarps * 32, smem);
+  decode_simt_kernel<D, BITS, ROPE><<<ctas, kWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
+// with RoPE: every width (decode_simt_rope_d{64,128}.cu)
+template <int D>
+cudaError_t launch_rope_d(const Args& a, int ctas, int smem, cudaStream_t s, int* resident) {
+  switch (a.g.bits) {
+    case 1: return launch_one<D, 1, true>(a, ctas, smem, s, resident);
+    case 2: return launch_one<D, 2, true>(a, ctas, smem, s, resident);
+    case 3: return launch_one<D, 3, true>(a, ctas, smem, s, resident);
+    case 4: return launch_one<D, 4, true>(a, ctas, smem, s, resident);
+    case 5: return launch_one<D, 5, true>(a, ctas, smem, s, resident);
+    case 6: return launch_one<D, 6, true>(a, ctas, smem, s, resident);
+    case 7: return launch_one<D, 7, true>(a, ctas, smem, s, resident);
+    case 8: return launch_one<D, 8, true>(a, ctas, smem, s, resident);
+    default: return cudaErrorInvalidValue;
+  }
+}
+cudaError_t launch_rope_d64(const Args& a, int ctas, int smem, cudaStream_t s, int* resident);
+cudaError_t launch_rope_d128(const Args& a, int ctas, int smem, cudaStream_t s, int* resident);
+
+// without RoPE: the bit-stream widths
 template <int D>
 cudaError_t launch_d(const Args& a, int ctas, int smem, cudaStream_t s, int* resident) {
+  if (a.g.rope_l2b != 0.0)
+    return D == 64 ? launch_rope_d64(a, ctas, smem, s, resident) : launch_rope_d128(a, ctas, smem, s, resident);
   switch (a.g.bits) {
-    case 1: return launch_one<D, 1>(a, ctas, smem, s, resident);
-    case 3: return launch_one<D, 3>(a, ctas, smem, s, resident);
-    case 5: return launch_one<D, 5>(a, ctas, smem, s, resident);
-    case 6: return launch_one<D, 6>(a, ctas, smem, s, resident);
-    case 7: return launch_one<D, 7>(a, ctas, smem, s, resident);
+    case 1: return launch_one<D, 1, false>(a, ctas, smem, s, resident);
+    case 3: return launch_one<D, 3, false>(a, ctas, smem, s, resident);
+    case 5: return launch_one<D, 5, false>(a, ctas, smem, s, resident);
+    case 6: return launch_one<D, 6, false>(a, ctas, smem, s, resident);
+    case 7: return launch_one<D, 7, false>(a, ctas, smem, s, resident);
     default: return cudaErrorInvalidValue;
   }
 }

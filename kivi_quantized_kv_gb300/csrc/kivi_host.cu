@@ -70,6 +70,10 @@ int validate(const kivi_params* p) {
   if (p->outlier_permille > 0 &&
       (p->bits < 2 || p->bits > 4 || p->group % 32 != 0 || (p->bits == 3 && p->head_dim != 128)))
     return KIVI_EINVAL;
+  // pre-RoPE keys decode on CUDA cores (a group in one warp's shared memory,
+  // value rows whole 32-bit words), without outlier tables
+  if (!(p->rope_base == 0.0 || (p->rope_base > 1.0 && p->rope_base <= 1e7))) return KIVI_EINVAL;
+  if (p->rope_base != 0.0 && ((p->group != 32 && p->group != 64) || p->outlier_permille != 0)) return KIVI_EINVAL;
   return KIVI_OK;
 }
 
@@ -88,6 +92,7 @@ Geo geometry(const kivi_params& p) {
   g.bits = p.bits; g.G = p.group; g.R = p.residual; g.S = p.sinks;
   g.hq = p.h_q; g.hkv = p.h_kv; g.d = p.head_dim; g.B = p.batch; g.rep = p.h_q / p.h_kv;
   g.window = p.window;
+  g.rope_l2b = p.rope_base != 0.0 ? std::log2(p.rope_base) : 0.0;
   const int64_t d = p.head_dim, G = p.group, b = p.bits;
   if (p.window > 0) {
     g.n_slots = (p.window + G - 1) / G + 1;
@@ -331,8 +336,9 @@ cudaError_t attn_run(const kivi_cache& c, const Run& r, const kivi::DecodePlan& 
 float* ws_partials(const kivi_cache& c) { return reinterpret_cast<float*>(c.arena + c.g.ws_partials); }
 
 // Bit-stream widths decode on tensor cores at head dim 128 (a lane's quarter
-// of a key row is whole 32-bit words) and on CUDA cores at head dim 64.
-bool simt_path(const Geo& g) { return !kivi::word_rule(g.bits) && g.d != 128; }
+// of a key row is whole 32-bit words) and on CUDA cores at head dim 64;
+// pre-RoPE keys (a rotation per token) decode on CUDA cores at every width.
+bool simt_path(const Geo& g) { return (!kivi::word_rule(g.bits) && g.d != 128) || g.rope_l2b != 0.0; }
 
 // The plans of runs [first, first + count) for one ragged launch (one query
 // token per sequence); fused: every sequence also attends to and appends one

@@ -20,6 +20,7 @@ struct Geo {
                            // then from out_ent the 4-byte entries {u8 t, u8 c, fp16 x}
   int32_t n_out;           // entries per table; 0 without outliers
   int32_t out_ent;         // offset of the entries inside a table
+  double rope_l2b;         // log2 of the RoPE base for pre-RoPE keys; 0 = keys arrive rotated
   int64_t cache_bytes;
   int64_t ws_partials;   // arena offset of the split-K partials
   int64_t ws_counters;   // arena offset of the per-unit merge counters

@@ -50,6 +50,7 @@ class Workload:
     v_lognormal: bool = True
     seed: int = 0
     outlier_permille: int = 0   # dense-and-sparse: values per thousand kept exactly in the side tables
+    rope_base: float = 0.0      # > 0: the cache takes pre-RoPE keys and rotates them at attention
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -84,6 +85,11 @@ WORKLOADS = {
                           group=32, residual=128, sinks=4, outlier_permille=10),
     "mha7b_b3_o10": Workload("mha7b_b3_o10", batch=8, h_q=32, h_kv=32, head_dim=128, tokens=4096, bits=3,
                              group=32, residual=128, sinks=4, outlier_permille=10),
+    # pre-RoPE keys: the gqa8b shape with its keys given to the cache before
+    # the rotary embedding (the stream does not rotate them); the cache
+    # rotates each key at its position inside the decode
+    "gqa8b_b4_prerope": Workload("gqa8b_b4_prerope", batch=4, h_q=32, h_kv=8, head_dim=128, tokens=32768, bits=4,
+                                 group=32, residual=128, sinks=4, rope=False, rope_base=10000.0),
     # head dim 64 at 3 bits: the CUDA-core decode of the bit-stream widths
     "mha_d64_b3": Workload("mha_d64_b3", batch=8, h_q=32, h_kv=32, head_dim=64, tokens=4096, bits=3,
                            group=32, residual=128, sinks=4),

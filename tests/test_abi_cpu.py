@@ -65,7 +65,12 @@ def test_cache_bytes_covers_the_oracle_layout(abi, oracle_lib):
                                 dict(outlier_permille=-1), dict(outlier_permille=51),
                                 dict(outlier_permille=10, bits=8), dict(outlier_permille=10, bits=1),
                                 dict(outlier_permille=10, group=16, residual=32),
-                                dict(outlier_permille=10, bits=3)])
+                                dict(outlier_permille=10, bits=3),
+                                # pre-RoPE keys: base 0 or in (1, 1e7], G 32 or 64, no outlier tables
+                                dict(rope_base=1.0), dict(rope_base=-3.0), dict(rope_base=2e7),
+                                dict(rope_base=10000.0, group=16, residual=32),
+                                dict(rope_base=10000.0, group=128, residual=128),
+                                dict(rope_base=10000.0, outlier_permille=10)])
 def test_invalid_parameters_are_rejected(abi, kw):
     from kivi_quantized_kv_gb300 import cache_bytes
     cfg = params(**kw)

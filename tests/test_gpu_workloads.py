@@ -68,7 +68,7 @@ def run_sampled(w, units, chunk=2048, layer=0):
 
 
 @pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa8b_b4", "gqa8b_b2", "swa_mistral", "mha7b_b3", "gqa8b_b3",
-                                  "mha_d64_b3", "mha7b_o10", "mha7b_b3_o10"])
+                                  "mha_d64_b3", "mha7b_o10", "mha7b_b3_o10", "gqa8b_b4_prerope"])
 def test_workload_full_size_sampled_units(name):
     w = WORKLOADS[name]
     units = sorted({(0, 0), (w.batch - 1, w.h_kv - 1), (w.batch // 2, w.h_kv // 2)})
