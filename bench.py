@@ -658,7 +658,7 @@ def oracle_sample(w, units_max, seed=0, extra=4096):
     ws = w.with_(batch=bs, h_kv=hk, h_q=hk * rep)
     p = oracle.Params(bits=w.bits, group=w.group, residual=w.residual, sinks=w.sinks, h_q=ws.h_q, h_kv=ws.h_kv,
                       head_dim=w.head_dim, batch=ws.batch, max_tokens=0 if w.window else w.tokens + extra,
-                      window=w.window, outlier_permille=w.outlier_permille)
+                      window=w.window, outlier_permille=w.outlier_permille, rope_base=w.rope_base)
     c = oracle.Cache(p)
     kv = KVStream(ws, device="cpu")
     t = 0
