@@ -367,6 +367,12 @@ int kivi_set_num_splits(kivi_cache* cache, int32_t num_splits);
 /* Layout, counters and sizes of the handle.  Errors: ENULL. */
 int kivi_cache_layout(const kivi_cache* cache, kivi_layout* out);
 
+/* The layout a cache of these parameters has, without creating one (host
+ * only; touches no device): every offset and size as kivi_cache_layout
+ * reports it, the state fields those of an empty cache (tokens 0).
+ * Errors: ENULL, EINVAL (invalid parameters). */
+int kivi_layout_for(const kivi_params* params, kivi_layout* out);
+
 /* Algorithmic bytes one decode call must move at the current state: packed
  * codes of the visible quantized tokens, key (Δ, min) rows of the groups they
  * touch, value (Δ, min) pairs, fp16 ring tokens, fp32 sinks, q and out.

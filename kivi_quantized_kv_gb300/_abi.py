@@ -19,7 +19,7 @@ EXPORTS = (
     "kivi_cache_tokens", "kivi_prefill_attn_ragged", "kivi_cache_restore", "kivi_debug_inject_launch_failure",
     "kivi_decode_attn", "kivi_append_decode_attn", "kivi_append_decode_attn_host", "kivi_decode_attn_host",
     "kivi_decode_attn_noalloc", "kivi_prefill_attn", "kivi_prefill_scratch_bytes", "kivi_prefill_bytes",
-    "kivi_read_error", "kivi_set_num_splits", "kivi_cache_layout",
+    "kivi_read_error", "kivi_set_num_splits", "kivi_cache_layout", "kivi_layout_for",
     "kivi_decode_bytes", "kivi_status_string",
 )
 
@@ -85,6 +85,7 @@ def lib():
         "kivi_read_error": (ctypes.c_int, [vp, P(ctypes.c_uint32), vp]),
         "kivi_set_num_splits": (ctypes.c_int, [vp, i32]),
         "kivi_cache_layout": (ctypes.c_int, [vp, P(KiviLayout)]),
+        "kivi_layout_for": (ctypes.c_int, [P(KiviParams), P(KiviLayout)]),
         "kivi_decode_bytes": (i64, [vp]),
         "kivi_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }

@@ -636,12 +636,9 @@ int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {
   return KIVI_OK;
 }
 
-int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
-  if (!c || !out) return KIVI_ENULL;
-  const Geo& g = c->g;
-  const State st = kivi::state_at(g, c->T[0]);
-  bool uniform = true;
-  for (const int64_t t : c->T) uniform = uniform && t == c->T[0];
+namespace {
+// the geometry fields of a layout (the state fields are left 0)
+kivi_layout layout_of_geo(const Geo& g) {
   kivi_layout L{};
   L.n_slots = g.n_slots;
   L.sink_k = g.sink_k; L.sink_v = g.sink_v; L.res_k = g.res_k; L.res_v = g.res_v; L.groups = g.groups;
@@ -651,9 +648,28 @@ int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
   L.workspace_offset = g.ws_partials;
   L.arena_bytes = arena_bytes_of(g);
   L.workspace_bytes = L.arena_bytes - g.ws_partials;
+  L.max_splits = g.max_splits;
+  return L;
+}
+}  // namespace
+
+int kivi_layout_for(const kivi_params* p, kivi_layout* out) {
+  if (!p || !out) return KIVI_ENULL;
+  const int v = validate(p);
+  if (v != KIVI_OK) return v;
+  *out = layout_of_geo(geometry(*p));
+  return KIVI_OK;
+}
+
+int kivi_cache_layout(const kivi_cache* c, kivi_layout* out) {
+  if (!c || !out) return KIVI_ENULL;
+  const Geo& g = c->g;
+  const State st = kivi::state_at(g, c->T[0]);
+  bool uniform = true;
+  for (const int64_t t : c->T) uniform = uniform && t == c->T[0];
+  kivi_layout L = layout_of_geo(g);
   // the state of sequence 0; tokens is -1 when the sequences' lengths differ
   L.tokens = uniform ? c->T[0] : -1; L.n_sink = st.n_sink; L.n_groups = st.n_groups; L.n_res = st.n_res;
-  L.max_splits = g.max_splits;
   *out = L;
   return KIVI_OK;
 }

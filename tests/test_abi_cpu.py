@@ -137,3 +137,48 @@ def test_restore_rejects_bad_arguments_before_any_device_call(abi):
                                 ctypes.byref(h)) == abi.KIVI_EINVAL
     assert L.kivi_cache_restore(ctypes.byref(p), ctypes.c_void_p(258), 1 << 30, toks, None,
                                 ctypes.byref(h)) == abi.KIVI_EALIGN
+
+
+LAYOUT_CASES = [
+    dict(),
+    dict(bits=2, head_dim=128, batch=8, h_q=32, h_kv=32, max_tokens=4096),
+    dict(bits=8, group=64, residual=64, window=4096, max_tokens=0, h_q=32, h_kv=8, batch=32, head_dim=128),
+    dict(bits=3, head_dim=128, outlier_permille=10),
+    dict(bits=2, group=64, residual=64, outlier_permille=50),
+    dict(bits=4, group=32, residual=96, sinks=0, outlier_permille=1, window=200, max_tokens=0),
+    dict(bits=5, group=64, residual=64, rope_base=10000.0),
+    dict(bits=1, group=32, residual=32, sinks=7, rope_base=500000.0, head_dim=128),
+    dict(bits=7, group=32, residual=64, head_dim=128, sinks=3),
+    dict(bits=6, group=64, residual=128, head_dim=64, sinks=0, window=300, max_tokens=0),
+]
+
+
+@pytest.mark.parametrize("kw", LAYOUT_CASES)
+def test_host_layout_equals_the_oracle_layout(abi, oracle_lib, kw):
+    """The library's byte layout (kivi_layout_for, host only) against the
+    oracle's own computation of it, offset by offset: the cache region the
+    GPU tests compare byte for byte starts from the same map."""
+    cfg = params(**kw)
+    p = cfg.c()
+    lay = abi.KiviLayout()
+    assert abi.lib().kivi_layout_for(ctypes.byref(p), ctypes.byref(lay)) == abi.KIVI_OK
+    ref = oracle_lib.layout(oracle_lib.Params(**cfg.__dict__))
+    for name in ("n_slots", "sink_k", "sink_v", "res_k", "res_v", "groups", "block_bytes", "blk_kq", "blk_ks",
+                 "blk_vq", "blk_vs", "blk_ko", "blk_vo", "n_outliers", "unit_bytes", "cache_bytes"):
+        assert getattr(lay, name) == ref[name], name
+    assert lay.out_entries == ref["out_entries"]
+    assert lay.tokens == 0 and lay.n_groups == 0 and lay.workspace_offset >= lay.cache_bytes
+    assert lay.arena_bytes == cache_bytes_of(abi, p)
+
+
+def cache_bytes_of(abi, p):
+    return abi.lib().kivi_cache_bytes(ctypes.byref(p))
+
+
+def test_host_layout_rejects_what_create_rejects(abi):
+    lay = abi.KiviLayout()
+    bad = params(bits=9).c()
+    assert abi.lib().kivi_layout_for(ctypes.byref(bad), ctypes.byref(lay)) == abi.KIVI_EINVAL
+    assert abi.lib().kivi_layout_for(None, ctypes.byref(lay)) == abi.KIVI_ENULL
+    good = params().c()
+    assert abi.lib().kivi_layout_for(ctypes.byref(good), None) == abi.KIVI_ENULL
