@@ -33,7 +33,7 @@ class KoParams(ctypes.Structure):
         ("sinks", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32),
         ("max_tokens", ctypes.c_int64), ("window", ctypes.c_int64),
-        ("outlier_permille", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("outlier_permille", ctypes.c_int32), ("window_mode", ctypes.c_int32),
         ("rope_base", ctypes.c_double),
     ]
 
@@ -160,11 +160,14 @@ class Params:
     window: int = 0
     outlier_permille: int = 0
     rope_base: float = 0.0
+    # the other reading of a window composed with sinks: a pure window, in
+    # which the sinks expire like any other token (0 = sinks stay visible)
+    window_mode: int = 0
 
     def c(self) -> KoParams:
         return KoParams(self.bits, self.group, self.residual, self.sinks, self.h_q, self.h_kv,
-                        self.head_dim, self.batch, self.max_tokens, self.window, self.outlier_permille, 0,
-                        self.rope_base)
+                        self.head_dim, self.batch, self.max_tokens, self.window, self.outlier_permille,
+                        self.window_mode, self.rope_base)
 
 
 def validate(p: Params) -> int:

@@ -226,6 +226,7 @@ int validate(const ko_params& p) {
   if (p.window < 0 || p.max_tokens < 0) return kInvalid;
   if (p.window > 0 && p.window < p.residual) return kInvalid;
   if (p.outlier_permille < 0 || p.outlier_permille > 50) return kInvalid;
+  if (p.window_mode != 0 && p.window_mode != 1) return kInvalid;
   if (!(p.rope_base == 0.0 || (p.rope_base > 1.0 && p.rope_base <= 1e7))) return kInvalid;
   return kOk;
 }
@@ -457,12 +458,15 @@ void dequant_resident(const ko_cache& c, int64_t b_idx, int64_t h, double* K, do
 }
 
 // Dequantized keys/values of one unit plus visibility for a query at the
-// newest position T - 1.  Reading: with a window, sinks stay visible and every
-// other token is visible when it is among the most recent W tokens.
+// newest position T - 1.  Reading (window_mode 0): with a window, sinks stay
+// visible and every other token is visible when it is among the most recent W
+// tokens.  window_mode 1 (a pure window): the sinks too are visible only while
+// they are among the most recent W tokens.
 void dequant_unit(const ko_cache& c, int64_t b_idx, int64_t h, double* K, double* V, uint8_t* vis) {
   dequant_resident(c, b_idx, h, K, V, vis);
   const int64_t lo = (c.p.window > 0) ? c.T - c.p.window : 0;   // window start
-  for (int64_t a = c.p.sinks; a < c.T; ++a)
+  const int64_t from = c.p.window_mode == 1 ? 0 : c.p.sinks;     // tokens the window can expire
+  for (int64_t a = from; a < c.T; ++a)
     if (a < lo) vis[a] = 0;
 }
 
@@ -540,13 +544,14 @@ void attend_unit(const ko_cache& c, int64_t b_idx, int64_t h, const uint16_t* q,
 // attention step while the context accumulates in the cache).
 // Query j sits at position P = T - M + j; q and out are [B][M][H_q][d].
 // Token a is visible to it when the cache still holds a, a <= P, and, with a
-// window, a is a sink or among the W tokens ending at P.  Tokens of the chunk
+// window, a is a sink (window_mode 0 only) or among the W tokens ending at P.
+// Tokens of the chunk
 // are read as the cache holds them now (fp16 in the ring, codes once frozen).
 void attend_unit_causal(const ko_cache& c, int64_t b_idx, int64_t h, const uint16_t* q, int64_t M,
                         double* out) {
   const ko_params& p = c.p;
   const int d = p.head_dim;
-  const int64_t T = c.T, S = p.sinks;
+  const int64_t T = c.T, S = p.window_mode == 1 ? 0 : p.sinks;   // sinks that outlive the window
   const int rep = p.h_q / p.h_kv;
   std::vector<double> K(static_cast<size_t>(T) * d), V(static_cast<size_t>(T) * d);
   std::vector<uint8_t> res(static_cast<size_t>(T)), vis(static_cast<size_t>(T));
@@ -704,7 +709,8 @@ int ko_prefill_attn(const ko_cache* c, const uint16_t* q, int64_t n_queries, dou
 // touched, the value (Δ, min) of every visible quantized token, the fp16
 // residual keys and values, the fp32 sinks, the key and value outlier tables
 // (G + 1 u16 row pointers and n_outliers 4-byte entries each) of every group
-// touched; plus q and out (fp16) per head.
+// touched; plus q and out (fp16) per head.  Sinks count as visible (window_mode
+// 0, the CUDA library's reading).
 int64_t ko_decode_bytes(const ko_cache* c) {
   const ko_params& p = c->p;
   const int64_t d = p.head_dim, G = p.group, b = p.bits, S = p.sinks, T = c->T;

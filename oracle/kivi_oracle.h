@@ -47,7 +47,12 @@ typedef struct ko_params {
   int32_t outlier_permille; /* dense-and-sparse: per frozen key block and value
                                block, ceil(permille * G * d / 1000) values kept
                                exactly in a side table; 0 = none */
-  int32_t reserved;
+  int32_t window_mode; /* the two readings of a window composed with sinks
+                          (tract #2329 "Relationship to other PRs" gives no
+                          sink rule): 0 = the sinks stay visible beside the
+                          most recent W tokens (the CUDA library's reading);
+                          1 = a pure window, the sinks expire like any other
+                          token once they leave the most recent W */
   double rope_base;  /* 0: keys arrive rotated (post-RoPE).  > 1: keys arrive
                         and are stored before RoPE; attention rotates each
                         dequantized key at its position (rotate-half pairs

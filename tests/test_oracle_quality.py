@@ -72,7 +72,9 @@ def test_int8_near_lossless(oracle_lib, seed):
     synthetic keys (N(0,1) queries against x10-30 outlier channels) give a
     sharper softmax than GPT-2, so absolute deviations run about twice the
     page's; the pin is int8 < 2% (mean over rows) and the page's ratios
-    between widths: int4/int8 ~14-20x, int2/int4 ~4-7x."""
+    between widths, int4/int8 14-20x and int2/int4 4.1-7.3x (from 7-10% /
+    0.5% and 41-51% / 7-10%), each held to within a factor 1.5 of the
+    page's range on this synthetic stand-in."""
     k, v, q = outlier_stream(2, 4, 512, 64, seed=seed)
     ref = full_precision(q, k, v, 1)
     dev = {}
@@ -83,8 +85,8 @@ def test_int8_near_lossless(oracle_lib, seed):
     # kvquant++ README: 3 bits sits between 2 (some loss) and 4 (near-lossless)
     assert dev[4] < dev[3] < dev[2]
     assert deviation(run(oracle_lib, 8, k, v, q)[0], ref) < 0.05
-    assert 8.0 < dev[4] / dev[8] < 40.0
-    assert 2.0 < dev[2] / dev[4] < 10.0
+    assert 14.0 / 1.5 < dev[4] / dev[8] < 20.0 * 1.5
+    assert 4.1 / 1.5 < dev[2] / dev[4] < 7.3 * 1.5
 
 
 def _attend_dequant(q, K, V):
