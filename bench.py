@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--ragged", action="store_true",
                     help="ragged batch: decode with sequence b holding T - T*b/(2B) tokens; with --prefill, "
                          "sequence b takes a chunk of M - M*b/(2B) tokens (all lengths differ)")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed windows of exactly --steps steps each; the line reports the median window")
+    ap.add_argument("--sweep", action="store_true",
+                    help="every cell of the 32-layer decode-step sweep, one JSON line per cell")
     return ap.parse_args()
 
 
@@ -309,7 +313,9 @@ def run_ours(args, rank, world, device):
     from kivi_quantized_kv_gb300.synth import KVStream, queries
 
     w = workload(args.workload)
-    total_steps = args.steps + args.warmup
+    # W warm-up steps, R timed windows of K steps, then K steps timed one by
+    # one for the decode kernel's own time
+    total_steps = args.warmup + (args.repeats + 1) * args.steps
     cap_extra = total_steps + 64
     cfg = KiviConfig.from_workload(w)
     if w.window == 0:
@@ -323,9 +329,15 @@ def run_ours(args, rank, world, device):
     stream = torch.cuda.current_stream(device)
 
     caches = []
-    # ragged: sequence b starts at T - 1 - T*b/(2B) tokens (every length differs)
-    targets = [w.tokens - 1 - ((w.tokens * b) // (2 * w.batch) if args.ragged else 0) for b in range(w.batch)]
     for r in range(n_rep):
+        # ragged: sequence b starts at T - 1 - T*b/(2B) tokens (every length
+        # differs).  Replica r starts r*G/n_rep tokens shorter, so that the
+        # steps whose token freezes a group (one in G per sequence) fall
+        # evenly over any window of consecutive steps, as they do over a long
+        # run, instead of all replicas freezing within the same few steps
+        stagger = (r * w.group) // n_rep
+        targets = [w.tokens - 1 - stagger - ((w.tokens * b) // (2 * w.batch) if args.ragged else 0)
+                   for b in range(w.batch)]
         c = KiviCache(cfg, device=device)
         kv = KVStream(w.with_(seed=w.seed + 100 * r), device=device)
         t = [0] * w.batch
@@ -375,33 +387,14 @@ def run_ours(args, rank, world, device):
     T_before = [c.tokens_per_sequence() for c, _ in caches]   # tokens of each replica's sequences before the timed steps
     meta = [(c.layout()["n_slots"], c.layout()["block_bytes"]) for c, _ in caches]
 
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(device) if rank == 0 else None
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
-    if clocks:
-        clocks.start()
-        time.sleep(0.05)
-        clocks.mark_begin()
-    t0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
-    t1.record(stream)
-    torch.cuda.synchronize(device)
-    if clocks:
-        clocks.mark_end()
-    clk = clocks.stop() if clocks else None
-    if world > 1:
-        torch.distributed.barrier()
-    ms = t0.elapsed_time(t1)
-    # bytes of the timed steps, from each replica's token count at each step
+    # per timed step (from the first one after the warm-up): its bytes, its
+    # launches and whether its token freezes a group, from each replica's
+    # token count at that step
     T_now = [list(t) for t in T_before]
     w1 = w.with_(batch=1)
-    dec_bytes = app_bytes = launches = 0
-    for i in range(args.steps):
-        r = (args.warmup + i) % n_rep
+    per_step = []
+    for s in range(args.warmup, total_steps):
+        r = s % n_rep
         n_slots, block_bytes = meta[r]
         # the library's runs (consecutive sequences of equal length): one run is
         # one decode launch (plus a flush launch when its token freezes a
@@ -412,37 +405,251 @@ def run_ours(args, rank, world, device):
         if (w.bits not in (2, 4, 8) and w.head_dim != 128) or w.rope_base:
             # the CUDA-core decode (bit-stream widths at head dim 64, pre-RoPE
             # keys): per run, append (flush, write) + decode
-            launches += sum((2 if f else 1) + 1 for f in freezes)
+            launches = sum((2 if f else 1) + 1 for f in freezes)
         elif not fused:   # kivi_append, one launch pair (flush, write) per run, then the decode
-            launches += sum(2 if f else 1 for f in freezes) + -(-len(runs) // 64)
+            launches = sum(2 if f else 1 for f in freezes) + -(-len(runs) // 64)
         else:
-            for i in range(0, len(runs), 64):
-                launches += 1 + (1 if any(freezes[i:i + 64]) else 0)
+            launches = sum(1 + (1 if any(freezes[i:i + 64]) else 0) for i in range(0, len(runs), 64))
+        dec = app = 0
         for b in range(w.batch):
-            app_bytes += append_bytes_at(w1, T_now[r][b], block_bytes)
+            app += append_bytes_at(w1, T_now[r][b], block_bytes)
             T_now[r][b] += 1
-            dec_bytes += decode_bytes_at(w1, T_now[r][b], n_slots)
+            dec += decode_bytes_at(w1, T_now[r][b], n_slots)
+        per_step.append((dec, app, launches, any(freezes)))
+    clocks = ClockSampler(device) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.05)
+        clocks.mark_begin()
+    # R windows of exactly K steps, each bracketed by a barrier and a device
+    # synchronisation on both sides and timed by CUDA events on the stream
+    windows = []
+    s0 = args.warmup
+    for rep in range(args.repeats):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(s0 + i)
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+        ms = t0.elapsed_time(t1)
+        steps_w = per_step[s0 - args.warmup:s0 - args.warmup + args.steps]
+        dec_b = sum(x[0] for x in steps_w)
+        app_b = sum(x[1] for x in steps_w)
+        ms_max, all_bytes = across_ranks(ms, dec_b + app_b, world, device)
+        windows.append({"ms": ms_max, "bytes": all_bytes, "dec_bytes": dec_b, "app_bytes": app_b,
+                        "dec_ms": ms, "launches": sum(x[2] for x in steps_w),
+                        "freezing_steps": sum(1 for x in steps_w if x[3])})
+        s0 += args.steps
+    if clocks:
+        clocks.mark_end()
+    clk = clocks.stop() if clocks else None
+    # the median window (by throughput) is the line's value
+    order = sorted(range(len(windows)), key=lambda i: windows[i]["bytes"] / windows[i]["ms"])
+    med = windows[order[len(order) // 2]]
+    value = med["bytes"] / (med["ms"] / 1e3) / 1e9
+
+    # the decode kernel's own time: K more steps, each bracketed by events;
+    # the steps that freeze no group are one decode launch each (the fused
+    # step), so their mean duration is the decode kernel's launch time
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    torch.cuda.synchronize(device)
+    for i in range(args.steps):
+        ev[i].record(stream)
+        step(s0 + i)
+    ev[args.steps].record(stream)
+    torch.cuda.synchronize(device)
+    dur = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     for r, (c, _) in enumerate(caches):   # the byte count above is the library's own
         assert c.tokens_per_sequence() == T_now[r]
         assert c.decode_bytes() == sum(decode_bytes_at(w1, t, meta[r][0]) for t in T_now[r]), \
             "decode byte count mismatch"
-    ms_max, all_bytes = across_ranks(ms, dec_bytes + app_bytes, world, device)
-    step_bytes = (dec_bytes + app_bytes) / args.steps
-    value = all_bytes / (ms_max / 1e3) / 1e9
-    # the decode kernel's roofline: the timed steps back to back are that
-    # kernel's launches (plus a flush launch on the steps that freeze a
-    # group, counted against it), so its achieved rate is the decode bytes
-    # over the whole timed span
-    dec_gbs = dec_bytes / (ms / 1e3) / 1e9
+    steps_k = per_step[s0 - args.warmup:s0 - args.warmup + args.steps]
+    plain = [(d, x[0]) for d, x in zip(dur, steps_k) if not x[3]] or [(d, x[0]) for d, x in zip(dur, steps_k)]
+    flush_steps = [d for d, x in zip(dur, steps_k) if x[3]]
+    kern_ms = sum(d for d, _ in plain) / len(plain)
+    kern_bytes = sum(b for _, b in plain) / len(plain)
     res = {
-        "w": w, "cfg": cfg, "n_rep": n_rep, "per_cache": per_cache, "ms": ms_max, "value": value,
-        "dec_gbs": dec_gbs, "dec_ms": ms / args.steps, "app_ms": ms / args.steps,
-        "dec_bytes": dec_bytes / args.steps, "fused": fused, "step_bytes": step_bytes, "launches": launches,
-        "clocks": clk, "app_tok_s": w.batch * args.steps / (ms / 1e3),
+        "w": w, "cfg": cfg, "n_rep": n_rep, "per_cache": per_cache, "ms": med["ms"], "value": value,
+        "dec_gbs": kern_bytes / (kern_ms / 1e3) / 1e9, "dec_ms": kern_ms, "dec_bytes": kern_bytes,
+        "window_dec_gbs": med["dec_bytes"] / (med["dec_ms"] / 1e3) / 1e9,
+        "flush_step_ms": (sum(flush_steps) / len(flush_steps)) if flush_steps else None,
+        "fused": fused, "step_bytes": med["bytes"] / args.steps, "launches": med["launches"],
+        "clocks": clk, "app_tok_s": w.batch * world * args.steps / (med["ms"] / 1e3),
+        "windows": [{"ms": round(x["ms"], 4), "gbs": round(x["bytes"] / (x["ms"] / 1e3) / 1e9, 1),
+                     "freezing_steps": x["freezing_steps"]} for x in windows],
+        "kernel_steps": len(plain),
     }
     if not args.no_e2e and not args.ragged:
         res["e2e"] = run_e2e(args, caches, new_kv, w, device, stream)
     return res
+
+
+def run_sweep_cell(args, device, w):
+    """One cell of the 32-layer decode-step sweep: a step appends one token to
+    every sequence of every layer and runs every layer's decode attention
+    over its cache (one kivi_append_decode_attn per layer, the 32 layers in
+    order).  Layer l's K/V stream is seeded 1000003*seed + l.  Small cells
+    rotate over whole-model replicas until 4x the 129 MB L2 is covered; a
+    cell whose caches do not fit the free device memory is reported as such,
+    with its footprint from kivi_cache_bytes."""
+    import ctypes
+    import torch
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig, _abi, cache_bytes
+    from kivi_quantized_kv_gb300.synth import KVStream, queries
+
+    layers = w.layers
+    total_steps = args.warmup + (args.repeats + 1) * args.steps
+    cfg = KiviConfig(**{**KiviConfig.from_workload(w).__dict__, "max_tokens": w.tokens + total_steps + 64})
+    per_layer = cache_bytes(cfg)
+    model = per_layer * layers
+    l2 = 129 * 1024 * 1024
+    n_rep = max(1, -(-4 * l2 // model))
+    free, _total = torch.cuda.mem_get_info(device)
+    # the timed steps' inputs and the fill's staging chunks need room too
+    inputs = total_steps * layers * 2 * w.batch * w.h_kv * w.head_dim * 2
+    staging = 12 * w.batch * w.h_kv * 4096 * w.head_dim * 4
+    need = n_rep * model + inputs + staging + (1 << 30)
+    base_cfg = workload_config(w, {"layers": layers, "parallelism": "replicas1"})
+    if need > free:
+        return {"metric": METRIC, "workload": w.name, "does_not_fit": True,
+                "footprint_bytes": int(model), "free_bytes": int(free),
+                "note": "32 layers of kivi_cache_bytes exceed the free device memory", "config": base_cfg}
+    stream = torch.cuda.current_stream(device)
+    reps = []   # per replica: list of (cache, stream) per layer
+    for r in range(n_rep):
+        stagger = (r * w.group) // n_rep
+        lay = []
+        for l in range(layers):
+            c = KiviCache(cfg, device=device)
+            kv = KVStream(w.with_(seed=w.seed + 100 * r), layer=l, device=device)
+            t = 0
+            target = w.tokens - 1 - stagger
+            while t < target:
+                n = min(4096, target - t)
+                k, v = kv.next(n)
+                c.append(k, v)
+                t += n
+            lay.append((c, kv))
+        reps.append(lay)
+    torch.cuda.synchronize(device)
+    # per step and layer: the new token and a query, resident before timing
+    new_kv = [[reps[s % n_rep][l][1].next(1) for l in range(layers)] for s in range(total_steps)]
+    qs = [[queries(w, step=s, layer=l, device=device) for l in range(layers)] for s in range(min(total_steps, 8))]
+    outs = [torch.empty((w.batch, w.h_q, w.head_dim), dtype=torch.float16, device=device) for _ in range(layers)]
+    torch.cuda.synchronize(device)
+    L = _abi.lib()
+    vp = ctypes.c_void_p
+    sp = vp(stream.cuda_stream)
+    args_of = [[(reps[s % n_rep][l][0]._h, vp(new_kv[s][l][0].data_ptr()), vp(new_kv[s][l][1].data_ptr()),
+                 vp(qs[s % len(qs)][l].data_ptr()), vp(outs[l].data_ptr())) for l in range(layers)]
+               for s in range(total_steps)]
+    fn = L.kivi_append_decode_attn
+
+    def step(s):
+        for a in args_of[s]:
+            st = fn(*a, sp)
+            if st != 0:
+                raise RuntimeError(_abi.status_string(st))
+
+    T0 = [reps[r][0][0].tokens for r in range(n_rep)]
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize(device)
+    # bytes of every timed step (the same for every layer of a replica)
+    T_now = [reps[r][0][0].tokens for r in range(n_rep)]
+    n_slots, block_bytes = reps[0][0][0].layout()["n_slots"], reps[0][0][0].layout()["block_bytes"]
+    w1 = w.with_(batch=1)
+    per_step = []
+    for s in range(args.warmup, total_steps):
+        r = s % n_rep
+        freeze = state_at(w, T_now[r] + 1)[1] > state_at(w, T_now[r])[1]
+        app = append_bytes_at(w1, T_now[r], block_bytes) * w.batch
+        T_now[r] += 1
+        dec = decode_bytes_at(w1, T_now[r], n_slots) * w.batch
+        per_step.append((dec * layers, app * layers, layers * (2 if freeze else 1), freeze, dec))
+    clocks = ClockSampler(device)
+    clocks.start()
+    time.sleep(0.05)
+    clocks.mark_begin()
+    windows = []
+    s0 = args.warmup
+    for rep in range(args.repeats):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(s0 + i)
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+        st = per_step[s0 - args.warmup:s0 - args.warmup + args.steps]
+        windows.append({"ms": t0.elapsed_time(t1), "bytes": sum(x[0] + x[1] for x in st),
+                        "launches": sum(x[2] for x in st), "freezing_steps": sum(1 for x in st if x[3])})
+        s0 += args.steps
+    clocks.mark_end()
+    clk = clocks.stop()
+    order = sorted(range(len(windows)), key=lambda i: windows[i]["bytes"] / windows[i]["ms"])
+    med = windows[order[len(order) // 2]]
+    # the decode kernel's own launch time: K more steps, each layer's call
+    # bracketed by events; calls whose token freezes no group are one launch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * layers + 1)]
+    torch.cuda.synchronize(device)
+    j = 0
+    for i in range(args.steps):
+        for a in args_of[s0 + i]:
+            ev[j].record(stream)
+            st = fn(*a, sp)
+            if st != 0:
+                raise RuntimeError(_abi.status_string(st))
+            j += 1
+    ev[j].record(stream)
+    torch.cuda.synchronize(device)
+    st_k = per_step[s0 - args.warmup:s0 - args.warmup + args.steps]
+    plain = [ev[i * layers + l].elapsed_time(ev[i * layers + l + 1]) for i in range(args.steps) if not st_k[i][3]
+             for l in range(layers)]
+    plain_bytes = [st_k[i][4] for i in range(args.steps) if not st_k[i][3]]
+    for r in range(n_rep):
+        for c, _ in reps[r]:
+            assert c.read_error() == 0
+            assert c.tokens == T0[r] + sum(1 for s in range(total_steps) if s % n_rep == r)
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    kern_ms = sum(plain) / len(plain) if plain else None
+    kern_bytes = sum(plain_bytes) / len(plain_bytes) if plain_bytes else None
+    step_ms = med["ms"] / args.steps
+    value = med["bytes"] / (med["ms"] / 1e3) / 1e9
+    achieved = kern_bytes / (kern_ms / 1e3) / 1e9 if kern_ms else None
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16xf16->f32", "data": "synthetic",
+        "config": {**base_cfg, "l2": f"{n_rep} rotating replicas of the 32-layer caches x {model / 1e6:.0f} MB"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None, "traffic": None,
+                     "kernel": "decode_mma_kernel (one launch per layer)", "peak_source": src,
+                     "bytes_per_launch": int(kern_bytes) if kern_bytes else None},
+        "gpu_launches": med["launches"], "clocks": clk, "repeats": args.repeats,
+        "windows": [{"ms": round(x["ms"], 4), "gbs": round(x["bytes"] / (x["ms"] / 1e3) / 1e9, 1),
+                     "freezing_steps": x["freezing_steps"]} for x in windows],
+        "bytes_per_step": int(med["bytes"] / args.steps),
+        "decode_steps_per_s": round(1e3 / step_ms, 2),
+        "tokens_per_s": round(w.batch * 1e3 / step_ms, 1),
+        "tokens_per_s_kind": "sequence tokens decoded per second (each appended to all 32 layers)",
+        "decode_us_per_layer": round(kern_ms * 1e3, 2) if kern_ms else None,
+        "footprint_bytes": int(model),
+    }
+
+
+def sweep_cells():
+    from kivi_quantized_kv_gb300.synth import SWEEP_BATCH, SWEEP_BITS, SWEEP_TOKENS, sweep_workload
+    return [sweep_workload(b, t, bits) for b in SWEEP_BATCH for t in SWEEP_TOKENS for bits in SWEEP_BITS]
 
 
 def run_prefill(args, device):
@@ -739,6 +946,13 @@ def main():
             raise SystemExit("--prefill runs on one GPU")
         print(json.dumps(run_prefill(args, device)), flush=True)
         return
+    if args.sweep or w.layers > 1:
+        if world > 1:
+            raise SystemExit("the sweep runs on one GPU")
+        for cell in (sweep_cells() if args.sweep else [w]):
+            print(json.dumps(run_sweep_cell(args, device, cell)), flush=True)
+            torch.cuda.empty_cache()
+        return
     r = run_ours(args, rank, world, device)
     if rank != 0:
         if world > 1:
@@ -754,7 +968,9 @@ def main():
         "config": workload_config(w, {"parallelism": f"replicas{world}",
                                       "l2": f"{r['n_rep']} rotating cache replicas x {r['per_cache'] / 1e6:.0f} MB "
                                             f"(> 4x 129 MB L2)",
-                                      "appended_per_sequence": -(-(args.steps + args.warmup) // r["n_rep"]),
+                                      "appended_per_sequence": -(-(args.warmup + (args.repeats + 1) * args.steps) //
+                                                                 r["n_rep"]),
+                                      "replica_stagger": "replica r starts r*G/replicas tokens short of T - 1",
                                       "ragged": bool(args.ragged)}),
         "roofline": {"bound": "hbm", "achieved": round(r["dec_gbs"], 1), "peak": peak, "unit": "GB/s",
                      "frac": round(r["dec_gbs"] / peak, 4), "traffic": traffic,
@@ -765,9 +981,15 @@ def main():
                      "bytes_per_launch": int(r["dec_bytes"])},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
+        "repeats": args.repeats,
+        "windows": r["windows"],
         "decode_gbs": round(r["dec_gbs"], 1),
         "decode_frac_of_8tbs": round(r["dec_gbs"] / NOMINAL_HBM_GBS, 4),
         "decode_us": round(r["dec_ms"] * 1e3, 2),
+        "decode_us_kind": (f"mean CUDA-event time of the {r['kernel_steps']} of {args.steps} steps (timed one by "
+                           f"one after the windows) whose token freezes no group: one decode launch each"),
+        "flush_step_us": round(r["flush_step_ms"] * 1e3, 2) if r["flush_step_ms"] else None,
+        "window_decode_gbs": round(r["window_dec_gbs"], 1),
         "decode_steps_per_s": round(1e3 / r["dec_ms"], 1),
         "step_call": "kivi_append_decode_attn" if r["fused"] else "kivi_append + kivi_decode_attn",
         "append_tokens_per_s": round(r["app_tok_s"], 1),

@@ -76,8 +76,50 @@ def test_workload_full_size_sampled_units(name):
     print(f"{name}: worst row error {err:.2e}")
 
 
-@pytest.mark.parametrize("batch,tokens,bits,layer", [(16, 16384, 4, 0), (1, 131072, 2, 31), (128, 1024, 8, 5)])
+def sampled_units(batch, h_kv, n, seed):
+    """n distinct (sequence, kv head) units, the first and last among them."""
+    g = np.random.default_rng(seed)
+    total = batch * h_kv
+    others = [int(u) for u in g.permutation(total) if u not in (0, total - 1)]
+    pick = sorted({0, total - 1} | set(others[:max(0, n - 2)]))
+    return [(u // h_kv, u % h_kv) for u in pick]
+
+
+@pytest.mark.parametrize("batch,tokens,bits,layer", [(16, 16384, 4, 0), (1, 131072, 2, 31), (128, 1024, 8, 5),
+                                                     (16, 1024, 2, 17)])
 def test_sweep_cells_sampled(batch, tokens, bits, layer):
+    """Cells of the 32-layer decode-step sweep at full size, 16 sampled
+    (sequence, kv head) units each (every unit when a cell has fewer)."""
     w = sweep_workload(batch, tokens, bits)
-    units = sorted({(0, 0), (batch - 1, 7), (batch // 2, 3)})
-    run_sampled(w, units, chunk=4096, layer=layer)
+    run_sampled(w, sampled_units(batch, w.h_kv, 16, seed=batch * 7 + bits), chunk=4096, layer=layer)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_sweep_full_32_layer_step(bits):
+    """One whole decode step of the smallest sweep cell (B 1, T 1024): each of
+    the 32 layers holds its own cache (seeded per layer) and takes its fused
+    append + decode call; every layer's bytes and every head's output are
+    checked against an oracle cache of that layer."""
+    from kivi_quantized_kv_gb300.synth import KVStream, queries
+    w = sweep_workload(1, 1024, bits)
+    dev = torch.device("cuda")
+    cfg = KiviConfig.from_workload(w)
+    worst = 0.0
+    for layer in range(w.layers):
+        cache = KiviCache(cfg, device=dev)
+        ref = oracle.Cache(oparams(cfg))
+        stream = KVStream(w, layer=layer, device="cpu")
+        k, v = stream.next(w.tokens - 1)
+        cache.append(k.to(dev), v.to(dev))
+        assert ref.append(k.numpy(), v.numpy()) == 0
+        k1, v1 = stream.next(1)
+        q = queries(w, layer=layer)
+        out = cache.append_decode(k1.to(dev), v1.to(dev), q.to(dev)).float().cpu().numpy()
+        assert ref.append(k1.numpy(), v1.numpy()) == 0
+        torch.cuda.synchronize()
+        assert np.array_equal(cache.cache_region().cpu().numpy(), ref.arena()), layer
+        err = row_rel_err(out, ref.decode_attn(q.numpy(), threads=8))
+        assert err <= TOL, (layer, err)
+        worst = max(worst, err)
+        assert cache.read_error() == 0
+    print(f"32 layers, {bits} bits: worst row error {worst:.2e}")
