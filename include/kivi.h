@@ -61,9 +61,7 @@ typedef enum kivi_status {
  *              kvquant++ README: 3 bits recommended).  b in {2, 4, 8} pack
  *              by the word rule below; the other widths pack as a bit
  *              stream and need G in {32, 64}.  Every width decodes on
- *              tensor cores at head dim 128; the bit-stream widths at head
- *              dim 64 decode on CUDA cores and have no multi-query
- *              (prefill) attention.
+ *              tensor cores at head dims 64 and 128.
  *   group      G: tokens per frozen key group; a multiple of 16 in [16, 256].
  *   residual   R: capacity of the fp16 residual ring; R >= G and R % G == 0.
  *   sinks      S in [0, 1024]: leading tokens kept in fp32.
@@ -91,10 +89,9 @@ typedef struct kivi_params {
   int32_t outlier_permille;   /* dense-and-sparse outliers: 0 = none, else
                                  1..50 per mille of each frozen key block and
                                  value block kept exactly (see the layout
-                                 below); needs bits 2..4, group a multiple of
-                                 32 and, at 3 bits, head_dim 128.  Decode and
-                                 the fused step add the corrections; the
-                                 multi-query attention refuses such a cache */
+                                 below); needs bits 2..4 and group a multiple
+                                 of 32.  Decode, the fused step and the
+                                 multi-query attention add the corrections */
   int32_t reserved;           /* 0 */
   double rope_base;           /* 0: keys arrive rotated (post-RoPE, or no
                                  RoPE).  > 1 (at most 1e7): pre-RoPE keys
@@ -193,6 +190,18 @@ int kivi_cache_restore(const kivi_params* params, void* d_arena, size_t arena_by
  * unchanged (launches it made before stay made).  0 disarms.  Nothing is
  * injected on the device.  Errors: EINVAL (n < 0). */
 int kivi_debug_inject_launch_failure(int64_t n);
+
+/* Host-side control of the decode's bounded copy waits, for tests of the
+ * error path (the method's pages have no counterpart).  Every decode warp
+ * waits at most this long for each of its copies into shared memory; when a
+ * wait runs out the warp stops consuming, lets the copies it issued land
+ * (those waits keep the 2 s bound), and sets bit 0 of the cache's error word
+ * (kivi_read_error), so the call's outputs are invalid but the launch ends.
+ * ns >= 1 sets the limit for launches made from now on, in any handle of
+ * the process; 0 restores the default of 2 s.  A limit of a few nanoseconds
+ * makes waits run out while the copies are still in flight.
+ * Errors: EINVAL (ns < 0). */
+int kivi_debug_set_wait_limit(int64_t ns);
 
 /* Frees the host handle.  The arena stays the caller's. */
 void kivi_cache_destroy(kivi_cache* cache);
@@ -299,9 +308,8 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  * oldest part of its first queries' windows).  The newest query's row equals
  * kivi_decode_attn's output for it.  Work: as kivi_decode_attn with n_queries
  * times the query rows per kv head, each row masked to its own positions.
- * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, a bit-stream width
- * at head dim 64, or a cache with outlier tables), EALIGN, ENOSPC (scratch
- * too small), ECUDA. */
+ * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, or a cache of
+ * pre-RoPE keys), EALIGN, ENOSPC (scratch too small), ECUDA. */
 int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream);
 
@@ -328,11 +336,13 @@ size_t kivi_prefill_scratch_bytes(const kivi_cache* cache, int64_t n_queries);
 int64_t kivi_prefill_bytes(const kivi_cache* cache, int64_t n_queries);
 
 /* Reads and clears the device error word that the cache's attention launches
- * set instead of hanging: bit 0 = a bulk copy into shared memory did not
- * complete within its bounded wait (2 s), bit 1 = a warp waited in vain for
- * its combine slot to be released.  Either bit means the affected outputs are
- * not valid.  Unlike every other call this one synchronises `stream` (it
- * returns the value).  Errors: ENULL, ECUDA. */
+ * (kivi_decode_attn, kivi_append_decode_attn, kivi_prefill_attn and
+ * kivi_decode_attn_noalloc, with their variants) set instead of hanging:
+ * bit 0 = a bulk copy into shared memory did not complete within its bounded
+ * wait (2 s, or the limit of kivi_debug_set_wait_limit), bit 1 = a warp
+ * waited in vain for its combine slot to be released.  Either bit means the
+ * affected outputs are not valid.  Unlike every other call this one
+ * synchronises `stream` (it returns the value).  Errors: ENULL, ECUDA. */
 int kivi_read_error(kivi_cache* cache, uint32_t* flags, void* cuda_stream);
 
 /* Decode attention that allocates nothing (the method's pages have no
@@ -352,6 +362,8 @@ int kivi_read_error(kivi_cache* cache, uint32_t* flags, void* cuda_stream);
  *   - All calls share the array: calls whose GPU work overlaps (concurrent
  *     streams or host threads) race on it.  The merge counters in it are
  *     cleared by every call.
+ *   - The bounded waits report into the cache's own error word, which lives
+ *     in the arena the caller already owns: read it with kivi_read_error.
  *   - Three partial records per query head, 3 * B * h_q * (head_dim + 4) * 4
  *     bytes, plus the merge counters must fit in 4 MiB, else KIVI_ESCRATCH and
  *     nothing runs; the work is spread over fewer CTAs when fewer records fit.

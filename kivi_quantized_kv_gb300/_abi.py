@@ -17,6 +17,7 @@ KIVI_OK, KIVI_EINVAL, KIVI_EALIGN, KIVI_ECAPACITY, KIVI_ENOSPC, KIVI_ECUDA, KIVI
 EXPORTS = (
     "kivi_cache_bytes", "kivi_cache_create", "kivi_cache_destroy", "kivi_append", "kivi_append_ragged",
     "kivi_cache_tokens", "kivi_prefill_attn_ragged", "kivi_cache_restore", "kivi_debug_inject_launch_failure",
+    "kivi_debug_set_wait_limit",
     "kivi_decode_attn", "kivi_append_decode_attn", "kivi_append_decode_attn_host", "kivi_decode_attn_host",
     "kivi_decode_attn_noalloc", "kivi_prefill_attn", "kivi_prefill_scratch_bytes", "kivi_prefill_bytes",
     "kivi_read_error", "kivi_set_num_splits", "kivi_cache_layout", "kivi_layout_for",
@@ -73,6 +74,7 @@ def lib():
         "kivi_cache_tokens": (ctypes.c_int, [vp, P(i64)]),
         "kivi_cache_restore": (ctypes.c_int, [P(KiviParams), vp, ctypes.c_size_t, P(i64), vp, P(vp)]),
         "kivi_debug_inject_launch_failure": (ctypes.c_int, [i64]),
+        "kivi_debug_set_wait_limit": (ctypes.c_int, [i64]),
         "kivi_prefill_attn_ragged": (ctypes.c_int, [vp, vp, vp, P(i64), i64, vp, ctypes.c_size_t, vp]),
         "kivi_decode_attn": (ctypes.c_int, [vp, vp, vp, vp]),
         "kivi_append_decode_attn": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),

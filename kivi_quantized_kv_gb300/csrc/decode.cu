@@ -23,6 +23,8 @@ DecodeShape decode_shape(const Geo& g) {
   const int64_t xch_bytes = ch == 32 ? 512 : 256;
   // with outlier tables: the [4][CH] p exchange and the [4][d] fp32 value corrections
   const int64_t corr_bytes = g.n_out > 0 ? 16 * (ch + g.d) : 0;
+  // pre-RoPE keys: the angle row of the current group or tail chunk (mma::Rope)
+  const int64_t rope_bytes = g.rope_l2b != 0.0 ? (g.d / 2 + 8) * 8 : 0;
   // shared memory of one CTA: the SM's 228 KB shared by kDecodeCtasPerSm
   // CTAs, less the 1 KB the driver reserves per CTA and room for the static
   // shared memory, and at most the 227 KB one CTA may have
@@ -30,7 +32,7 @@ DecodeShape decode_shape(const Geo& g) {
   if (budget > 227 * 1024 - 512) budget = 227 * 1024 - 512;
   auto per_warp_of = [&](int stages) {
     return static_cast<int64_t>(stages) * sh.stage_bytes + q_bytes + slot_bytes + xch_bytes + corr_bytes +
-           12 * stages;
+           rope_bytes + 12 * stages;
   };
   // as many warps (up to kDecodeWarps) as fit with two copy stages each, then
   // more stages (up to four) while they fit; very large group blocks get a
@@ -53,6 +55,7 @@ int decode_ctas_per_sm(const Geo& g) {
   const DecodeShape sh = decode_shape(g);
   const int threads = sh.nw * 32;
   const int smem = decode_smem(sh, g.split_stride);
+  if (g.rope_l2b != 0.0) return mma::occupancy_rope_b(g.bits, g, threads, smem);
   if (g.n_out > 0) return mma::occupancy_outl_b(g.bits, g, threads, smem);
   if (g.bits == 2) return mma::occupancy_b2(g, threads, smem);
   if (g.bits == 4) return mma::occupancy_b4(g, threads, smem);
@@ -73,6 +76,7 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
   a.partials = partials;
   a.counters = counters;
   a.error = error;
+  a.wait_ns = copy_wait_ns();
   a.plan = plan;
   a.ns = sh.ns;
   a.stage_bytes = sh.stage_bytes;
@@ -104,6 +108,7 @@ cudaError_t launch_decode_scratch(const Geo& g, const uint8_t* arena, const __ha
   if (injected_launch_failure()) return cudaErrorLaunchFailure;
   const int threads = sh.nw * 32;
   const int smem = decode_smem(sh, stride);
+  if (g.rope_l2b != 0.0) return mma::launch_rope_b(g.bits, a, grid, threads, smem, stream);
   if (g.n_out > 0) return mma::launch_outl_b(g.bits, a, grid, threads, smem, stream);
   if (g.bits == 2) return mma::launch_b2(a, grid, threads, smem, stream);
   if (g.bits == 4) return mma::launch_b4(a, grid, threads, smem, stream);
@@ -124,6 +129,7 @@ cudaError_t launch_decode_ragged(const Geo& g, const uint8_t* arena, const __hal
   a.partials = partials;
   a.counters = counters;
   a.error = error;
+  a.wait_ns = copy_wait_ns();
   a.plan = plan;
   a.plan.nq = 1;
   a.plan.q_rows = 1;
@@ -148,6 +154,7 @@ cudaError_t launch_decode_ragged(const Geo& g, const uint8_t* arena, const __hal
   if (injected_launch_failure()) return cudaErrorLaunchFailure;
   const int threads = sh.nw * 32;
   const int smem = decode_smem(sh, stride);
+  if (g.rope_l2b != 0.0) return mma::launch_rg_rope_b(g.bits, a, runs, grid, threads, smem, stream);
   if (g.n_out > 0) return mma::launch_rg_outl_b(g.bits, a, runs, grid, threads, smem, stream);
   if (g.bits == 2) return mma::launch_rg_b2(a, runs, grid, threads, smem, stream);
   if (g.bits == 4) return mma::launch_rg_b4(a, runs, grid, threads, smem, stream);

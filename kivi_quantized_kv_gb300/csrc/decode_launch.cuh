@@ -10,13 +10,13 @@ namespace kivi {
 namespace mma {
 
 // the kernel of an instantiation
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
 constexpr auto kernel_of() {
-  if constexpr (RG) return decode_mma_ragged_kernel<D, BITS, CH, MQ, OUTL>;
-  else return decode_mma_kernel<D, BITS, CH, MQ, false, OUTL>;
+  if constexpr (RG) return decode_mma_ragged_kernel<D, BITS, CH, MQ, OUTL, ROPE>;
+  else return decode_mma_kernel<D, BITS, CH, MQ, false, OUTL, ROPE>;
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
 cudaError_t prepare() {
   // opt in to the largest dynamic shared memory once per instantiation
   static std::atomic<int> done{0};
@@ -27,18 +27,18 @@ cudaError_t prepare() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, kernel_of<D, BITS, CH, MQ, RG, OUTL>());
+  e = cudaFuncGetAttributes(&fa, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>());
   if (e != cudaSuccess) return e;
   // the opt-in limit covers static + dynamic shared memory
-  e = cudaFuncSetAttribute(kernel_of<D, BITS, CH, MQ, RG, OUTL>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            optin - static_cast<int>(fa.sharedSizeBytes));
   if (e == cudaSuccess) done.store(1, std::memory_order_release);
   return e;
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
 cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
-  cudaError_t e = prepare<D, BITS, CH, MQ, RG, OUTL>();
+  cudaError_t e = prepare<D, BITS, CH, MQ, RG, OUTL, ROPE>();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the CTAs may start (and set up their
   // shared memory) while the previous kernel in the stream drains; the kernel
@@ -53,17 +53,18 @@ cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int th
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if constexpr (RG) e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL>(), a, rt);
-  else e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL>(), a);
+  if constexpr (RG) e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>(), a, rt);
+  else e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>(), a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
 int occupancy_one(int threads, int smem) {
-  if (prepare<D, BITS, CH, MQ, RG, OUTL>() != cudaSuccess) return 1;
+  if (prepare<D, BITS, CH, MQ, RG, OUTL, ROPE>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_of<D, BITS, CH, MQ, RG, OUTL>(), threads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>(), threads, smem) !=
+      cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }
@@ -80,12 +81,14 @@ cudaError_t launch_mq(const Args& a, const RunTableT<RG>& rt, dim3 grid, int thr
               : launch_one<128, BITS, 16, MQ, RG>(a, rt, grid, threads, smem, s);
 }
 
-// bit-stream widths: head dim 128 and 32-token chunks only (a lane's quarter
-// of a key row, and its 8 codes of a value row, start on 32-bit words)
+// bit-stream widths: 32-token chunks only (a lane's 8 codes of a value row
+// start on a 32-bit word); at head dim 64 a lane's quarter of a key row may
+// start on a 16-bit boundary, which the kernel aligns
 template <int BITS, bool MQ, bool RG>
 cudaError_t launch_stream(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
-  if (a.g.d != 128 || (a.g.G % 32) != 0) return cudaErrorInvalidValue;
-  return launch_one<128, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s);
+  if ((a.g.G % 32) != 0) return cudaErrorInvalidValue;
+  return a.g.d == 64 ? launch_one<64, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s)
+                     : launch_one<128, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s);
 }
 
 template <int BITS>
@@ -113,7 +116,8 @@ cudaError_t launch_bits_ragged(const Args& a, const RunTable& rt, dim3 grid, int
 template <int BITS>
 int occupancy_bits(const Geo& g, int threads, int smem) {
   if constexpr (stream_bits<BITS>()) {
-    return occupancy_one<128, BITS, 32, false, false>(threads, smem);
+    return g.d == 64 ? occupancy_one<64, BITS, 32, false, false>(threads, smem)
+                     : occupancy_one<128, BITS, 32, false, false>(threads, smem);
   } else {
     const bool ch32 = (g.G % 32) == 0;
     if (g.d == 64)
@@ -123,6 +127,35 @@ int occupancy_bits(const Geo& g, int threads, int smem) {
                 : occupancy_one<128, BITS, 16, false, false>(threads, smem);
   }
 }
+
+// pre-RoPE keys (decode_rope_b*.cu): every width, 32-token chunks (G 32 or
+// 64), head dims 64 and 128; one or several query tokens, uniform or ragged
+template <int BITS, bool MQ, bool RG>
+cudaError_t launch_rope_mq(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
+  if ((a.g.G % 32) != 0) return cudaErrorInvalidValue;
+  return a.g.d == 64 ? launch_one<64, BITS, 32, MQ, RG, false, true>(a, rt, grid, threads, smem, s)
+                     : launch_one<128, BITS, 32, MQ, RG, false, true>(a, rt, grid, threads, smem, s);
+}
+template <int BITS>
+cudaError_t launch_rope_bits(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s) {
+  const NoRuns none{0};
+  return a.plan.q_rows > 1 ? launch_rope_mq<BITS, true, false>(a, none, grid, threads, smem, s)
+                           : launch_rope_mq<BITS, false, false>(a, none, grid, threads, smem, s);
+}
+template <int BITS>
+cudaError_t launch_rope_bits_ragged(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
+                                    cudaStream_t s) {
+  return launch_rope_mq<BITS, false, true>(a, rt, grid, threads, smem, s);
+}
+template <int BITS>
+int occupancy_rope_bits(const Geo& g, int threads, int smem) {
+  return g.d == 64 ? occupancy_one<64, BITS, 32, false, false, false, true>(threads, smem)
+                   : occupancy_one<128, BITS, 32, false, false, false, true>(threads, smem);
+}
+cudaError_t launch_rope_b(int bits, const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
+cudaError_t launch_rg_rope_b(int bits, const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
+                             cudaStream_t s);
+int occupancy_rope_b(int bits, const Geo& g, int threads, int smem);
 
 // defined in decode_b2.cu, decode_b4.cu, decode_b8.cu
 cudaError_t launch_b2(const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
@@ -138,7 +171,7 @@ cudaError_t launch_rg_stream_b(int bits, const Args& a, const RunTable& rt, dim3
 int occupancy_stream_b(int bits, const Geo& g, int threads, int smem);
 int occupancy_b2(const Geo& g, int threads, int smem);
 // with outlier tables (decode_outl.cu): 2 to 4 bits, 32-token chunks, one
-// query token per sequence
+// or (uniform launches) several query tokens per sequence
 cudaError_t launch_outl_b(int bits, const Args& a, dim3 grid, int threads, int smem, cudaStream_t s);
 cudaError_t launch_rg_outl_b(int bits, const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
                              cudaStream_t s);

@@ -98,6 +98,7 @@ struct Args {
   float* partials;      // [B * nq * h_q][stride][d + 4]: o[d], m, l, 2 pad
   unsigned* counters;   // [units]: CTAs finished per unit
   unsigned* error;      // kErrCopy | kErrSlot
+  unsigned long long wait_ns;   // how long a warp waits for a copy before it gives up (kErrCopy)
   DecodePlan plan;
   int32_t ns;           // copy stages per warp
   int32_t stage_bytes;  // bytes per stage (block bytes rounded up to 128)
@@ -195,14 +196,27 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Waits for a barrier phase, suspended rather than spinning (a spinning warp
-// would take issue slots from the warps that compute); gives up after
-// kWaitNs and reports false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// would take issue slots from the warps that compute); gives up once the wait
+// has lasted `limit_ns` and reports false.
+// A limit of 1 ns gives up at once unless the phase is already complete (a
+// test of the expiry path: the copies still arrive, and the try_wait forms
+// may suspend the thread until they do).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (limit_ns <= 1) return mbar_test_wait(bar, parity);
+  if (limit_ns >= kWaitNs && mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
   const unsigned long long t0 = global_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+    if (global_ns() - t0 >= limit_ns) return false;
   }
 }
 
@@ -599,18 +613,315 @@ __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, 
   if (threadIdx.x == 0) a.counters[u] = 0u;
 }
 
+// Scores of one chunk (CH tokens) for the lane's head c: lane (r, c) gets
+// the tokens TPL r + i of the chunk, rowa / rowb the shared addresses of its
+// first key-row pair (odd r of 64-byte rows swapped: sw).  bq holds the folded
+// query of the lane's B column, scs the scale of the accumulated codes, cst_h
+// the head's Σ q_c min_c.
+// Words of a lane's key quarter: whole words, except a bit-stream quarter
+// of 2 b bytes at head dim 64 for odd b (it may start on a 16-bit boundary:
+// one word more, shifted down by ksh bits).
+template <int D, int BITS>
+__host__ __device__ constexpr bool key_quarter_unaligned() { return stream_bits<BITS>() && (D * BITS / 32) % 4 != 0; }
+template <int D, int BITS>
+__host__ __device__ constexpr int key_quarter_words() {
+  return key_quarter_unaligned<D, BITS>() ? (D * BITS / 32 + 2 + 3) / 4 : (D * BITS / 8) / 16;
+}
+
+template <int D, int BITS, int CH>
+__device__ __forceinline__ void chunk_scores(const uint32_t (&bq)[D / 8], uint32_t rowa, uint32_t rowb, float scs,
+                                             float cst_h, int sw, int ksh, float (&sv)[CH / 8]) {
+  constexpr int RK = D * BITS / 8, KW = key_quarter_words<D, BITS>(), NP = D / 8, NKC = D / 16, TPL = CH / 8;
+  constexpr int NA = n_acc<BITS>();
+#pragma unroll
+  for (int v2 = 0; v2 < TPL / 2; ++v2) {
+    uint32_t w0[KW], w1[KW];
+    const uint32_t row0 = rowa + 2 * v2 * RK;
+    const uint32_t row1 = rowb + 2 * v2 * RK;
+    if constexpr (key_quarter_unaligned<D, BITS>()) {   // from the 4-byte boundary below, shifted down
+#pragma unroll
+      for (int i = 0; i < KW; ++i) {
+        w0[i] = lds32(row0 + 4 * i);
+        w1[i] = lds32(row1 + 4 * i);
+      }
+#pragma unroll
+      for (int i = 0; i < KW; ++i) {
+        w0[i] = i + 1 < KW ? __funnelshift_r(w0[i], w0[i + 1], ksh) : (w0[i] >> ksh);
+        w1[i] = i + 1 < KW ? __funnelshift_r(w1[i], w1[i + 1], ksh) : (w1[i] >> ksh);
+      }
+    } else if constexpr (stream_bits<BITS>()) {   // a quarter of b words, 4-byte aligned
+#pragma unroll
+      for (int i = 0; i < KW; ++i) {
+        w0[i] = lds32(row0 + 4 * i);
+        w1[i] = lds32(row1 + 4 * i);
+      }
+    } else if constexpr (KW >= 4) {
+#pragma unroll
+      for (int i = 0; i < KW; i += 4) {
+        const uint4 x = lds128(row0 + 4 * i);
+        const uint4 y = lds128(row1 + 4 * i);
+        w0[i] = x.x; w0[i + 1] = x.y; w0[i + 2] = x.z; w0[i + 3] = x.w;
+        w1[i] = y.x; w1[i + 1] = y.y; w1[i + 2] = y.z; w1[i + 3] = y.w;
+      }
+    } else if constexpr (KW == 2) {
+      const uint2 x = lds64(row0);
+      const uint2 y = lds64(row1);
+      w0[0] = x.x; w0[1] = x.y; w1[0] = y.x; w1[1] = y.y;
+    } else {
+      w0[0] = lds32(row0);
+      w1[0] = lds32(row1);
+    }
+    float acc[NA][4];
+#pragma unroll
+    for (int i = 0; i < NA; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < NKC; ++j) {
+      const int pa = ord_pair<BITS, NP>(2 * j), pb = ord_pair<BITS, NP>(2 * j + 1);
+      mma16816(acc[acc_of<BITS, NP>(j)], code_pair<BITS>(w0, pa), code_pair<BITS>(w1, pa),
+               code_pair<BITS>(w0, pb), code_pair<BITS>(w1, pb), bq[pa], bq[pb]);
+    }
+    float s_a = (acc[0][0] + acc[0][1]) * acc_scale<BITS>(0);
+    float s_b = (acc[0][2] + acc[0][3]) * acc_scale<BITS>(0);
+#pragma unroll
+    for (int i = 1; i < NA; ++i) {
+      s_a = fmaf(acc[i][0] + acc[i][1], acc_scale<BITS>(i), s_a);
+      s_b = fmaf(acc[i][2] + acc[i][3], acc_scale<BITS>(i), s_b);
+    }
+    s_a = fmaf(s_a, scs, cst_h);
+    s_b = fmaf(s_b, scs, cst_h);
+    sv[2 * v2] = sw ? s_b : s_a;
+    sv[2 * v2 + 1] = sw ? s_a : s_b;
+  }
+}
+
+// ---------------------------------------------------------- pre-RoPE keys
+// Keys stored before the rotary embedding (KV-cache quantization guide
+// (pigeon), "KVQuant adds").  The score of the key at position a is
+// q · R(a θ) k̂_a.  With a = a0 + j (a0 the first position of a frozen group
+// or a tail chunk, j < G), R(a θ) = R(a0 θ) R(j θ) and R is orthogonal, so
+//   q · R(a θ) k̂ = (R(-a0 θ) q) · (R(j θ) k̂):
+// the query rows are turned back by the base angle once per group (the B
+// operand, split into hi/lo fp16 halves as the folded query of the plain
+// decode), and each dequantized key is turned by its offset's angle, taken
+// from a fixed table (rope.cu), in fp32 and split into hi/lo fp16 A
+// operands, so both factors of every product are exact to 22 bits.  The score
+// k-chunk kc pairs each channel with its rotation partner: k = 2c + e is
+// channel RS c + 2 kc + e of the first half and k = 8 + 2c + e the same channel
+// of the second half (RS = D/8), so lane (r, c) holds both channels of each
+// pair it turns and reads two contiguous RS-channel regions of a key row.
+//
+// cos and sin of a θ by the Cody-Waite reduction (W. J. Cody and W. Waite,
+// "Software Manual for the Elementary Functions", 1980): θ is carried as
+// th_hi + th_lo, a th_hi is split exactly into p + e with one fma, the
+// multiple k of 2π nearest to a θ is taken off p with 2π in two fp32 parts
+// (k times the first part is exact in the fma), then the small terms are
+// added.  Positions from 2^24 on, which fp32 does not hold exactly, reduce in
+// double.
+constexpr float kInv2Pi = 0.15915494309189535f;
+constexpr float kTwoPiHi = 6.28318548202514648f;      // fl(2π)
+constexpr float kTwoPiLo = -1.7484555314695172e-7f;   // 2π - fl(2π)
+__device__ __forceinline__ float2 h2f(uint32_t x) { return __half22float2(*reinterpret_cast<const __half2*>(&x)); }
+
+__device__ __forceinline__ float2 rope_cs(int64_t a, float th_hi, float th_lo) {
+  float r;
+  if (a < (int64_t{1} << 24)) {
+    const float af = static_cast<float>(a);
+    const float p = af * th_hi;
+    const float e = fmaf(af, th_hi, -p);
+    const float t = fmaf(af, th_lo, e);
+    const float k = rintf((p + t) * kInv2Pi);
+    r = fmaf(-k, kTwoPiHi, p);
+    r = fmaf(-k, kTwoPiLo, r) + t;
+  } else {
+    const double x = static_cast<double>(a) * (static_cast<double>(th_hi) + static_cast<double>(th_lo));
+    r = static_cast<float>(x - 6.283185307179586476925 * rint(x * 0.15915494309189533576888));
+  }
+  float sn, cs;
+  __sincosf(r, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+template <int D>
+struct Rope {
+  static constexpr int kRS = D / 8;                  // channels of a lane's region per half
+  static constexpr int kRowBytes = (D / 2 + 8) * 8;  // a warp's angle row: (cos, sin) per pair, regions 16 B apart
+  static constexpr int kQRow = 2 * D + 4;            // query rows in natural order, 4 bytes of padding
+  __host__ __device__ static constexpr int idx(int i) { return i + 2 * (i / kRS); }
+};
+
+// The warp's angle row for base position a: (cos, sin)(a θ_i), i < D/2.
+// tab: the RoPE tables ([θ hi, lo] per pair first).
+template <int D>
+__device__ __forceinline__ void rope_angles(float2* wrow, const float* __restrict__ tab, int64_t a) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = lane; i < D / 2; i += 32) {
+    const float2 th = __ldg(reinterpret_cast<const float2*>(tab) + i);
+    wrow[Rope<D>::idx(i)] = rope_cs(a, th.x, th.y);
+  }
+  __syncwarp();
+}
+
+// fp16 pair of x0, x1: their high parts (11 significant bits, exact in fp16)
+// or the rest
+__device__ __forceinline__ uint32_t rope_split(float x0, float x1, bool lo) {
+  const float h0 = __uint_as_float(__float_as_uint(x0) & 0xFFFFE000u);
+  const float h1 = __uint_as_float(__float_as_uint(x1) & 0xFFFFE000u);
+  return lo ? pack_half2(x0 - h0, x1 - h1) : pack_half2(h0, h1);
+}
+
+// B fragment pair of R(-a0 θ) q for the lane's column and k-chunk kc (made
+// when needed rather than kept live): query row at qrow_s (natural order),
+// part lo (odd column) or hi; the warp's angle row at wrow_s.
+template <int D>
+__device__ __forceinline__ void rope_fold_kc(uint32_t& b0, uint32_t& b1, int kc, uint32_t qrow_s, uint32_t wrow_s,
+                                             int c, bool lo) {
+  constexpr int RS = Rope<D>::kRS, H = D / 2;
+  const int i = RS * c + 2 * kc;
+  const float2 qa = h2f(lds32(qrow_s + 2 * i));
+  const float2 qb = h2f(lds32(qrow_s + 2 * (i + H)));
+  const uint4 w = lds128(wrow_s + 8 * Rope<D>::idx(i));   // (cos, sin) of pairs i and i + 1
+  const float c0 = __uint_as_float(w.x), s0 = __uint_as_float(w.y);
+  const float c1 = __uint_as_float(w.z), s1 = __uint_as_float(w.w);
+  // R(-φ) (x, y) = (c x + s y, c y - s x)
+  b0 = rope_split(fmaf(c0, qa.x, s0 * qb.x), fmaf(c1, qa.y, s1 * qb.y), lo);
+  b1 = rope_split(fmaf(c0, qb.x, -s0 * qa.x), fmaf(c1, qb.y, -s1 * qa.y), lo);
+}
+
+// Codes of a lane's key region: NW words from the 4-byte boundary at or below
+// its first code, shifted so that the region starts at bit 0.  Word rule: a
+// region is whole words, except 16 channels of 2 bits (head dim 64), whose
+// codes sit in bits 8..15 of both halves of their word for odd c; bit streams:
+// RS b bits from bit RS c b.
+template <int D, int BITS>
+struct RopeCodes {
+  static constexpr int RS = Rope<D>::kRS;
+  static constexpr bool kStream = stream_bits<BITS>();
+  static constexpr int NW = kStream ? (RS * BITS + 24 + 31) / 32 : (RS * BITS >= 32 ? RS * BITS / 32 : 1);
+  static constexpr int kHalfBytes = (D / 2) * BITS / 8;   // the second half's region is this far on
+  // byte offset of the region's first word and the shift inside it, for c
+  __device__ static void where(int c, uint32_t& off, int& sh) {
+    const int bit = RS * c * BITS;
+    off = static_cast<uint32_t>(bit >> 5) * 4u;
+    sh = kStream ? (bit & 31) : ((bit & 31) >> 1);
+  }
+  __device__ static void load(uint32_t (&w)[NW], uint32_t addr, int sh) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = lds32(addr + 4 * i);
+    if constexpr (kStream) {
+#pragma unroll
+      for (int i = 0; i < NW; ++i) w[i] = i + 1 < NW ? __funnelshift_r(w[i], w[i + 1], sh) : (w[i] >> sh);
+    } else if constexpr (RS * BITS < 32) {
+      w[0] >>= sh;   // bits crossing from the high half into the low one are masked off below
+    }
+  }
+  // the two codes of local pair k (channels RS c + 2k, + 1) as floats
+  __device__ static void pair(const uint32_t (&w)[NW], int k, float& f0, float& f1) {
+    constexpr uint32_t M = (1u << BITS) - 1u;
+    uint32_t lo, hi;
+    if constexpr (kStream) {
+      const int bit = 2 * BITS * k, wi = bit >> 5, s = bit & 31;
+      const uint32_t t = (s + 2 * BITS <= 32 || wi + 1 >= NW) ? (w[wi] >> s) : __funnelshift_r(w[wi], w[wi + 1], s);
+      lo = t & M;
+      hi = (t >> BITS) & M;
+    } else {
+      constexpr int PPW = 16 / BITS;   // pairs per word
+      const uint32_t x = (w[k / PPW] >> (BITS * (k % PPW))) & (M * 0x00010001u);
+      lo = x & 0xFFFFu;
+      hi = x >> 16;
+    }
+    // 2^23 + code, then 2^23 off: exact
+    f0 = __uint_as_float(0x4B000000u | lo) - 8388608.f;
+    f1 = __uint_as_float(0x4B000000u | hi) - 8388608.f;
+  }
+};
+
+// Scores of a frozen group's chunk (CH tokens from s0) for pre-RoPE keys:
+// lane (r, c) gets head c's scores of tokens s0 + TPL r + i, the same layout as
+// chunk_scores.  kq, ks: shared addresses of the block's key codes and key
+// (Δ, min) rows; otab: the offset table; scs: the score scale.
+template <int D, int BITS, int CH>
+__device__ __forceinline__ void rope_chunk_scores(uint32_t qrow_s, uint32_t wrow_s, uint32_t kq, uint32_t ks, int s0,
+                                                  int sw, const float2* __restrict__ otab, int G, float scs,
+                                                  float (&sv)[CH / 8]) {
+  using RC = RopeCodes<D, BITS>;
+  constexpr int RS = Rope<D>::kRS, H = D / 2, TPL = CH / 8, NT = TPL / 2, RK = D * BITS / 8, NW = RC::NW;
+  const int lane = threadIdx.x & 31, r = lane >> 2, c = lane & 3;
+  uint32_t roff;
+  int rsh;
+  RC::where(c, roff, rsh);
+  // the code regions of the lane's tokens: tile v2, token e (A row r or r + 8), half
+  uint32_t w[NT][2][2][NW];
+#pragma unroll
+  for (int v2 = 0; v2 < NT; ++v2) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t row = kq + static_cast<uint32_t>((s0 + TPL * r + 2 * v2 + (e ^ sw)) * RK) + roff;
+      RC::load(w[v2][e][0], row, rsh);
+      RC::load(w[v2][e][1], row + RC::kHalfBytes, rsh);
+    }
+  }
+  float acc[NT][4];
+#pragma unroll
+  for (int v2 = 0; v2 < NT; ++v2) acc[v2][0] = acc[v2][1] = acc[v2][2] = acc[v2][3] = 0.f;
+#pragma unroll
+  for (int kc = 0; kc < D / 16; ++kc) {
+    const int i = RS * c + 2 * kc;
+    uint32_t b0, b1;
+    rope_fold_kc<D>(b0, b1, kc, qrow_s, wrow_s, c, (r & 1) != 0);
+    const float2 da = h2f(lds32(ks + 2 * i));
+    const float2 db = h2f(lds32(ks + 2 * (i + H)));
+    const float2 ma = h2f(lds32(ks + 2 * D + 2 * i));
+    const float2 mb = h2f(lds32(ks + 2 * D + 2 * (i + H)));
+#pragma unroll
+    for (int v2 = 0; v2 < NT; ++v2) {
+      uint32_t ah[4], al[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = s0 + TPL * r + 2 * v2 + (e ^ sw);   // the token's offset in its group
+        float x0, x1, y0, y1;
+        RC::pair(w[v2][e][0], kc, x0, x1);
+        RC::pair(w[v2][e][1], kc, y0, y1);
+        x0 = fmaf(x0, da.x, ma.x); x1 = fmaf(x1, da.y, ma.y);
+        y0 = fmaf(y0, db.x, mb.x); y1 = fmaf(y1, db.y, mb.y);
+        const float2 r0 = __ldg(otab + i * (G + 1) + j), r1 = __ldg(otab + (i + 1) * (G + 1) + j);
+        // R(φ) (x, y) = (c x - s y, s x + c y), halved by the table
+        const float u0 = fmaf(r0.x, x0, -r0.y * y0), v0 = fmaf(r0.y, x0, r0.x * y0);
+        const float u1 = fmaf(r1.x, x1, -r1.y * y1), v1 = fmaf(r1.y, x1, r1.x * y1);
+        ah[e] = rope_split(u0, u1, false);
+        al[e] = rope_split(u0, u1, true);
+        ah[2 + e] = rope_split(v0, v1, false);
+        al[2 + e] = rope_split(v0, v1, true);
+      }
+      mma16816(acc[v2], ah[0], ah[1], ah[2], ah[3], b0, b1);
+      mma16816(acc[v2], al[0], al[1], al[2], al[3], b0, b1);
+    }
+  }
+#pragma unroll
+  for (int v2 = 0; v2 < NT; ++v2) {
+    const float s_a = (acc[v2][0] + acc[v2][1]) * scs, s_b = (acc[v2][2] + acc[v2][3]) * scs;
+    sv[2 * v2] = sw ? s_b : s_a;
+    sv[2 * v2 + 1] = sw ? s_a : s_b;
+  }
+}
+
 template <bool RG>
 using RunTableT = typename std::conditional<RG, RunTable, NoRuns>::type;
 
 // The kernel body.  RG: a ragged launch; per-unit plan values come from the
-// run table `rt` (the unit's run) instead of the launch's plan.
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL>
+// run table `rt` (the unit's run) instead of the launch's plan.  ROPE: keys
+// stored before the rotary embedding, turned at their positions in the score
+// products (see rope_chunk_scores).
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL, bool ROPE>
 __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& rt) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   using WS = WarpSmem<D, CH>;
   // outlier corrections (OUTL): per warp a [4][CH] fp32 exchange of the
   // chunk's p and the [4][D] fp32 value corrections
   constexpr int kCorr = OUTL ? 16 * (CH + D) : 0;
+  // pre-RoPE keys: per warp the angle row of the current group or tail chunk
+  constexpr int kRopeRow = ROPE ? Rope<D>::kRowBytes : 0;
+  static_assert(!(ROPE && OUTL), "pre-RoPE keys take no outlier tables");
   constexpr int RK = D * BITS / 8;          // key row bytes
   constexpr int KW = RK / 16;               // 32-bit words of a lane's key quarter
   constexpr int QD = D / 4;                 // channels of a lane's quarter
@@ -673,11 +984,14 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   float* slots = reinterpret_cast<float*>(q_all + nw * WS::kQ);
   uint8_t* xch_all = reinterpret_cast<uint8_t*>(slots) + nw * WS::kSlot;
   float* corr_all = reinterpret_cast<float*>(xch_all + nw * WS::kXch);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(corr_all) + nw * kCorr);
+  uint8_t* rope_all = reinterpret_cast<uint8_t*>(corr_all) + nw * kCorr;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rope_all + nw * kRopeRow);
   __shared__ unsigned s_arrive;   // warps signed in for the current combine
   __shared__ unsigned s_done;     // combines completed
   __shared__ unsigned s_flag;     // this CTA merges its last unit
   __shared__ unsigned s_next;     // positions of the CTA's range claimed so far
+  __shared__ float s_qf[kDecodeWarps][4];    // per warp: the query prescale 2^e of each row of the open unit
+  __shared__ float s_vsc[kDecodeWarps][2];   // per warp: the open unit's value scale 2^F (0: not chosen), 2^-F
 
   uint8_t* my_stages = stages + static_cast<size_t>(warp) * a.ns * a.stage_bytes;
   uint8_t* qw = q_all + warp * WS::kQ;
@@ -685,6 +999,10 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   float* pbuf = corr_all + warp * (kCorr / 4);   // [4][CH]: p of (head, token) of the open chunk
   float* ocorr = pbuf + 4 * CH;                  // [4][D], real scale, at the running max
   const uint32_t xw_s = smem_addr(xw);
+  float2* wrow = reinterpret_cast<float2*>(rope_all + warp * kRopeRow);   // pre-RoPE keys: the angle row
+  // pre-RoPE keys: the rotation tables in the arena's workspace (θ, then the
+  // offsets' (cos, sin) / 2), read through the read-only cache
+  const float* rtab = ROPE ? reinterpret_cast<const float*>(a.arena + g.ws_rope) : nullptr;
   const uint32_t bar0 = smem_addr(bars + warp * a.ns);
   int* ring_w = reinterpret_cast<int*>(bars + nw * a.ns) + warp * a.ns;   // this warp's item ring
   const uint32_t blk_bytes = static_cast<uint32_t>(g.block_bytes);
@@ -868,7 +1186,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   // waits for the consumer's current stage; false after an abort
   auto acquire = [&]() -> bool {
     if (aborted) return false;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * c_st, c_ph));   // warp-uniform verdict
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * c_st, c_ph, a.wait_ns));   // warp-uniform verdict
     if (!ok) {
       aborted = true;
       if (lane == 0) atomicOr(a.error, kErrCopy);
@@ -886,20 +1204,26 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   const int hh_col = r >> 1;
   // P' of score-layout token TPL*r + i enters value pair ((TPL*r + i) % (CH/4)) / 2,
   // whose codes sit at bit k: p is scaled by 2^-k in fp32 before the hi/lo split
-  float vscl[TPL];
-#pragma unroll
-  for (int i = 0; i < TPL; ++i) {
+  auto vscl_at = [&](int i) -> float {
     const int l = (TPL * r + i) % (CH / 4);
     const int kb = stream_bits<BITS>() ? 0 : (BITS * ((l / 2) % (16 / (stream_bits<BITS>() ? 1 : BITS)))) % 8;
-    vscl[i] = __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);
-  }
+    return __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);
+  };
+  float vscl[TPL];
+#pragma unroll
+  for (int i = 0; i < TPL; ++i) vscl[i] = vscl_at(i);
   const float sc_scale = qscale * kTwo24;
 
   // per-lane shared-memory offsets inside a group block (loop invariant)
   constexpr bool kSwap = (RK == 64);   // 64-byte key rows: odd r swaps its row pair
   const int sw = kSwap ? (r & 1) : 0;
-  const uint32_t o_k0 = static_cast<uint32_t>(g.blk_kq) + (TPL * r + sw) * RK + c * (RK / 4);
-  const uint32_t o_k1 = static_cast<uint32_t>(g.blk_kq) + (TPL * r + 1 - sw) * RK + c * (RK / 4);
+  // a lane's quarter of a key row starts at byte c RK/4; at head dim 64 a
+  // bit-stream quarter (2 b bytes) may start on a 16-bit boundary: its words
+  // are read from the 4-byte boundary below and shifted down by ksh bits
+  const uint32_t q_off = static_cast<uint32_t>(c * (RK / 4));
+  const int ksh = static_cast<int>(8 * (q_off & 3u));
+  const uint32_t o_k0 = static_cast<uint32_t>(g.blk_kq) + (TPL * r + sw) * RK + (q_off & ~3u);
+  const uint32_t o_k1 = static_cast<uint32_t>(g.blk_kq) + (TPL * r + 1 - sw) * RK + (q_off & ~3u);
   const uint32_t o_ds = static_cast<uint32_t>(g.blk_ks) + c * (D / 2);   // key Δ; key min at + 2D
   const uint32_t o_vs = static_cast<uint32_t>(g.blk_vs) + TPL * r * 4;   // value (Δ, min) of token TPL*r
   const uint32_t vrow = static_cast<uint32_t>(g.G) * BITS / 8;           // bytes of one value-code row
@@ -935,6 +1259,18 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
     return __half2float(p[ch & 1]);
   };
 
+  // the prescale 2^e of query row c (this lane's score head) of the open unit
+  auto head_qf = [&]() -> float { return s_qf[threadIdx.x >> 5][threadIdx.x & 3]; };
+  // P' = p Δ_t 2^(F - k): a power of two 2^F per unit, chosen from the largest
+  // Δ_t of the warp's first frozen chunk of the unit, keeps the fp16 pair of
+  // P' away from the subnormals when the values are small (the rounding of a
+  // subnormal hi half is not caught by the lo half); the accumulators give
+  // 2^-F back when they turn to real scale.  In the warp's s_vsc: 2^F (0 until chosen), then 2^-F
+  auto value_unscale = [&]() -> float {
+    const float* v = s_vsc[threadIdx.x >> 5];
+    return v[0] == 0.f ? 1.f : v[1];
+  };
+
   // token masks, needed with a window or with several query tokens: this
   // lane's score column c is query row 4 pass + c of the open unit, i.e.
   // query token jq at position hi = q_pos0 + jq, which sees the positions
@@ -958,6 +1294,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
     cslot = static_cast<int>(blockIdx.x) - first;
     res_m = -INFINITY; res_l = 0.f; res_mn = 0.f;
     o_real = false;
+    if (lane == 0) s_vsc[warp][0] = 0.f;   // the unit's value scale: not chosen yet
 #pragma unroll
     for (int i = 0; i < NCT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
     if constexpr (OUTL) {   // this lane's entries: head c, channels 16 ct + r (+ 8)
@@ -994,7 +1331,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
     if (c < nh) {
       float* so = my_slot + c * (D + 4);
       if (r == 0) { so[D] = res_m; so[D + 1] = lh; }
-      const float osc = o_real ? 1.f : kTwo24;
+      const float osc = o_real ? 1.f : kTwo24 * value_unscale();
 #pragma unroll
       for (int ct = 0; ct < NCT; ++ct) {
         so[16 * ct + r] = fmaf(oacc[ct][0] + oacc[ct][1], osc, mh);
@@ -1038,17 +1375,46 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         open_unit(cu);
       }
       // copied to this warp's q area: quarter rows padded by 16 bytes, heads
-      // past nh zero
+      // past nh zero.  A row whose largest |q_c| exceeds 1 is stored scaled by
+      // 2^-e (exact: a power of two) so that its largest |q_c| is below 1;
+      // the folded q_c Δ_c is then at most Δ_c, inside the fp16 range for
+      // every fp16 Δ_c, and the scores take 2^e back (head_qf, kept in the
+      // row's first quarter padding).
       const uint8_t* src = my_stages + c_st * a.stage_bytes;
 #pragma unroll
       for (int kk = lane; kk < 4 * D / 8; kk += 32) {
         const int hh = kk / (D / 8), idx = kk % (D / 8);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (hh < nh) v = *reinterpret_cast<const uint4*>(src + hh * D * 2 + idx * 16);
-        // pairs (0, 1, 2, 3) of the chunk stored as (0, 2, 1, 3): the Σ q·min
-        // MMAs then take their B pairs straight from one 16-byte load
-        *reinterpret_cast<uint4*>(qw + hh * WS::kQRow + (idx / (QD / 8)) * WS::kQS + (idx % (QD / 8)) * 16) =
-            make_uint4(v.x, v.z, v.y, v.w);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vw[j]));
+          m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+#pragma unroll
+        for (int o = 1; o < D / 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));   // the row's chunks
+        int e = 0;
+        if (m > 1.f) frexpf(m, &e);                  // m in [2^(e-1), 2^e): m 2^-e below 1
+        if (e > 0) {
+          // 2^-e as an fp16 pair (e <= 16: a normal number or a subnormal)
+          const uint32_t h = e <= 14 ? static_cast<uint32_t>(15 - e) << 10 : 1u << (24 - e);
+          const uint32_t s2 = h | (h << 16);
+          v.x = hmul2_u(v.x, s2); v.y = hmul2_u(v.y, s2); v.z = hmul2_u(v.z, s2); v.w = hmul2_u(v.w, s2);
+        }
+        if constexpr (ROPE) {
+          // natural channel order, rows 2D + 4 bytes apart (a lane's reads of
+          // its two regions then fall on distinct banks)
+          uint32_t* dq = reinterpret_cast<uint32_t*>(qw + hh * Rope<D>::kQRow + idx * 16);
+          dq[0] = v.x; dq[1] = v.y; dq[2] = v.z; dq[3] = v.w;
+        } else {
+          // pairs (0, 1, 2, 3) of the chunk stored as (0, 2, 1, 3): the Σ q·min
+          // MMAs then take their B pairs straight from one 16-byte load
+          *reinterpret_cast<uint4*>(qw + hh * WS::kQRow + (idx / (QD / 8)) * WS::kQS + (idx % (QD / 8)) * 16) =
+              make_uint4(v.x, v.z, v.y, v.w);
+        }
+        if (idx == 0) s_qf[warp][hh] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
       }
       release();
       __syncwarp();
@@ -1061,6 +1427,16 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
       const int64_t grp = f_gfirst(c_k) + pos;
       const uint32_t blk = stages_s + c_st * a.stage_bytes;   // shared address of the block
 
+      const float qf = head_qf();   // head c's query prescale 2^e
+      const int64_t a_grp = g.S + grp * g.G;
+      uint32_t bq[ROPE ? 1 : NP];
+      float cst_h = 0.f, scs;
+      if constexpr (ROPE) {
+        // the query turned back by the group's base angle a_grp θ (hi/lo
+        // columns); the keys' offsets are turned in rope_chunk_scores
+        rope_angles<D>(wrow, rtab, a_grp);
+        scs = 2.f * qscale * qf;   // the table halves the turned keys
+      } else {
       // (1) the query (natural pair order) and the folded B fragments:
       // hi = fp16(q Δ) in even columns, lo = q Δ - hi in odd ones
       uint32_t q2[NP];   // natural pair order (the q area holds pairs 0, 2, 1, 3 of each 4)
@@ -1069,7 +1445,6 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         const uint4 v = lds128(q_s + 16 * i);
         q2[4 * i] = v.x; q2[4 * i + 1] = v.z; q2[4 * i + 2] = v.y; q2[4 * i + 3] = v.w;
       }
-      uint32_t bq[NP];
 #pragma unroll
       for (int i = 0; i < NP / 4; ++i) {
         const uint4 dv = lds128(blk + o_ds + 16 * i);
@@ -1091,61 +1466,20 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         mma16816(cst_a, mv.x, mv.y, mv.z, mv.w, q2[4 * i], q2[4 * i + 2]);
         mma16816(cst_b, mv.x, mv.y, mv.z, mv.w, q2[4 * i + 1], q2[4 * i + 3]);
       }
-      const float cst_h = (cst_a[0] + cst_b[2]) * qscale;
-      const int64_t a_grp = g.S + grp * g.G;
+      cst_h = (cst_a[0] + cst_b[2]) * (qscale * qf);
+      scs = sc_scale * qf;
+      }
 
       for (int s0 = 0; s0 < g.G; s0 += CH) {
         // (3) scores: lane (r, c) gets head c's scores of tokens s0 + TPL*r + i
         float sv[TPL];
-#pragma unroll
-        for (int v2 = 0; v2 < TPL / 2; ++v2) {
-          uint32_t w0[KW], w1[KW];
-          // 64-byte rows: odd r takes the pair's rows in swapped order so the
-          // two rows of a shared-memory phase fall in different bank halves
-          const uint32_t row0 = blk + o_k0 + (s0 + 2 * v2) * RK;
-          const uint32_t row1 = blk + o_k1 + (s0 + 2 * v2) * RK;
-          if constexpr (kStream) {   // a quarter of b words, 4-byte aligned
-#pragma unroll
-            for (int i = 0; i < KW; ++i) {
-              w0[i] = lds32(row0 + 4 * i);
-              w1[i] = lds32(row1 + 4 * i);
-            }
-          } else if constexpr (KW >= 4) {
-#pragma unroll
-            for (int i = 0; i < KW; i += 4) {
-              const uint4 x = lds128(row0 + 4 * i);
-              const uint4 y = lds128(row1 + 4 * i);
-              w0[i] = x.x; w0[i + 1] = x.y; w0[i + 2] = x.z; w0[i + 3] = x.w;
-              w1[i] = y.x; w1[i + 1] = y.y; w1[i + 2] = y.z; w1[i + 3] = y.w;
-            }
-          } else if constexpr (KW == 2) {
-            const uint2 x = lds64(row0);
-            const uint2 y = lds64(row1);
-            w0[0] = x.x; w0[1] = x.y; w1[0] = y.x; w1[1] = y.y;
-          } else {
-            w0[0] = lds32(row0);
-            w1[0] = lds32(row1);
-          }
-          float acc[NA][4];
-#pragma unroll
-          for (int i = 0; i < NA; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-          for (int j = 0; j < NKC; ++j) {
-            const int pa = ord_pair<BITS, NP>(2 * j), pb = ord_pair<BITS, NP>(2 * j + 1);
-            mma16816(acc[acc_of<BITS, NP>(j)], code_pair<BITS>(w0, pa), code_pair<BITS>(w1, pa),
-                     code_pair<BITS>(w0, pb), code_pair<BITS>(w1, pb), bq[pa], bq[pb]);
-          }
-          float s_a = (acc[0][0] + acc[0][1]) * acc_scale<BITS>(0);
-          float s_b = (acc[0][2] + acc[0][3]) * acc_scale<BITS>(0);
-#pragma unroll
-          for (int i = 1; i < NA; ++i) {
-            s_a = fmaf(acc[i][0] + acc[i][1], acc_scale<BITS>(i), s_a);
-            s_b = fmaf(acc[i][2] + acc[i][3], acc_scale<BITS>(i), s_b);
-          }
-          s_a = fmaf(s_a, sc_scale, cst_h);
-          s_b = fmaf(s_b, sc_scale, cst_h);
-          sv[2 * v2] = sw ? s_b : s_a;
-          sv[2 * v2 + 1] = sw ? s_a : s_b;
+        if constexpr (ROPE) {
+          rope_chunk_scores<D, BITS, CH>(smem_addr(qw + hh_col * Rope<D>::kQRow), smem_addr(wrow),
+                                         blk + static_cast<uint32_t>(g.blk_kq), blk + static_cast<uint32_t>(g.blk_ks),
+                                         s0, sw, reinterpret_cast<const float2*>(rtab + D), g.G, scs, sv);
+        } else {
+          const uint32_t rowa = blk + o_k0 + s0 * RK, rowb = blk + o_k1 + s0 * RK;
+          chunk_scores<D, BITS, CH>(bq, rowa, rowb, scs, cst_h, sw, ksh, sv);
         }
         if constexpr (OUTL) {
           // key outliers of the lane's tokens (rows s0 + TPL r .. of the
@@ -1164,7 +1498,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
             const int i = static_cast<int>(ent & 0xFFu) - t_lo;
             const int ch = static_cast<int>((ent >> 8) & 0xFFu);
             const float ds = (__half2float(__ushort_as_half(static_cast<unsigned short>(ent >> 16))) -
-                              __half2float(kmin[ch])) * (qscale * q_at(c, ch));
+                              __half2float(kmin[ch])) * (qscale * qf * q_at(c, ch));
 #pragma unroll
             for (int j = 0; j < TPL; ++j) sv[j] += (j == i) ? ds : 0.f;
           }
@@ -1213,6 +1547,25 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
             const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
             dm[0] = f0.x; dm[1] = f0.y; dm[2] = f1.x; dm[3] = f1.y;
           }
+          // the unit's value scale 2^F, chosen by the warp's first frozen
+          // chunk of the unit from its largest Δ_t
+          float fsc = s_vsc[warp][0];
+          if (fsc == 0.f) {
+            float dmx = dm[0];
+#pragma unroll
+            for (int i = 1; i < TPL; ++i) dmx = fmaxf(dmx, dm[2 * i]);
+            dmx = warp_max_rows(dmx);   // the chunk's largest Δ_t (the same in every lane)
+            int ex = 0;
+            frexpf(dmx, &ex);
+            const int F = ex < 6 ? 6 - ex : 0;   // Δ_t 2^F below 2^6: p up to 2^8 keeps P' below 2^14
+            fsc = __uint_as_float(static_cast<uint32_t>(127 + F) << 23);
+            if (lane == 0) {
+              s_vsc[warp][0] = fsc;
+              s_vsc[warp][1] = __uint_as_float(static_cast<uint32_t>(127 - F) << 23);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < TPL; ++i) dm[2 * i] *= fsc;
 #pragma unroll
           for (int i = 0; i < TPL; ++i) {
             const float p = ex2(sv[i] - mref);
@@ -1220,6 +1573,37 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
             res_mn = fmaf(p, dm[2 * i + 1], res_mn);
             pd[i] = p * dm[2 * i] * vscl[i];
             if constexpr (OUTL) pbuf[c * CH + TPL * r + i] = p;
+          }
+        }
+        // fp16 range of P': p_t Δ_t 2^-k (p up to 2^8 behind a lazy max) goes
+        // past 65504 only for values spanning more than about 2^8 (2^b - 1)
+        // within one token.  One vote per chunk; then head c's reference is
+        // raised by a power of two E (res_m + E in log2 units), which scales
+        // p, l, Σ p min, the accumulators and P' by 2^-E exactly, so P' stays
+        // below 2^15 and nothing else changes
+        {
+          float pm = pd[0];
+#pragma unroll
+          for (int i = 1; i < TPL; ++i) pm = fmaxf(pm, pd[i]);
+          if (__any_sync(0xffffffffu, pm > 65504.f)) {
+            pm = warp_max_rows(pm);   // head c's largest P' of the chunk
+            int ex = 0;
+            frexpf(pm, &ex);
+            const int E = pm > 65504.f ? ex - 15 : 0;   // pm 2^-E in [2^14, 2^15)
+            if (E > 0) {
+              const float corr = __uint_as_float(static_cast<uint32_t>(127 - E) << 23);
+              res_m += static_cast<float>(E);
+              res_l *= corr;
+              res_mn *= corr;
+#pragma unroll
+              for (int i = 0; i < NCT; ++i) { oacc[i][0] *= corr; oacc[i][1] *= corr; oacc[i][2] *= corr; oacc[i][3] *= corr; }
+              rescale_corr(corr);
+#pragma unroll
+              for (int i = 0; i < TPL; ++i) {
+                pd[i] *= corr;
+                if constexpr (OUTL) pbuf[c * CH + TPL * r + i] *= corr;
+              }
+            }
           }
         }
         // (5) P' hi/lo into the exchange buffer (head c, tokens TPL*r ..)
@@ -1308,47 +1692,87 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
       const uint8_t* kst = my_stages + c_st * a.stage_bytes;
       const uint8_t* vst = kst + 16 * D;
       if (!o_real) {   // from here on oacc holds real-scale values
+        const float to_real = kTwo24 * value_unscale();
 #pragma unroll
-        for (int i = 0; i < NCT; ++i) { oacc[i][0] *= kTwo24; oacc[i][1] *= kTwo24; oacc[i][2] *= kTwo24; oacc[i][3] *= kTwo24; }
+        for (int i = 0; i < NCT; ++i) { oacc[i][0] *= to_real; oacc[i][1] *= to_real; oacc[i][2] *= to_real; oacc[i][3] *= to_real; }
         o_real = true;
       }
-      uint32_t q2[NP];   // natural pair order
+      float s;
+      if constexpr (ROPE) {
+        // the chunk's tokens sit at positions a_b + r: the query turned back
+        // by a_b θ, each key turned by its offset r
+        const int64_t a_b = tk.fresh ? f_fresh_pos(c_k)
+                          : tk.sink  ? static_cast<int64_t>(tk.first)
+                                     : g.S + (f_gfirst(c_k) + f_nvis(c_k)) * g.G + tk.first;
+        rope_angles<D>(wrow, rtab, a_b);
+        const uint32_t qrow_s = smem_addr(qw + hh_col * Rope<D>::kQRow), wrow_s = smem_addr(wrow);
+        const float2* otab = reinterpret_cast<const float2*>(rtab + D);
+        constexpr int RS = Rope<D>::kRS, H = D / 2;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < NP / 4; ++i) {
-        const uint4 v = lds128(q_s + 16 * i);
-        q2[4 * i] = v.x; q2[4 * i + 1] = v.z; q2[4 * i + 2] = v.y; q2[4 * i + 3] = v.w;
-      }
-      // keys of token r (zero past the chunk), natural pair order of quarter c
-      uint32_t ka[NP];
-      if (r < tk.n) {
-        if (tk.sink) {
-          const float* kr = reinterpret_cast<const float*>(kst) + r * D + c * QD;
+        for (int kc = 0; kc < NKC; ++kc) {
+          const int i = RS * c + 2 * kc;
+          uint32_t ah0 = 0u, ah2 = 0u, al0 = 0u, al2 = 0u;
+          if (r < tk.n) {
+            float2 xa, xb;   // channels (i, i + 1) and (i + H, i + H + 1) of token r
+            if (tk.sink) {
+              xa = *reinterpret_cast<const float2*>(kst + (r * D + i) * 4);
+              xb = *reinterpret_cast<const float2*>(kst + (r * D + i + H) * 4);
+            } else {
+              xa = h2f(*reinterpret_cast<const uint32_t*>(kst + (r * D + i) * 2));
+              xb = h2f(*reinterpret_cast<const uint32_t*>(kst + (r * D + i + H) * 2));
+            }
+            const float2 r0 = __ldg(otab + i * (g.G + 1) + r), r1 = __ldg(otab + (i + 1) * (g.G + 1) + r);
+            const float u0 = fmaf(r0.x, xa.x, -r0.y * xb.x), v0 = fmaf(r0.y, xa.x, r0.x * xb.x);
+            const float u1 = fmaf(r1.x, xa.y, -r1.y * xb.y), v1 = fmaf(r1.y, xa.y, r1.x * xb.y);
+            ah0 = rope_split(u0, u1, false); al0 = rope_split(u0, u1, true);
+            ah2 = rope_split(v0, v1, false); al2 = rope_split(v0, v1, true);
+          }
+          uint32_t b0, b1;
+          rope_fold_kc<D>(b0, b1, kc, qrow_s, wrow_s, c, (r & 1) != 0);
+          mma16816(acc, ah0, 0u, ah2, 0u, b0, b1);
+          mma16816(acc, al0, 0u, al2, 0u, b0, b1);
+        }
+        s = (r < tk.n) ? (acc[0] + acc[1]) * (2.f * qscale * head_qf()) : -INFINITY;
+      } else {
+        uint32_t q2[NP];   // natural pair order
 #pragma unroll
-          for (int i = 0; i < NP / 2; ++i) {
-            const float4 f = reinterpret_cast<const float4*>(kr)[i];
-            ka[2 * i] = pack_half2(f.x, f.y);
-            ka[2 * i + 1] = pack_half2(f.z, f.w);
+        for (int i = 0; i < NP / 4; ++i) {
+          const uint4 v = lds128(q_s + 16 * i);
+          q2[4 * i] = v.x; q2[4 * i + 1] = v.z; q2[4 * i + 2] = v.y; q2[4 * i + 3] = v.w;
+        }
+        // keys of token r (zero past the chunk), natural pair order of quarter c
+        uint32_t ka[NP];
+        if (r < tk.n) {
+          if (tk.sink) {
+            const float* kr = reinterpret_cast<const float*>(kst) + r * D + c * QD;
+#pragma unroll
+            for (int i = 0; i < NP / 2; ++i) {
+              const float4 f = reinterpret_cast<const float4*>(kr)[i];
+              ka[2 * i] = pack_half2(f.x, f.y);
+              ka[2 * i + 1] = pack_half2(f.z, f.w);
+            }
+          } else {
+            const uint8_t* kr = kst + (r * D + c * QD) * 2;
+#pragma unroll
+            for (int i = 0; i < NP / 4; ++i) {
+              const uint4 v = reinterpret_cast<const uint4*>(kr)[i];
+              ka[4 * i] = v.x; ka[4 * i + 1] = v.y; ka[4 * i + 2] = v.z; ka[4 * i + 3] = v.w;
+            }
           }
         } else {
-          const uint8_t* kr = kst + (r * D + c * QD) * 2;
 #pragma unroll
-          for (int i = 0; i < NP / 4; ++i) {
-            const uint4 v = reinterpret_cast<const uint4*>(kr)[i];
-            ka[4 * i] = v.x; ka[4 * i + 1] = v.y; ka[4 * i + 2] = v.z; ka[4 * i + 3] = v.w;
-          }
+          for (int i = 0; i < NP; ++i) ka[i] = 0u;
         }
-      } else {
+        // scores: rows r = tokens, column 2c = head c (every column holds its head's q)
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < NP; ++i) ka[i] = 0u;
+        for (int j = 0; j < NKC; ++j) {
+          if (j & 1) mma16816(acc1, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
+          else       mma16816(acc0, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
+        }
+        s = (r < tk.n) ? (acc0[0] + acc1[0]) * (qscale * head_qf()) : -INFINITY;
       }
-      // scores: rows r = tokens, column 2c = head c (every column holds its head's q)
-      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < NKC; ++j) {
-        if (j & 1) mma16816(acc1, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
-        else       mma16816(acc0, ka[2 * j], 0u, ka[2 * j + 1], 0u, q2[2 * j], q2[2 * j + 1]);
-      }
-      float s = (r < tk.n) ? (acc0[0] + acc1[0]) * qscale : -INFINITY;
       if constexpr (MQ) {   // token r's position against column c's visible range
         const int64_t hi = col_hi(), lo = col_lo(hi);
         const int64_t t = tk.fresh ? f_fresh_pos(c_k)
@@ -1433,26 +1857,28 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   }
 
   // drain this warp's copies still in flight (only after an abort), bounded
+  // by the full limit whatever the consumer's was: the copies that were
+  // issued land in this CTA's shared memory before it exits
   if (aborted) {
     for (int k = 0; k < inflight; ++k) {
-      mbar_wait(bar0 + 8 * c_st, c_ph);
+      mbar_wait(bar0 + 8 * c_st, c_ph, kWaitNs);
       if (++c_st == a.ns) { c_st = 0; c_ph ^= 1u; }
     }
   }
 }
 
 // Uniform launches: the plan is the launch's own (one kernel parameter).
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mma_kernel(const Args a) {
   const NoRuns none{0};
-  decode_body<D, BITS, CH, MQ, false, OUTL>(a, none);
+  decode_body<D, BITS, CH, MQ, false, OUTL, ROPE>(a, none);
 }
 
 // Ragged launches: the runs' plans travel as a grid constant.
-template <int D, int BITS, int CH, bool MQ, bool OUTL = false>
+template <int D, int BITS, int CH, bool MQ, bool OUTL = false, bool ROPE = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     decode_mma_ragged_kernel(const Args a, const __grid_constant__ RunTable rt) {
-  decode_body<D, BITS, CH, MQ, true, OUTL>(a, rt);
+  decode_body<D, BITS, CH, MQ, true, OUTL, ROPE>(a, rt);
 }
 
 }  // namespace mma

@@ -14,7 +14,10 @@
 namespace kivi {
 namespace {
 std::atomic<int64_t> g_fail_countdown{0};   // 0 = disarmed; n = the n-th launch from now fails
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;   // 2 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 }  // namespace
+unsigned long long copy_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 bool injected_launch_failure() {
   int64_t n = g_fail_countdown.load(std::memory_order_relaxed);
   while (n > 0) {
@@ -50,8 +53,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int validate(const kivi_params* p) {
   if (!p) return KIVI_ENULL;
   if (p->bits < 1 || p->bits > 8) return KIVI_EINVAL;
-  // the bit-stream widths decode on CUDA cores, a frozen group in one warp's
-  // shared memory and its value rows whole 32-bit words
+  // the bit-stream widths: a value row of a 32-token chunk is whole 32-bit
+  // words; groups of 32 or 64 tokens
   if (!kivi::word_rule(p->bits) && p->group != 32 && p->group != 64) return KIVI_EINVAL;
   if (!(p->head_dim == 64 || p->head_dim == 128)) return KIVI_EINVAL;
   if (p->group < 16 || p->group > 256 || p->group % 16 != 0) return KIVI_EINVAL;
@@ -66,10 +69,8 @@ int validate(const kivi_params* p) {
   if (p->window > 0 && p->window < p->residual) return KIVI_EINVAL;
   if (p->outlier_permille < 0 || p->outlier_permille > 50 || p->reserved != 0) return KIVI_EINVAL;
   // the outlier corrections are built into the tensor-core decode at 2 to 4
-  // bits (3 at head dim 128) with 32-token chunks
-  if (p->outlier_permille > 0 &&
-      (p->bits < 2 || p->bits > 4 || p->group % 32 != 0 || (p->bits == 3 && p->head_dim != 128)))
-    return KIVI_EINVAL;
+  // bits with 32-token chunks
+  if (p->outlier_permille > 0 && (p->bits < 2 || p->bits > 4 || p->group % 32 != 0)) return KIVI_EINVAL;
   // pre-RoPE keys decode on CUDA cores (a group in one warp's shared memory,
   // value rows whole 32-bit words), without outlier tables
   if (!(p->rope_base == 0.0 || (p->rope_base > 1.0 && p->rope_base <= 1e7))) return KIVI_EINVAL;
@@ -128,12 +129,11 @@ Geo geometry(const kivi_params& p) {
   const int64_t bhkv = static_cast<int64_t>(p.batch) * p.h_kv;
   g.ws_k = round_up(g.ws_out + bhq * d * 2, kAlign);
   g.ws_v = round_up(g.ws_k + bhkv * d * 2, kAlign);
+  g.ws_rope = round_up(g.ws_v + bhkv * d * 2, kAlign);
   return g;
 }
 
-int64_t arena_bytes_of(const Geo& g) {
-  return round_up(g.ws_v + static_cast<int64_t>(g.B) * g.hkv * g.d * 2, kAlign);
-}
+int64_t arena_bytes_of(const Geo& g) { return round_up(g.ws_rope + kivi::rope_table_bytes(g), kAlign); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ECUDA; }
 
@@ -270,7 +270,8 @@ int open_handle(const kivi_params* params, void* d_arena, size_t arena_bytes, co
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   const int64_t from = keep ? g.ws_counters : 0;   // counters and error word are adjacent
   const int64_t to = keep ? g.ws_error + 4 : arena_bytes_of(g);
-  const cudaError_t e = cudaMemsetAsync(c->arena + from, 0, static_cast<size_t>(to - from), s);
+  cudaError_t e = cudaMemsetAsync(c->arena + from, 0, static_cast<size_t>(to - from), s);
+  if (e == cudaSuccess) e = kivi::launch_rope_table(g, c->arena, s);   // pre-RoPE keys: the rotation tables
   if (e != cudaSuccess) { delete c; return KIVI_ECUDA; }
   *out = c;
   return KIVI_OK;
@@ -293,6 +294,13 @@ int kivi_cache_restore(const kivi_params* params, void* d_arena, size_t arena_by
 int kivi_debug_inject_launch_failure(int64_t n) {
   if (n < 0) return KIVI_EINVAL;
   kivi::g_fail_countdown.store(n, std::memory_order_relaxed);
+  return KIVI_OK;
+}
+
+int kivi_debug_set_wait_limit(int64_t ns) {
+  if (ns < 0) return KIVI_EINVAL;
+  kivi::g_wait_ns.store(ns == 0 ? kivi::kDefaultWaitNs : static_cast<unsigned long long>(ns),
+                        std::memory_order_relaxed);
   return KIVI_OK;
 }
 
@@ -335,10 +343,9 @@ cudaError_t attn_run(const kivi_cache& c, const Run& r, const kivi::DecodePlan& 
 }
 float* ws_partials(const kivi_cache& c) { return reinterpret_cast<float*>(c.arena + c.g.ws_partials); }
 
-// Bit-stream widths decode on tensor cores at head dim 128 (a lane's quarter
-// of a key row is whole 32-bit words) and on CUDA cores at head dim 64;
-// pre-RoPE keys (a rotation per token) decode on CUDA cores at every width.
-bool simt_path(const Geo& g) { return (!kivi::word_rule(g.bits) && g.d != 128) || g.rope_l2b != 0.0; }
+// Every cache decodes on tensor cores (the CUDA-core decode is kept for
+// nothing but reference).
+bool simt_path(const Geo&) { return false; }
 
 // The plans of runs [first, first + count) for one ragged launch (one query
 // token per sequence); fused: every sequence also attends to and appends one
@@ -608,9 +615,10 @@ int noalloc_scratch(void** out) {
 int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda_stream) {
   if (!c || !q || !out) return KIVI_ENULL;
   if (!aligned(q, 16) || !aligned(out, 16)) return KIVI_EALIGN;
-  // scratch: [error word][merge counters, npass per (sequence, kv head)][partials]
+  // scratch: [merge counters, npass per (sequence, kv head)][partials]; the
+  // bounded waits report into the cache's own error word (kivi_read_error)
   const int64_t npass = (c->g.rep + 3) / 4;
-  const int64_t head_bytes = kAlign + round_up(static_cast<int64_t>(c->g.B) * c->g.hkv * npass * 4, kAlign);
+  const int64_t head_bytes = round_up(static_cast<int64_t>(c->g.B) * c->g.hkv * npass * 4, kAlign);
   const int64_t record = static_cast<int64_t>(c->g.B) * c->g.hq * (c->g.d + 4) * 4;   // one CTA per unit
   const int64_t fit = (static_cast<int64_t>(kNoAllocScratchBytes) - head_bytes) / record;
   if (fit < 3) return KIVI_ESCRATCH;   // at least two CTAs per unit
@@ -619,14 +627,13 @@ int kivi_decode_attn_noalloc(kivi_cache* c, const void* q, void* out, void* cuda
   if (st != KIVI_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   unsigned char* bytes = static_cast<unsigned char*>(base);
-  unsigned* error = reinterpret_cast<unsigned*>(bytes);
-  unsigned* counters = reinterpret_cast<unsigned*>(bytes + kAlign);
+  unsigned* counters = reinterpret_cast<unsigned*>(bytes);
   float* partials = reinterpret_cast<float*>(bytes + head_bytes);
   if (cudaMemsetAsync(bytes, 0, static_cast<size_t>(head_bytes), s) != cudaSuccess) return KIVI_ECUDA;
   // each launch leaves the counters zero and caps its CTAs so a unit's
   // partials fit
   return cuda_status(decode_all(*c, static_cast<const __half*>(q), static_cast<__half*>(out), nullptr, nullptr,
-                                partials, static_cast<int32_t>(fit), counters, error, s));
+                                partials, static_cast<int32_t>(fit), counters, ws_error(*c), s));
 }
 
 int kivi_set_num_splits(kivi_cache* c, int32_t num_splits) {
@@ -756,8 +763,8 @@ size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
 int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch) return KIVI_ENULL;
-  // multi-query attention: the tensor-core path, without outlier tables
-  if (simt_path(c->g) || c->g.n_out > 0) return KIVI_EINVAL;
+  // multi-query attention: the tensor-core path
+  if (simt_path(c->g)) return KIVI_EINVAL;
   if (n_queries > min_tokens_of(*c) || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
   if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(c->g, n_queries)) return KIVI_ENOSPC;
@@ -768,7 +775,7 @@ int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries
 int kivi_prefill_attn_ragged(kivi_cache* c, const void* q, void* out, const int64_t* n_queries, int64_t m_max,
                              void* scratch, size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch || !n_queries) return KIVI_ENULL;
-  if (simt_path(c->g) || c->g.n_out > 0) return KIVI_EINVAL;
+  if (simt_path(c->g)) return KIVI_EINVAL;
   if (!prefill_count_ok(c->g, m_max)) return KIVI_EINVAL;
   for (int32_t b = 0; b < c->g.B; ++b)
     if (n_queries[b] < 0 || n_queries[b] > m_max || n_queries[b] > c->T[b]) return KIVI_EINVAL;

@@ -27,6 +27,7 @@ struct Geo {
   int64_t ws_error;      // arena offset of the device error word
   int64_t ws_q, ws_out;  // arena offsets of the host-call staging buffers
   int64_t ws_k, ws_v;    // staging of one new token per sequence (fused host-buffer step)
+  int64_t ws_rope;       // arena offset of the RoPE tables (pre-RoPE keys; rope.cu)
   int32_t max_splits;    // CTAs that may share one unit (partial records - 2)
   int32_t split_stride;  // partial records per query head
 };
@@ -51,6 +52,15 @@ __host__ __device__ inline State state_at(const Geo& g, int64_t T) {
 // the launch about to be made is the one armed to fail; it is then not made
 // and the caller reports cudaErrorLaunchFailure.
 bool injected_launch_failure();
+// How long a decode warp waits for one of its copies before it gives up and
+// sets the error word's copy bit (kivi_debug_set_wait_limit; 2 s by default).
+unsigned long long copy_wait_ns();
+
+// ---- pre-RoPE keys (rope.cu) ----
+// Bytes of the RoPE tables of a geometry (0 without pre-RoPE keys), and the
+// launch that writes them into the arena's workspace.
+int64_t rope_table_bytes(const Geo& g);
+cudaError_t launch_rope_table(const Geo& g, uint8_t* arena, cudaStream_t stream);
 
 // ---- append (append.cu) ----
 // Quantizes and packs groups [g_begin, g_end) of every unit.  Tokens with

@@ -46,8 +46,8 @@ def test_cache_bytes_covers_the_oracle_layout(abi, oracle_lib):
     for kw in (dict(), dict(bits=2, head_dim=128, batch=8, h_q=32, h_kv=32, max_tokens=4096),
                dict(bits=8, group=64, residual=64, window=4096, max_tokens=0, h_q=32, h_kv=8, batch=32,
                     head_dim=128),
-               dict(bits=3, head_dim=128, outlier_permille=10), dict(bits=2, group=64, residual=64,
-                                                                      outlier_permille=50)):
+               dict(bits=3, head_dim=128, outlier_permille=10), dict(bits=3, outlier_permille=10),
+               dict(bits=2, group=64, residual=64, outlier_permille=50)):
         cfg = params(**kw)
         lay = oracle_lib.layout(oracle_lib.Params(**cfg.__dict__))
         nb = cache_bytes(cfg)
@@ -65,8 +65,7 @@ def test_cache_bytes_covers_the_oracle_layout(abi, oracle_lib):
                                 dict(outlier_permille=-1), dict(outlier_permille=51),
                                 dict(outlier_permille=10, bits=8), dict(outlier_permille=10, bits=1),
                                 dict(outlier_permille=10, group=16, residual=32),
-                                dict(outlier_permille=10, bits=3),
-                                # pre-RoPE keys: base 0 or in (1, 1e7], G 32 or 64, no outlier tables
+                                 # pre-RoPE keys: base 0 or in (1, 1e7], G 32 or 64, no outlier tables
                                 dict(rope_base=1.0), dict(rope_base=-3.0), dict(rope_base=2e7),
                                 dict(rope_base=10000.0, group=16, residual=32),
                                 dict(rope_base=10000.0, group=128, residual=128),
@@ -118,6 +117,13 @@ def test_fault_injection_arming_is_host_only(abi):
     assert L.kivi_debug_inject_launch_failure(-1) == abi.KIVI_EINVAL
     assert L.kivi_debug_inject_launch_failure(3) == abi.KIVI_OK
     assert L.kivi_debug_inject_launch_failure(0) == abi.KIVI_OK
+
+
+def test_wait_limit_setting_is_host_only(abi):
+    L = abi.lib()
+    assert L.kivi_debug_set_wait_limit(-1) == abi.KIVI_EINVAL
+    assert L.kivi_debug_set_wait_limit(5) == abi.KIVI_OK
+    assert L.kivi_debug_set_wait_limit(0) == abi.KIVI_OK
 
 
 def test_restore_rejects_bad_arguments_before_any_device_call(abi):

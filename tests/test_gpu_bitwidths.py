@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, Pair, random_q, random_stream
+from gpu_util import TOL, Pair, random_q, random_stream, row_rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -59,37 +59,47 @@ def test_bit_stream_widths_match_oracle(shape):
 
 
 def test_three_bits_ragged_and_prefill():
-    """3 bits at head dim 128 (the tensor-core path): a ragged batch decodes
-    per sequence and chunked prefill matches the oracle; at head dim 64 (the
-    CUDA-core path) multi-query attention is refused."""
-    import ctypes
-    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig, _abi
+    """3 bits at head dims 128 and 64: a ragged batch decodes per sequence and
+    chunked prefill matches the oracle (at head dim 64 a lane's quarter of a
+    3-bit key row starts on a 16-bit boundary, which the kernel aligns)."""
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
     import oracle
-    from gpu_util import oparams, row_rel_err
-    cfg = KiviConfig(bits=3, group=32, residual=64, sinks=4, h_q=4, h_kv=4, head_dim=128, batch=3, max_tokens=600)
-    c = KiviCache(cfg)
-    refs = [oracle.Cache(oparams(cfg, batch=1)) for _ in range(3)]
-    k, v = random_stream(cfg, 500, seed=33)
-    counts = [400, 123, 7]
-    c.append_ragged(k[:, :, :400].contiguous().cuda(), v[:, :, :400].contiguous().cuda(), counts)
-    for b, n in enumerate(counts):
-        assert refs[b].append(k[b:b + 1, :, :n].numpy(), v[b:b + 1, :, :n].numpy()) == 0
-    q = random_q(cfg, 5)
-    out = c.decode(q.cuda()).float().cpu().numpy()
-    for b in range(3):
-        assert row_rel_err(out[b:b + 1], refs[b].decode_attn(q[b:b + 1].numpy())) <= TOL
-    g = torch.Generator().manual_seed(9)
-    qq = torch.randn((3, 7, 4, 128), generator=g).half()
-    pout = c.prefill_ragged(qq.cuda(), [7, 7, 7]).float().cpu().numpy()
-    for b in range(3):
-        assert row_rel_err(pout[b:b + 1], refs[b].prefill_attn(qq[b:b + 1].numpy())) <= TOL
-    assert c.read_error() == 0
-    small = KiviConfig(bits=3, group=32, residual=64, sinks=4, h_q=4, h_kv=4, head_dim=64, batch=1, max_tokens=64)
-    c64 = KiviCache(small)
-    z = torch.zeros((1, 4, 8, 64), dtype=torch.float16, device="cuda")
-    c64.append(z, z)
-    sc = torch.empty(c64.prefill_scratch_bytes(4), dtype=torch.uint8, device="cuda")
-    q4 = torch.zeros((1, 4, 4, 64), dtype=torch.float16, device="cuda")
-    vp = ctypes.c_void_p
-    assert _abi.lib().kivi_prefill_attn(c64._h, vp(q4.data_ptr()), vp(q4.data_ptr()), 4, vp(sc.data_ptr()),
-                                        sc.numel(), None) == _abi.KIVI_EINVAL
+    from gpu_util import oparams
+    for d in (128, 64):
+        cfg = KiviConfig(bits=3, group=32, residual=64, sinks=4, h_q=4, h_kv=4, head_dim=d, batch=3, max_tokens=600)
+        c = KiviCache(cfg)
+        refs = [oracle.Cache(oparams(cfg, batch=1)) for _ in range(3)]
+        k, v = random_stream(cfg, 500, seed=33)
+        counts = [400, 123, 7]
+        c.append_ragged(k[:, :, :400].contiguous().cuda(), v[:, :, :400].contiguous().cuda(), counts)
+        for b, n in enumerate(counts):
+            assert refs[b].append(k[b:b + 1, :, :n].numpy(), v[b:b + 1, :, :n].numpy()) == 0
+        q = random_q(cfg, 5)
+        out = c.decode(q.cuda()).float().cpu().numpy()
+        for b in range(3):
+            assert row_rel_err(out[b:b + 1], refs[b].decode_attn(q[b:b + 1].numpy())) <= TOL, (d, b)
+        g = torch.Generator().manual_seed(9)
+        qq = torch.randn((3, 7, 4, d), generator=g).half()
+        pout = c.prefill_ragged(qq.cuda(), [7, 7, 7]).float().cpu().numpy()
+        for b in range(3):
+            assert row_rel_err(pout[b:b + 1], refs[b].prefill_attn(qq[b:b + 1].numpy())) <= TOL, (d, b)
+        assert c.read_error() == 0
+
+
+@pytest.mark.parametrize("bits", [1, 5, 6, 7])
+def test_prefill_at_head_dim_64_bit_streams(bits):
+    """Chunked prefill of the other bit-stream widths at head dim 64 (quarters
+    of 2 b bytes: aligned at 6 bits, on a 16-bit boundary at 1, 5 and 7)."""
+    from kivi_quantized_kv_gb300 import KiviConfig
+    cfg = KiviConfig(bits=bits, group=32, residual=32, sinks=3, h_q=8, h_kv=2, head_dim=64, batch=2, max_tokens=500)
+    p = Pair(cfg)
+    k, v = random_stream(cfg, 400, seed=bits)
+    g = torch.Generator().manual_seed(bits)
+    t = 0
+    for m in (200, 48, 1):
+        p.append(k[:, :, t:t + m].contiguous(), v[:, :, t:t + m].contiguous())
+        t += m
+        q = torch.randn((cfg.batch, m, cfg.h_q, cfg.head_dim), generator=g).half()
+        out = p.gpu.prefill(q.cuda()).float().cpu().numpy()
+        assert row_rel_err(out, p.ref.prefill_attn(q.numpy(), threads=8)) <= TOL, m
+    assert p.bytes_equal()

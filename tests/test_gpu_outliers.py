@@ -128,18 +128,55 @@ def test_ragged_lengths_with_outliers():
     assert gpu.read_error() == 0
 
 
-def test_prefill_is_refused_with_outliers():
-    import ctypes
-    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig, _abi
-    cfg = KiviConfig(bits=4, group=32, residual=32, sinks=0, h_q=4, h_kv=4, head_dim=128, batch=1, max_tokens=64,
+@pytest.mark.parametrize("shape", [
+    # 4 bits, d 128, GQA rep 4 (a head pass of four rows spans one query token)
+    dict(bits=4, group=32, residual=64, sinks=4, h_q=8, h_kv=2, head_dim=128, batch=2, max_tokens=700,
+         outlier_permille=10),
+    # 3 bits at head dim 64 (bit stream), MHA (a pass of four rows spans four query tokens), 2 %
+    dict(bits=3, group=32, residual=32, sinks=2, h_q=4, h_kv=4, head_dim=64, batch=2, max_tokens=700,
+         outlier_permille=20),
+    # 2 bits, d 128, GQA rep 3, a wrapping window
+    dict(bits=2, group=64, residual=64, sinks=1, h_q=6, h_kv=2, head_dim=128, batch=1, max_tokens=0, window=160,
+         outlier_permille=5),
+])
+def test_prefill_with_outliers(shape):
+    """Chunked prefill (the causal attention of a chunk's queries) over a cache
+    with outlier tables: every row within 2e-3 of the oracle's causal
+    attention, chunks shorter and longer than the ring (so some chunk tokens
+    are read from codes and their tables), bytes identical after each chunk."""
+    from kivi_quantized_kv_gb300 import KiviConfig
+    cfg = KiviConfig(**shape)
+    p = Pair(cfg)
+    k, v = spiky_stream(cfg, 700, seed=21)
+    t = 0
+    g = torch.Generator().manual_seed(4)
+    for m in (130, 9, 100, 1, 70):
+        p.append(k[:, :, t:t + m].contiguous(), v[:, :, t:t + m].contiguous())
+        t += m
+        assert p.bytes_equal()
+        q = torch.randn((cfg.batch, m, cfg.h_q, cfg.head_dim), generator=g).half()
+        out = p.gpu.prefill(q.cuda()).float().cpu().numpy()
+        exp = p.ref.prefill_attn(q.numpy(), threads=8)
+        assert row_rel_err(out, exp) <= TOL, m
+    assert p.gpu.read_error() == 0
+
+
+def test_outlier_tables_at_head_dim_64_three_bits():
+    """3 bits (bit stream) at head dim 64 with 1 % outlier tables: bytes and
+    decode against the oracle, through fused steps across group freezes."""
+    from kivi_quantized_kv_gb300 import KiviConfig
+    cfg = KiviConfig(bits=3, group=64, residual=64, sinks=4, h_q=8, h_kv=2, head_dim=64, batch=2, max_tokens=700,
                      outlier_permille=10)
-    c = KiviCache(cfg)
-    k = torch.zeros((1, 4, 40, 128), dtype=torch.float16, device="cuda")
-    c.append(k, k)
-    q = torch.zeros((1, 4, 4, 128), dtype=torch.float16, device="cuda")
-    sc = torch.empty(max(c.prefill_scratch_bytes(4), 256), dtype=torch.uint8, device="cuda")
-    out = torch.empty_like(q)
-    vp = ctypes.c_void_p
-    assert _abi.lib().kivi_prefill_attn(c._h, vp(q.data_ptr()), vp(out.data_ptr()), 4, vp(sc.data_ptr()),
-                                        sc.numel(), None) == _abi.KIVI_EINVAL
-    torch.cuda.synchronize()
+    p = Pair(cfg)
+    k, v = spiky_stream(cfg, 600, seed=12)
+    p.append(k[:, :, :500].contiguous(), v[:, :, :500].contiguous())
+    assert p.bytes_equal()
+    assert p.decode_err(random_q(cfg, 2)) <= TOL
+    for i in range(100):
+        kk, vv = k[:, :, 500 + i:501 + i].contiguous(), v[:, :, 500 + i:501 + i].contiguous()
+        q = random_q(cfg, 200 + i)
+        out = p.gpu.append_decode(kk.cuda(), vv.cuda(), q.cuda()).float().cpu().numpy()
+        assert p.ref.append(kk.numpy(), vv.numpy()) == 0
+        assert row_rel_err(out, p.ref.decode_attn(q.numpy(), threads=8)) <= TOL, i
+    assert p.bytes_equal()
+    assert p.gpu.read_error() == 0

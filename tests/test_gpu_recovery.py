@@ -89,3 +89,34 @@ def test_injected_launch_failures_leave_counts_and_allow_retry():
     assert p.bytes_equal()
     assert L.kivi_debug_inject_launch_failure(0) == 0
     assert p.gpu.read_error() == 0
+
+
+def test_expired_copy_wait_sets_the_error_bit_and_the_next_call_is_exact():
+    """Every decode wait for a copy is bounded.  With the limit set to 1 ns
+    (kivi_debug_set_wait_limit) the waits run out while the copies are still
+    on their way, although every copy does arrive: the warps that give up let
+    their copies land, the launch ends, and bit 0 of the error word is set.
+    The next call at the default limit matches the oracle and sets no bit."""
+    from kivi_quantized_kv_gb300 import KiviConfig, _abi
+    L = _abi.lib()
+    cfg = KiviConfig(bits=4, group=32, residual=64, sinks=4, h_q=16, h_kv=4, head_dim=128, batch=4,
+                     max_tokens=3000)
+    p = Pair(cfg)
+    k, v = random_stream(cfg, 2500, seed=8)
+    p.append(k, v)
+    q = random_q(cfg, 5)
+    assert p.gpu.read_error() == 0
+    flags = 0
+    try:
+        assert L.kivi_debug_set_wait_limit(1) == 0
+        for _ in range(3):   # thousands of waits per launch; one running out is enough
+            p.gpu.decode(q.cuda())
+            flags |= p.gpu.read_error()
+            if flags & 1:
+                break
+    finally:
+        assert L.kivi_debug_set_wait_limit(0) == 0
+    assert flags & 1, flags
+    assert p.decode_err(q) <= TOL
+    assert p.gpu.read_error() == 0
+    assert p.bytes_equal()

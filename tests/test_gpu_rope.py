@@ -110,18 +110,38 @@ def test_ragged_lengths_with_pre_rope_keys():
     assert gpu.read_error() == 0
 
 
-def test_prefill_is_refused_with_pre_rope_keys():
-    import ctypes
-    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig, _abi
-    cfg = KiviConfig(bits=4, group=32, residual=32, sinks=0, h_q=4, h_kv=4, head_dim=128, batch=1, max_tokens=64,
-                     rope_base=10000.0)
-    c = KiviCache(cfg)
-    k = torch.zeros((1, 4, 40, 128), dtype=torch.float16, device="cuda")
-    c.append(k, k)
-    q = torch.zeros((1, 4, 4, 128), dtype=torch.float16, device="cuda")
-    sc = torch.empty(max(c.prefill_scratch_bytes(4), 256), dtype=torch.uint8, device="cuda")
-    out = torch.empty_like(q)
-    vp = ctypes.c_void_p
-    assert _abi.lib().kivi_prefill_attn(c._h, vp(q.data_ptr()), vp(out.data_ptr()), 4, vp(sc.data_ptr()),
-                                        sc.numel(), None) == _abi.KIVI_EINVAL
-    torch.cuda.synchronize()
+@pytest.mark.parametrize("shape", [CASES[0], CASES[1], CASES[3], CASES[4]])
+def test_prefill_with_pre_rope_keys(shape):
+    """Chunked prefill (each query token attends causally over the cache)
+    over pre-RoPE keys: every row within 2e-3 of the oracle's causal
+    attention, chunks shorter and longer than the ring, bytes identical."""
+    from kivi_quantized_kv_gb300 import KiviConfig
+    cfg = KiviConfig(**{"rope_base": 10000.0, **shape})
+    p = Pair(cfg)
+    k, v = random_stream(cfg, 700, seed=23)
+    g = torch.Generator().manual_seed(11)
+    t = 0
+    for m in (150, 9, 100, 1, 64):
+        p.append(k[:, :, t:t + m].contiguous(), v[:, :, t:t + m].contiguous())
+        t += m
+        q = torch.randn((cfg.batch, m, cfg.h_q, cfg.head_dim), generator=g).half()
+        out = p.gpu.prefill(q.cuda()).float().cpu().numpy()
+        assert row_rel_err(out, p.ref.prefill_attn(q.numpy(), threads=8)) <= TOL, m
+    assert p.bytes_equal()
+    assert p.gpu.read_error() == 0
+
+
+def test_long_positions_with_pre_rope_keys():
+    """Positions past 2^17 (a 32-token window over a stream of 140000 tokens,
+    base angles reduced mod 2π from large multiples): decode within 2e-3."""
+    from kivi_quantized_kv_gb300 import KiviConfig
+    cfg = KiviConfig(bits=4, group=32, residual=32, sinks=2, h_q=4, h_kv=1, head_dim=128, batch=1, max_tokens=0,
+                     window=64, rope_base=10000.0)
+    p = Pair(cfg)
+    k, v = random_stream(cfg, 4000, seed=5)
+    # 35 passes over the same 4000 tokens: positions reach 140000
+    for rnd in range(35):
+        p.append(k, v)
+    assert p.gpu.tokens == 140000
+    assert p.bytes_equal()
+    assert p.decode_err(random_q(cfg, 9)) <= TOL
