@@ -974,9 +974,7 @@ def main():
                                       "ragged": bool(args.ragged)}),
         "roofline": {"bound": "hbm", "achieved": round(r["dec_gbs"], 1), "peak": peak, "unit": "GB/s",
                      "frac": round(r["dec_gbs"] / peak, 4), "traffic": traffic,
-                     "kernel": ("decode_simt_kernel (CUDA cores, per-run append then decode)"
-                                if (w.bits not in (2, 4, 8) and w.head_dim != 128) or w.rope_base else
-                                "decode_mma_kernel (stream-K split-K, merge and fresh-token append in the same launch)"),
+                     "kernel": "decode_mma_kernel (stream-K split-K, merge and fresh-token append in the same launch)",
                      "peak_source": src,
                      "bytes_per_launch": int(r["dec_bytes"])},
         "gpu_launches": r["launches"],
@@ -1005,18 +1003,18 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-DECODE_SOURCES = ("kivi_internal.cuh", "decode_mma.cuh", "decode_launch.cuh", "decode.cu",
-                  "decode_b2.cu", "decode_b4.cu", "decode_b8.cu", "decode_simt.cuh", "decode_simt.cu",
-                  "decode_simt_d64.cu", "decode_simt_d128.cu", "decode_simt_rope_d64.cu", "decode_simt_rope_d128.cu",
-                  "decode_outl.cuh", "decode_outl.cu",
-                  "decode_outl_b2.cu", "decode_outl_b3.cu", "decode_outl_b4.cu")
+def decode_sources():
+    """The decode kernels' sources: the shared internal header, the rotation
+    table and every decode* file, in name order."""
+    csrc = os.path.join(ROOT, "kivi_quantized_kv_gb300", "csrc")
+    return ["kivi_internal.cuh", "rope.cu"] + sorted(f for f in os.listdir(csrc) if f.startswith("decode"))
 
 
 def decode_sources_sha():
     """sha256 over the decode kernel's sources, in a fixed order."""
     import hashlib
     h = hashlib.sha256()
-    for n in DECODE_SOURCES:
+    for n in decode_sources():
         with open(os.path.join(ROOT, "kivi_quantized_kv_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

@@ -102,9 +102,13 @@ typedef struct kivi_params {
                                  dequantized key at its own position a:
                                  channels (i, i + d/2) by the angle
                                  a * rope_base^(-2i/d); q arrives rotated.
-                                 Needs group 32 or 64 and no outlier tables;
-                                 decodes on CUDA cores; the multi-query
-                                 attention refuses such a cache */
+                                 Needs group 32 or 64 and no outlier tables.
+                                 Decode, the fused step and the multi-query
+                                 attention run on tensor cores: the query is
+                                 turned back by each group's first position
+                                 and the keys by their offset inside the
+                                 group (a table the handle writes once into
+                                 the workspace) */
 } kivi_params;
 
 /* Byte layout of the arena and current state (all offsets in bytes).
@@ -308,8 +312,8 @@ int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host,
  * oldest part of its first queries' windows).  The newest query's row equals
  * kivi_decode_attn's output for it.  Work: as kivi_decode_attn with n_queries
  * times the query rows per kv head, each row masked to its own positions.
- * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536, or a cache of
- * pre-RoPE keys), EALIGN, ENOSPC (scratch too small), ECUDA. */
+ * Errors: ENULL, EINVAL (n_queries < 1, > T or > 65536), EALIGN, ENOSPC
+ * (scratch too small), ECUDA. */
 int kivi_prefill_attn(kivi_cache* cache, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream);
 

@@ -343,10 +343,6 @@ cudaError_t attn_run(const kivi_cache& c, const Run& r, const kivi::DecodePlan& 
 }
 float* ws_partials(const kivi_cache& c) { return reinterpret_cast<float*>(c.arena + c.g.ws_partials); }
 
-// Every cache decodes on tensor cores (the CUDA-core decode is kept for
-// nothing but reference).
-bool simt_path(const Geo&) { return false; }
-
 // The plans of runs [first, first + count) for one ragged launch (one query
 // token per sequence); fused: every sequence also attends to and appends one
 // new token taken from the inputs.
@@ -395,23 +391,6 @@ cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const 
   const Geo& g = c.g;
   const bool fused = k_fresh != nullptr;
   const std::vector<Run> runs = runs_of(c);
-  if (simt_path(g)) {
-    // bit-stream widths at head dim 64: per run, the new token's append
-    // (fused step) and a CUDA-core decode
-    for (const Run& r : runs) {
-      if (fused) {
-        const cudaError_t e = append_run(c, r, k_fresh, v_fresh, 1, 1, s);
-        if (e != cudaSuccess) return e;
-      }
-      const kivi::DecodePlan pl = plan_for(c, fused ? r.T + 1 : r.T, r.nb);
-      const Geo gs = sub_geo(g, r.nb);
-      const int64_t row0 = static_cast<int64_t>(r.b0) * g.hq * g.d;
-      const cudaError_t e = kivi::launch_decode_simt(gs, run_base(c, r), q + row0, out + row0, pl, partials, stride,
-                                                     counters, c.num_sms, s);
-      if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-  }
   if (runs.size() == 1) {
     const Run& r = runs[0];
     if (fused) {
@@ -763,8 +742,6 @@ size_t kivi_prefill_scratch_bytes(const kivi_cache* c, int64_t n_queries) {
 int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries, void* scratch,
                       size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch) return KIVI_ENULL;
-  // multi-query attention: the tensor-core path
-  if (simt_path(c->g)) return KIVI_EINVAL;
   if (n_queries > min_tokens_of(*c) || !prefill_count_ok(c->g, n_queries)) return KIVI_EINVAL;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(scratch, kAlign)) return KIVI_EALIGN;
   if (static_cast<int64_t>(scratch_bytes) < prefill_scratch_of(c->g, n_queries)) return KIVI_ENOSPC;
@@ -775,7 +752,6 @@ int kivi_prefill_attn(kivi_cache* c, const void* q, void* out, int64_t n_queries
 int kivi_prefill_attn_ragged(kivi_cache* c, const void* q, void* out, const int64_t* n_queries, int64_t m_max,
                              void* scratch, size_t scratch_bytes, void* cuda_stream) {
   if (!c || !q || !out || !scratch || !n_queries) return KIVI_ENULL;
-  if (simt_path(c->g)) return KIVI_EINVAL;
   if (!prefill_count_ok(c->g, m_max)) return KIVI_EINVAL;
   for (int32_t b = 0; b < c->g.B; ++b)
     if (n_queries[b] < 0 || n_queries[b] > m_max || n_queries[b] > c->T[b]) return KIVI_EINVAL;

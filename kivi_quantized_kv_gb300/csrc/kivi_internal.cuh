@@ -148,12 +148,6 @@ inline int32_t decode_smem(const DecodeShape& sh, int32_t /*stride*/) { return s
 // Resident decode CTAs per SM for this geometry (queries the device).
 int decode_ctas_per_sm(const Geo& g);
 
-// Decode on CUDA cores for the bit-stream code widths (b in {1, 3, 5, 6, 7};
-// G in {32, 64}): one query token per sequence, no fresh token; `partials` and
-// `counters` as for the tensor-core decode; the grid is sized for `sms` SMs.
-cudaError_t launch_decode_simt(const Geo& g, const uint8_t* arena, const __half* q, __half* out,
-                               const DecodePlan& plan, float* partials, int32_t stride, unsigned* counters,
-                               int32_t sms, cudaStream_t stream);
 // Packing rule of a code width: the word rule (b in {2, 4, 8}) or a bit stream.
 inline bool word_rule(int bits) { return bits == 2 || bits == 4 || bits == 8; }
 

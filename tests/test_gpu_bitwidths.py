@@ -2,8 +2,8 @@
 kvquant++ README recommends 3) against the oracle, through the C ABI.
 
 These widths pack as a plain bit stream and decode on the tensor cores at
-head dim 128 (two codes unpacked into one fp16x2 operand register) and on
-CUDA cores at head dim 64 (decode_simt.cuh).  Bytes must equal the oracle's; decode and fused steps
+head dims 64 and 128 (two codes unpacked into one fp16x2 operand register).
+Bytes must equal the oracle's; decode, fused steps and multi-query attention
 within 2e-3.  Streams cross sinks, the filling ring, group freezes, a wrapping
 window and ragged lengths.
 """
