@@ -16,10 +16,10 @@
  *   - tract #2458 "quantized KV-cache storage op (int8/int4)": the first S
  *     tokens (attention sinks) stay in f32 in both stores; key blocks keep
  *     frozen scales once written.
- *   - tract #2329 "KIVI-style KV-cache quantization", "What's in the PR": the
- *     fused op takes [Q, K_new, V_new], handles GQA, and its output has Q's
- *     shape; "Relationship to other PRs": a bounded sliding window composes
- *     with the quantized storage.
+ *   - tract #2329 "KIVI-style KV-cache quantization", "What's in the PR": a
+ *     fused op over the query and the new keys and values, with grouped-query
+ *     heads and an output shaped like the query; "Relationship to other PRs":
+ *     a bounded sliding window composes with the quantized storage.
  *
  * Memory ownership: the caller allocates every device buffer (the arena,
  * prefill scratch and all inputs/outputs).  The library allocates only the
@@ -258,8 +258,8 @@ int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_str
 
 /* One decode step in one call: appends one token to every sequence and
  * returns the decode attention over everything including that token, the
- * fused op of tract #2329 ("What's in the PR": inputs [Q, K_new, V_new],
- * output with Q's shape).  The result and the cache bytes are those of
+ * fused op of tract #2329, "What's in the PR" (it takes the query with the
+ * new keys and values and returns an output shaped like the query).  The result and the cache bytes are those of
  * kivi_append(k_new, v_new, 1) followed by kivi_decode_attn(q, out) (the
  * output to within the decode's rounding).  The new token is attended
  * straight from k_new / v_new and written into its sink or ring slot by the
@@ -345,8 +345,13 @@ int64_t kivi_prefill_bytes(const kivi_cache* cache, int64_t n_queries);
  * bit 0 = a bulk copy into shared memory did not complete within its bounded
  * wait (2 s, or the limit of kivi_debug_set_wait_limit), bit 1 = a warp
  * waited in vain for its combine slot to be released.  Either bit means the
- * affected outputs are not valid.  Unlike every other call this one
- * synchronises `stream` (it returns the value).  Errors: ENULL, ECUDA. */
+ * affected outputs are not valid.  The checked build of the library
+ * (libkivi_debug.so, compiled with KIVI_DEBUG_CHECKS=1) adds two bits that
+ * every kernel, appends included, may set: bit 2 = an arena address derived
+ * from the plan left the cache region (the access was skipped), bit 3 = an
+ * input key, value or query element was inf or NaN (a precondition of the
+ * method; the product build does not look).  Unlike every other call this
+ * one synchronises `stream` (it returns the value).  Errors: ENULL, ECUDA. */
 int kivi_read_error(kivi_cache* cache, uint32_t* flags, void* cuda_stream);
 
 /* Decode attention that allocates nothing (the method's pages have no

@@ -10,6 +10,7 @@ import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkivi.so")
+LIB_PATH_DEBUG = os.path.join(HERE, "libkivi_debug.so")
 
 KIVI_OK, KIVI_EINVAL, KIVI_EALIGN, KIVI_ECAPACITY, KIVI_ENOSPC, KIVI_ECUDA, KIVI_ENULL, KIVI_ESCRATCH = range(8)
 
@@ -54,15 +55,25 @@ class KiviError(RuntimeError):
 _lib = None
 
 
+def lib_path() -> str:
+    """libkivi.so, or the checked build libkivi_debug.so when the environment
+    sets KIVI_DEBUG_CHECKS=1."""
+    if os.environ.get("KIVI_DEBUG_CHECKS", "0") == "1":
+        return LIB_PATH_DEBUG
+    return LIB_PATH
+
+
 def lib():
-    """Loads libkivi.so; raises if it has not been built."""
+    """Loads the library; raises if it has not been built."""
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
-    L = ctypes.CDLL(LIB_PATH)
+    path = lib_path()
+    if not os.path.exists(path):
+        how = ("`python -m kivi_quantized_kv_gb300.build --debug-checks`" if path == LIB_PATH_DEBUG else
+               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        raise ImportError(f"{path} is missing: build it with {how} (needs nvcc)")
+    L = ctypes.CDLL(path)
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
     P = ctypes.POINTER
     sig = {

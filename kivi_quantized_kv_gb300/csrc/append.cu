@@ -124,21 +124,31 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
     const int64_t a = a0 + t;
     const __half* ks;
     const __half* vs;
+    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
     if (a < T_old) {
       const int64_t slot = (a - g.S) % g.R;
       ks = reinterpret_cast<const __half*>(unit + g.res_k) + slot * d;
       vs = reinterpret_cast<const __half*>(unit + g.res_v) + slot * d;
+      if (dbg_in_region(g, ks + c8, 16) && dbg_in_region(g, vs + c8, 16)) {
+        kv = *reinterpret_cast<const uint4*>(ks + c8);
+        vv = *reinterpret_cast<const uint4*>(vs + c8);
+      }
     } else {
       ks = k_new + in_off + (a - T_old) * d;
       vs = v_new + in_off + (a - T_old) * d;
+      kv = *reinterpret_cast<const uint4*>(ks + c8);
+      vv = *reinterpret_cast<const uint4*>(vs + c8);
+      dbg_check_finite(g, kv);
+      dbg_check_finite(g, vv);
     }
-    *reinterpret_cast<uint4*>(kx + t * d + c8) = *reinterpret_cast<const uint4*>(ks + c8);
-    *reinterpret_cast<uint4*>(vx + t * d + c8) = *reinterpret_cast<const uint4*>(vs + c8);
+    *reinterpret_cast<uint4*>(kx + t * d + c8) = kv;
+    *reinterpret_cast<uint4*>(vx + t * d + c8) = vv;
   }
   __syncthreads();
 
   const float top = static_cast<float>((1 << b) - 1);
   uint8_t* blk = unit + g.groups + (grp % g.n_slots) * g.block_bytes;
+  if (!dbg_in_region(g, blk, g.block_bytes)) return;   // uniform over the block
   __half* ks_out = reinterpret_cast<__half*>(blk + g.blk_ks);
   __half* vs_out = reinterpret_cast<__half*>(blk + g.blk_vs);
 
@@ -302,11 +312,14 @@ __global__ void write_kernel(Geo g, uint8_t* __restrict__ arena, const __half* _
     uint8_t* unit = arena + u * g.unit_bytes;
     const uint4 kv = *reinterpret_cast<const uint4*>(k_new + src);
     const uint4 vv = *reinterpret_cast<const uint4*>(v_new + src);
+    dbg_check_finite(g, kv);
+    dbg_check_finite(g, vv);
     if (a < g.S) {
       const __half2* kh = reinterpret_cast<const __half2*>(&kv);
       const __half2* vh = reinterpret_cast<const __half2*>(&vv);
       float* sk = reinterpret_cast<float*>(unit + g.sink_k) + a * d + c8;
       float* sv = reinterpret_cast<float*>(unit + g.sink_v) + a * d + c8;
+      if (!dbg_in_region(g, sk, 32) || !dbg_in_region(g, sv, 32)) continue;
       float2 f[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) f[j] = __half22float2(kh[j]);
@@ -318,8 +331,11 @@ __global__ void write_kernel(Geo g, uint8_t* __restrict__ arena, const __half* _
       reinterpret_cast<float4*>(sv)[1] = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
     } else {
       const int64_t slot = (a - g.S) % g.R;
-      *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(unit + g.res_k) + slot * d + c8) = kv;
-      *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(unit + g.res_v) + slot * d + c8) = vv;
+      __half* rk = reinterpret_cast<__half*>(unit + g.res_k) + slot * d + c8;
+      __half* rv = reinterpret_cast<__half*>(unit + g.res_v) + slot * d + c8;
+      if (!dbg_in_region(g, rk, 16) || !dbg_in_region(g, rv, 16)) continue;
+      *reinterpret_cast<uint4*>(rk) = kv;
+      *reinterpret_cast<uint4*>(rv) = vv;
     }
   }
 }

@@ -255,6 +255,9 @@ int open_handle(const kivi_params* params, void* d_arena, size_t arena_bytes, co
   if (!c) return KIVI_ENULL;
   c->p = *params;
   c->g = g;
+  c->g.chk_lo = static_cast<const uint8_t*>(d_arena);
+  c->g.chk_hi = c->g.chk_lo + g.cache_bytes;
+  c->g.err = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(d_arena) + g.ws_error);
   c->arena = static_cast<uint8_t*>(d_arena);
   c->arena_bytes = arena_bytes;
   try {

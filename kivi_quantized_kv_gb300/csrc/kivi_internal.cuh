@@ -8,7 +8,21 @@
 
 #include "../../include/kivi.h"
 
+// Debug builds (compiled with -DKIVI_DEBUG_CHECKS=1 into libkivi_debug.so):
+// the kernels check every arena address they derive against the handle's
+// cache region and every input key, value and query for inf / NaN, and
+// record what they find in the arena's error word (kErrIndex, kErrNonFinite)
+// instead of trapping; an address that fails its check is not accessed.
+// The product build compiles the checks out.
+#ifndef KIVI_DEBUG_CHECKS
+#define KIVI_DEBUG_CHECKS 0
+#endif
+
 namespace kivi {
+
+constexpr bool kDebugChecks = KIVI_DEBUG_CHECKS != 0;
+constexpr unsigned kErrIndex = 4u;       // (debug builds) a derived address left the cache region; skipped
+constexpr unsigned kErrNonFinite = 8u;   // (debug builds) an input key, value or query was inf or NaN
 
 // Everything a kernel needs to address the arena; passed by value.
 struct Geo {
@@ -30,7 +44,32 @@ struct Geo {
   int64_t ws_rope;       // arena offset of the RoPE tables (pre-RoPE keys; rope.cu)
   int32_t max_splits;    // CTAs that may share one unit (partial records - 2)
   int32_t split_stride;  // partial records per query head
+  // set when a handle opens: the handle's cache region [chk_lo, chk_hi) and
+  // its error word (the debug checks; sub-geometries of a run keep them)
+  const uint8_t* chk_lo;
+  const uint8_t* chk_hi;
+  unsigned* err;
 };
+
+// Debug checks (no-ops in the product build).
+__device__ __forceinline__ bool dbg_in_region(const Geo& g, const void* p, int64_t bytes) {
+  if constexpr (!kDebugChecks) return true;
+  const uint8_t* q = static_cast<const uint8_t*>(p);
+  if (q >= g.chk_lo && bytes >= 0 && q + bytes <= g.chk_hi) return true;
+  atomicOr(g.err, kErrIndex);
+  return false;
+}
+// eight fp16 values: an exponent field of all ones is inf or NaN
+__device__ __forceinline__ void dbg_check_finite(const Geo& g, uint4 v) {
+  if constexpr (kDebugChecks) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      bad |= (w[i] & 0x7C00u) == 0x7C00u || (w[i] & 0x7C000000u) == 0x7C000000u;
+    if (bad) atomicOr(g.err, kErrNonFinite);
+  }
+}
 
 // Cache state after T tokens (lazy flush: a token that reaches a full ring
 // first pushes the ring's oldest G tokens out as one frozen group).

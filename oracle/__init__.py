@@ -9,8 +9,9 @@ Sources of each computation are cited in ``kivi_oracle.cpp``; in short:
   * KV-cache quantization guide (pigeon), "How it works", steps 1-5;
   * tract #2458 "quantized KV-cache storage op (int8/int4)": f32 attention
     sinks, frozen per-channel key blocks;
-  * tract #2329 "KIVI-style KV-cache quantization", "What's in the PR": GQA,
-    op contract [Q, K_new, V_new] -> Q-shaped output.
+  * tract #2329 "KIVI-style KV-cache quantization", "What's in the PR": GQA;
+    the op takes the query with the new keys and values and returns an output
+    shaped like the query.
 
 fp16 arrays are passed as numpy ``float16`` (or their ``uint16`` bit view).
 """

@@ -100,8 +100,8 @@ float f16_to_f32(uint16_t h) {
 //   * x values are fp16 widened exactly to fp32; every operation is one
 //     IEEE fp32 operation rounded to nearest-even, no fused multiply-add;
 //   * min and max are canonicalised with + 0.0f so that -0 becomes +0;
-//   * Δ is stored as fp16 (the "fp16 scales and zero points" of the spec) and
-//     the STORED fp16 Δ is the divisor that makes the codes;
+//   * Δ and the zero point are stored as fp16, and the STORED fp16 Δ is the
+//     divisor that makes the codes;
 //   * "round" is round-half-to-even; codes are clamped to [0, 2^b - 1]
 //     (the fp16 Δ can be a little smaller than the exact one);
 //   * when the stored Δ is zero (a constant vector) every code is 0.

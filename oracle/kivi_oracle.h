@@ -15,9 +15,11 @@
  *   - tract #2458 "quantized KV-cache storage op (int8/int4)", commit on
  *       attention sinks: the first SINK tokens are kept in f32 in both stores.
  *   - tract #2458 description: keys quantized in fixed-size blocks whose
- *       scales are frozen once written ("streaming consistency").
+ *       scales never change once written, so a stream gives the same bytes
+ *       however it is chunked.
  *   - tract #2329 "KIVI-style KV-cache quantization", "What's in the PR":
- *       GQA handled; inputs [Q, K_new, V_new], output has Q's shape.
+ *       grouped-query heads; the op takes the query with the new keys and
+ *       values, and its output is shaped like the query.
  *   - tract #2329 "Relationship to other PRs": bounded sliding-window cache
  *       composed with quantization.
  *

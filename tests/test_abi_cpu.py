@@ -34,6 +34,18 @@ def test_exports_every_declared_symbol(abi):
     assert sorted(abi.EXPORTS) == names
 
 
+def test_checked_build_exports_the_same_symbols(abi):
+    """KIVI_DEBUG_CHECKS=1 builds libkivi_debug.so with the same entry points;
+    the binding picks it only when the environment asks for it."""
+    from kivi_quantized_kv_gb300.build import build
+    path = build(debug_checks=True)
+    assert path.endswith("libkivi_debug.so") and path != abi.LIB_PATH
+    lib = ctypes.CDLL(path)
+    for n in header_functions():
+        assert hasattr(lib, n), n
+    assert abi.lib_path() == abi.LIB_PATH   # the product library unless KIVI_DEBUG_CHECKS=1
+
+
 def params(**kw):
     from kivi_quantized_kv_gb300 import KiviConfig
     base = dict(bits=4, group=32, residual=32, sinks=4, h_q=4, h_kv=4, head_dim=64, batch=1, max_tokens=256)

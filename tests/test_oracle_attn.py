@@ -2,8 +2,8 @@
 
 Sources: KV-cache quantization guide (pigeon), "How it works", step 5
 (softmax(q Kᵀ / sqrt(d)) V over the dequantized values); tract #2329 "What's
-in the PR" (GQA handled; output has Q's shape); tract #2329 "Relationship to
-other PRs" (sliding-window cache composed with quantization).
+in the PR" (grouped-query heads; an output shaped like the query); tract #2329
+"Relationship to other PRs" (sliding-window cache composed with quantization).
 """
 import numpy as np
 import pytest

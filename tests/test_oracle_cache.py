@@ -2,9 +2,9 @@
 
 Sources: KV-cache quantization guide (pigeon), "How it works", steps 1, 2, 4;
 tract #2458 "quantized KV-cache storage op (int8/int4)": f32 sinks (sink
-commit), "accumulation vs a plain concat" and "block-wise per-channel
-consistency over a growing range" (description, unit tests), frozen key-block
-scales ("streaming consistency").
+commit); its unit tests that a stream accumulated in pieces equals the stream
+concatenated, and that per-channel blocks stay consistent while the range
+grows (description); key-block scales that never change once written.
 """
 import numpy as np
 import pytest
@@ -70,8 +70,8 @@ def test_counters_match_closed_form_every_T(oracle_lib, S, R, G):
 @pytest.mark.parametrize("chunks", [[1] * 300, [300], [7, 64, 1, 128, 100], [36, 1, 263], [4, 33, 31, 232]])
 @pytest.mark.parametrize("window", [0, 64])
 def test_bulk_equals_sequential(oracle_lib, chunks, window):
-    """tract #2458: "accumulation vs a plain concat" — any chunking of the same
-    stream yields the same bytes."""
+    """tract #2458 (its test that accumulating a stream matches concatenating
+    it): any chunking of the same stream yields the same bytes."""
     p = P(oracle_lib, window=window, max_tokens=0 if window else 300)
     k, v = stream(p, 300, seed=3)
     ref = oracle_lib.Cache(p)
