@@ -97,7 +97,7 @@ struct Args {
   __half* out;
   float* partials;      // [B * nq * h_q][stride][d + 4]: o[d], m, l, 2 pad
   unsigned* counters;   // [units]: CTAs finished per unit
-  unsigned* error;      // kErrCopy | kErrSlot
+  unsigned* error;      // kErrCopy | kErrSlot (debug builds also kErrIndex | kErrNonFinite)
   unsigned long long wait_ns;   // how long a warp waits for a copy before it gives up (kErrCopy)
   DecodePlan plan;
   int32_t ns;           // copy stages per warp
@@ -195,12 +195,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Waits for a barrier phase, suspended rather than spinning (a spinning warp
-// would take issue slots from the warps that compute); gives up once the wait
-// has lasted `limit_ns` and reports false.
-// A limit of 1 ns gives up at once unless the phase is already complete (a
-// test of the expiry path: the copies still arrive, and the try_wait forms
-// may suspend the thread until they do).
+// Waits for a barrier phase: one non-blocking test first (the usual case: the
+// copy landed while the warp computed), then suspended rather than spinning
+// (a spinning warp would take issue slots from the warps that compute); gives
+// up once the wait has lasted `limit_ns` and reports false.  A limit of 1 ns
+// gives up at once unless the phase is already complete (a test of the expiry
+// path: the copies still arrive, and the try_wait forms may suspend the
+// thread until they do).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile("{\n\t.reg .pred p;\n\t"
@@ -210,8 +211,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
-  if (limit_ns <= 1) return mbar_test_wait(bar, parity);
-  if (limit_ns >= kWaitNs && mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
+  if (limit_ns <= 1) return false;
   const uint32_t hint = limit_ns < 1000000ull ? static_cast<uint32_t>(limit_ns) : 1000000u;
   const unsigned long long t0 = global_ns();
   for (;;) {
@@ -273,6 +274,14 @@ __device__ __forceinline__ void bulk_load_if(bool pred, uint32_t dst, const void
                "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %2;\n\t"
                "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "r"(static_cast<uint32_t>(pred)) : "memory");
+}
+
+// An arrival that completes the stage's phase with no copy (a debug build's
+// skipped copy whose address failed its check).
+__device__ __forceinline__ void mbar_arrive_if(bool pred, uint32_t bar) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+               "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}"
+               :: "r"(bar), "r"(static_cast<uint32_t>(pred)) : "memory");
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -543,6 +552,10 @@ __device__ __forceinline__ void publish(const Args& a, int64_t head, int ch, int
   if (total == 1) {
     a.out[head * D + ch] = __float2half_rn(L > 0.f ? O / L : 0.f);
   } else {
+    if (kDebugChecks && (cslot < 0 || cslot >= a.stride)) {   // a record outside the head's stride
+      atomicOr(a.error, kErrIndex);
+      return;
+    }
     float* dst = a.partials + (head * a.stride + cslot) * (D + 4);
     dst[ch] = O;
     if (ch == 0) { dst[D] = M; dst[D + 1] = L; }
@@ -815,6 +828,26 @@ struct RopeCodes {
       w[0] >>= sh;   // bits crossing from the high half into the low one are masked off below
     }
   }
+  // the two codes of local pair k (channels RS c + 2k, + 1) in the low and
+  // high halves of one word, each at bit pair_shift(k) of its half: the fp16
+  // subnormals code 2^(pair_shift(k) - 24), which convert to fp32 exactly
+  __device__ static constexpr int pair_shift(int k) {
+    return kStream ? 0 : (BITS * (k % (16 / BITS)) + BITS <= 10 ? BITS * (k % (16 / BITS))
+                                                                  : BITS * (k % (16 / BITS)) - 8);
+  }
+  __device__ static uint32_t pair_h(const uint32_t (&w)[NW], int k) {
+    constexpr uint32_t M = (1u << BITS) - 1u;
+    if constexpr (kStream) {
+      const int bit = 2 * BITS * k, wi = bit >> 5, s = bit & 31;
+      const uint32_t t = (s + 2 * BITS <= 32 || wi + 1 >= NW) ? (w[wi] >> s) : __funnelshift_r(w[wi], w[wi + 1], s);
+      return (t & M) | ((t << (16 - BITS)) & (M << 16));
+    } else {
+      constexpr int PPW = 16 / BITS;
+      const int s = BITS * (k % PPW);
+      const uint32_t x = w[k / PPW];
+      return s + BITS <= 10 ? x & ((M * 0x00010001u) << s) : (x >> 8) & ((M * 0x00010001u) << (s - 8));
+    }
+  }
   // the two codes of local pair k (channels RS c + 2k, + 1) as floats
   __device__ static void pair(const uint32_t (&w)[NW], int k, float& f0, float& f1) {
     constexpr uint32_t M = (1u << BITS) - 1u;
@@ -842,7 +875,7 @@ struct RopeCodes {
 // (Δ, min) rows; otab: the offset table; scs: the score scale.
 template <int D, int BITS, int CH>
 __device__ __forceinline__ void rope_chunk_scores(uint32_t qrow_s, uint32_t wrow_s, uint32_t kq, uint32_t ks, int s0,
-                                                  int sw, const float2* __restrict__ otab, int G, float scs,
+                                                  int sw, const float4* __restrict__ otab, int G, float scs,
                                                   float (&sv)[CH / 8]) {
   using RC = RopeCodes<D, BITS>;
   constexpr int RS = Rope<D>::kRS, H = D / 2, TPL = CH / 8, NT = TPL / 2, RK = D * BITS / 8, NW = RC::NW;
@@ -869,8 +902,11 @@ __device__ __forceinline__ void rope_chunk_scores(uint32_t qrow_s, uint32_t wrow
     const int i = RS * c + 2 * kc;
     uint32_t b0, b1;
     rope_fold_kc<D>(b0, b1, kc, qrow_s, wrow_s, c, (r & 1) != 0);
-    const float2 da = h2f(lds32(ks + 2 * i));
-    const float2 db = h2f(lds32(ks + 2 * (i + H)));
+    // Δ scaled by 2^(24 - pair_shift): the codes arrive as fp16 subnormals
+    const float sk = __uint_as_float(static_cast<uint32_t>(127 + 24 - RC::pair_shift(kc)) << 23);
+    float2 da = h2f(lds32(ks + 2 * i));
+    float2 db = h2f(lds32(ks + 2 * (i + H)));
+    da.x *= sk; da.y *= sk; db.x *= sk; db.y *= sk;
     const float2 ma = h2f(lds32(ks + 2 * D + 2 * i));
     const float2 mb = h2f(lds32(ks + 2 * D + 2 * (i + H)));
 #pragma unroll
@@ -879,12 +915,11 @@ __device__ __forceinline__ void rope_chunk_scores(uint32_t qrow_s, uint32_t wrow
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int j = s0 + TPL * r + 2 * v2 + (e ^ sw);   // the token's offset in its group
-        float x0, x1, y0, y1;
-        RC::pair(w[v2][e][0], kc, x0, x1);
-        RC::pair(w[v2][e][1], kc, y0, y1);
-        x0 = fmaf(x0, da.x, ma.x); x1 = fmaf(x1, da.y, ma.y);
-        y0 = fmaf(y0, db.x, mb.x); y1 = fmaf(y1, db.y, mb.y);
-        const float2 r0 = __ldg(otab + i * (G + 1) + j), r1 = __ldg(otab + (i + 1) * (G + 1) + j);
+        const float2 xc = h2f(RC::pair_h(w[v2][e][0], kc)), yc = h2f(RC::pair_h(w[v2][e][1], kc));
+        const float x0 = fmaf(xc.x, da.x, ma.x), x1 = fmaf(xc.y, da.y, ma.y);
+        const float y0 = fmaf(yc.x, db.x, mb.x), y1 = fmaf(yc.y, db.y, mb.y);
+        const float4 rr = __ldg(otab + (i / 2) * (G + 1) + j);   // (cos, sin) / 2 of pairs i and i + 1
+        const float2 r0 = make_float2(rr.x, rr.y), r1 = make_float2(rr.z, rr.w);
         // R(φ) (x, y) = (c x - s y, s x + c y), halved by the table
         const float u0 = fmaf(r0.x, x0, -r0.y * y0), v0 = fmaf(r0.y, x0, r0.x * y0);
         const float u1 = fmaf(r1.x, x1, -r1.y * y1), v1 = fmaf(r1.y, x1, r1.x * y1);
@@ -1145,7 +1180,9 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         uint32_t slot = f_slot0(p_k) + static_cast<uint32_t>(pos);
         if (ring_slots && slot >= n_slots) slot -= n_slots;
         sts32_if(leader, ring_s + 4 * p_st, 2 * p_rel);
-        bulk_load_if(leader, dst, p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes, blk_bytes, bar);
+        const uint8_t* src = p_unit + g.groups + static_cast<int64_t>(slot) * g.block_bytes;
+        if (dbg_in_region(g, src, blk_bytes)) bulk_load_if(leader, dst, src, blk_bytes, bar);
+        else mbar_arrive_if(leader, bar);
       } else {                // a tail chunk: key rows then value rows
         const TailChunk tk = tail_chunk(pos - p_nvis, f_sink(p_k), f_res(p_k), fresh);
         if (tk.n == 0) {
@@ -1159,19 +1196,32 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
             bulk_copy(dst + 16 * D, a.plan.v_fresh + row, 2 * D, bar);
           } else if (tk.sink) {
             const uint32_t bytes = static_cast<uint32_t>(tk.n) * D * 4;
-            bulk_arm(bar, 2 * bytes);
-            bulk_copy(dst, p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
-            bulk_copy(dst + 16 * D, p_unit + g.sink_v + static_cast<int64_t>(tk.first) * D * 4, bytes, bar);
+            const uint8_t* sk = p_unit + g.sink_k + static_cast<int64_t>(tk.first) * D * 4;
+            const uint8_t* sv = p_unit + g.sink_v + static_cast<int64_t>(tk.first) * D * 4;
+            if (dbg_in_region(g, sk, bytes) && dbg_in_region(g, sv, bytes)) {
+              bulk_arm(bar, 2 * bytes);
+              bulk_copy(dst, sk, bytes, bar);
+              bulk_copy(dst + 16 * D, sv, bytes, bar);
+            } else {
+              mbar_arrive_if(true, bar);
+            }
           } else {
             int s0 = f_rs0(p_k) + tk.first;
             if (s0 >= g.R) s0 -= g.R;
             const int n1 = min(tk.n, g.R - s0), n2 = tk.n - n1;   // the ring may wrap
-            bulk_arm(bar, static_cast<uint32_t>(tk.n) * D * 4);
-            bulk_copy(dst, p_unit + g.res_k + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
-            bulk_copy(dst + 16 * D, p_unit + g.res_v + static_cast<int64_t>(s0) * D * 2, n1 * D * 2, bar);
-            if (n2 > 0) {
-              bulk_copy(dst + n1 * D * 2, p_unit + g.res_k, n2 * D * 2, bar);
-              bulk_copy(dst + 16 * D + n1 * D * 2, p_unit + g.res_v, n2 * D * 2, bar);
+            const uint8_t* rk = p_unit + g.res_k + static_cast<int64_t>(s0) * D * 2;
+            const uint8_t* rv = p_unit + g.res_v + static_cast<int64_t>(s0) * D * 2;
+            if (dbg_in_region(g, rk, n1 * D * 2) && dbg_in_region(g, rv, n1 * D * 2) &&
+                dbg_in_region(g, p_unit + g.res_k, n2 * D * 2) && dbg_in_region(g, p_unit + g.res_v, n2 * D * 2)) {
+              bulk_arm(bar, static_cast<uint32_t>(tk.n) * D * 4);
+              bulk_copy(dst, rk, n1 * D * 2, bar);
+              bulk_copy(dst + 16 * D, rv, n1 * D * 2, bar);
+              if (n2 > 0) {
+                bulk_copy(dst + n1 * D * 2, p_unit + g.res_k, n2 * D * 2, bar);
+                bulk_copy(dst + 16 * D + n1 * D * 2, p_unit + g.res_v, n2 * D * 2, bar);
+              }
+            } else {
+              mbar_arrive_if(true, bar);
             }
           }
         }
@@ -1386,17 +1436,18 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         const int hh = kk / (D / 8), idx = kk % (D / 8);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (hh < nh) v = *reinterpret_cast<const uint4*>(src + hh * D * 2 + idx * 16);
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-        float m = 0.f;
+        // the largest |q_c| of the row as fp16 bits (magnitudes order as
+        // their bit patterns), then its exponent
+        uint32_t mb = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+        mb = max(mb & 0xFFFFu, mb >> 16);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vw[j]));
-          m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+        for (int o = 1; o < D / 8; o <<= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));   // the row's chunks
+        // m in [2^(e-1), 2^e) for m > 1: m 2^-e below 1
+        const int e = mb > 0x3C00u ? static_cast<int>(mb >> 10) - 14 : 0;
+        if constexpr (kDebugChecks) {
+          if (mb >= 0x7C00u) atomicOr(a.error, kErrNonFinite);   // an inf or NaN query element
         }
-#pragma unroll
-        for (int o = 1; o < D / 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));   // the row's chunks
-        int e = 0;
-        if (m > 1.f) frexpf(m, &e);                  // m in [2^(e-1), 2^e): m 2^-e below 1
         if (e > 0) {
           // 2^-e as an fp16 pair (e <= 16: a normal number or a subnormal)
           const uint32_t h = e <= 14 ? static_cast<uint32_t>(15 - e) << 10 : 1u << (24 - e);
@@ -1476,7 +1527,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         if constexpr (ROPE) {
           rope_chunk_scores<D, BITS, CH>(smem_addr(qw + hh_col * Rope<D>::kQRow), smem_addr(wrow),
                                          blk + static_cast<uint32_t>(g.blk_kq), blk + static_cast<uint32_t>(g.blk_ks),
-                                         s0, sw, reinterpret_cast<const float2*>(rtab + D), g.G, scs, sv);
+                                         s0, sw, reinterpret_cast<const float4*>(rtab + D), g.G, scs, sv);
         } else {
           const uint32_t rowa = blk + o_k0 + s0 * RK, rowb = blk + o_k1 + s0 * RK;
           chunk_scores<D, BITS, CH>(bq, rowa, rowb, scs, cst_h, sw, ksh, sv);
@@ -1706,7 +1757,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
                                      : g.S + (f_gfirst(c_k) + f_nvis(c_k)) * g.G + tk.first;
         rope_angles<D>(wrow, rtab, a_b);
         const uint32_t qrow_s = smem_addr(qw + hh_col * Rope<D>::kQRow), wrow_s = smem_addr(wrow);
-        const float2* otab = reinterpret_cast<const float2*>(rtab + D);
+        const float4* otab = reinterpret_cast<const float4*>(rtab + D);
         constexpr int RS = Rope<D>::kRS, H = D / 2;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1722,7 +1773,8 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
               xa = h2f(*reinterpret_cast<const uint32_t*>(kst + (r * D + i) * 2));
               xb = h2f(*reinterpret_cast<const uint32_t*>(kst + (r * D + i + H) * 2));
             }
-            const float2 r0 = __ldg(otab + i * (g.G + 1) + r), r1 = __ldg(otab + (i + 1) * (g.G + 1) + r);
+            const float4 rr = __ldg(otab + (i / 2) * (g.G + 1) + r);
+            const float2 r0 = make_float2(rr.x, rr.y), r1 = make_float2(rr.z, rr.w);
             const float u0 = fmaf(r0.x, xa.x, -r0.y * xb.x), v0 = fmaf(r0.y, xa.x, r0.x * xb.x);
             const float u1 = fmaf(r1.x, xa.y, -r1.y * xb.y), v1 = fmaf(r1.y, xa.y, r1.x * xb.y);
             ah0 = rope_split(u0, u1, false); al0 = rope_split(u0, u1, true);
@@ -1834,14 +1886,16 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         for (int part = 0; part < 2; ++part) {
           for (int e = 4 * lane; e < D; e += 128) {
             const uint2 x = *reinterpret_cast<const uint2*>(kst + part * 16 * D + 2 * e);
+            dbg_check_finite(g, make_uint4(x.x, x.y, 0u, 0u));
             if (fp < g.S) {
               const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
               const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
-              *reinterpret_cast<float4*>(base + (part ? g.sink_v : g.sink_k) + (fp * D + e) * 4) =
-                  make_float4(f0.x, f0.y, f1.x, f1.y);
+              uint8_t* dsk = base + (part ? g.sink_v : g.sink_k) + (fp * D + e) * 4;
+              if (dbg_in_region(g, dsk, 16)) *reinterpret_cast<float4*>(dsk) = make_float4(f0.x, f0.y, f1.x, f1.y);
             } else {
               const int64_t slot = (fp - g.S) % g.R;
-              *reinterpret_cast<uint2*>(base + (part ? g.res_v : g.res_k) + (slot * D + e) * 2) = x;
+              uint8_t* drs = base + (part ? g.res_v : g.res_k) + (slot * D + e) * 2;
+              if (dbg_in_region(g, drs, 8)) *reinterpret_cast<uint2*>(drs) = x;
             }
           }
         }

@@ -5,11 +5,12 @@
 //
 // Layout (floats): [theta]  θ_i = base^(-2i/d) for i < d/2 as two floats,
 // hi = fl(θ_i) and lo = fl(θ_i - hi), so that a θ_i can be reduced mod 2π in
-// fp32 without losing the product's low bits; then [offsets] for every pair
-// i and token offset j < G inside a group, 0.5 (cos jθ_i, sin jθ_i) at float2
-// index i (G + 1) + j (the extra column keeps a warp's reads on distinct
-// banks; its value is zero).  The factor 0.5 keeps rotated keys of the full
-// fp16 range inside fp16; the decode takes it back with its score scale.
+// fp32 without losing the product's low bits; then [offsets] for every even
+// pair i and token offset j < G inside a group, 0.5 (cos jθ_i, sin jθ_i,
+// cos jθ_(i+1), sin jθ_(i+1)) at float4 index (i / 2) (G + 1) + j (a lane
+// turns two adjacent pairs of one token with one 16-byte load; the extra
+// column j = G is zero).  The factor 0.5 keeps rotated keys of the full fp16
+// range inside fp16; the decode takes it back with its score scale.
 #include "kivi_internal.cuh"
 
 #include <math.h>
@@ -27,14 +28,16 @@ __global__ void rope_table_kernel(float* tab, double log2_base, int d, int G) {
     tab[2 * x] = hi;
     tab[2 * x + 1] = static_cast<float>(th - static_cast<double>(hi));
   }
-  if (x < h * (G + 1)) {
-    const int i = x / (G + 1), j = x % (G + 1);
-    float2 v = make_float2(0.f, 0.f);
+  if (x < (h / 2) * (G + 1)) {
+    const int p = x / (G + 1), j = x % (G + 1);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (j < G) {
-      const double a = static_cast<double>(j) * exp2(-(2.0 * i / d) * log2_base);
-      v = make_float2(static_cast<float>(0.5 * cos(a)), static_cast<float>(0.5 * sin(a)));
+      const double a0 = static_cast<double>(j) * exp2(-(2.0 * (2 * p) / d) * log2_base);
+      const double a1 = static_cast<double>(j) * exp2(-(2.0 * (2 * p + 1) / d) * log2_base);
+      v = make_float4(static_cast<float>(0.5 * cos(a0)), static_cast<float>(0.5 * sin(a0)),
+                      static_cast<float>(0.5 * cos(a1)), static_cast<float>(0.5 * sin(a1)));
     }
-    reinterpret_cast<float2*>(tab + d)[x] = v;
+    reinterpret_cast<float4*>(tab + d)[x] = v;
   }
 }
 
