@@ -835,11 +835,12 @@ struct RopeCodes {
     return kStream ? 0 : (BITS * (k % (16 / BITS)) + BITS <= 10 ? BITS * (k % (16 / BITS))
                                                                   : BITS * (k % (16 / BITS)) - 8);
   }
-  __device__ static uint32_t pair_h(const uint32_t (&w)[NW], int k) {
+  template <int N>
+  __device__ static uint32_t pair_h(const uint32_t (&w)[N], int k) {
     constexpr uint32_t M = (1u << BITS) - 1u;
     if constexpr (kStream) {
       const int bit = 2 * BITS * k, wi = bit >> 5, s = bit & 31;
-      const uint32_t t = (s + 2 * BITS <= 32 || wi + 1 >= NW) ? (w[wi] >> s) : __funnelshift_r(w[wi], w[wi + 1], s);
+      const uint32_t t = (s + 2 * BITS <= 32 || wi + 1 >= N) ? (w[wi] >> s) : __funnelshift_r(w[wi], w[wi + 1], s);
       return (t & M) | ((t << (16 - BITS)) & (M << 16));
     } else {
       constexpr int PPW = 16 / BITS;
@@ -883,15 +884,21 @@ __device__ __forceinline__ void rope_chunk_scores(uint32_t qrow_s, uint32_t wrow
   uint32_t roff;
   int rsh;
   RC::where(c, roff, rsh);
-  // the code regions of the lane's tokens: tile v2, token e (A row r or r + 8), half
-  uint32_t w[NT][2][2][NW];
+  // the code regions of the lane's tokens: tile v2, token e (A row r or r + 8),
+  // half.  Bit streams load a region's words up front; the word rule loads
+  // each word when its first pair comes up (fewer live registers)
+  constexpr int PPW = RC::kStream ? 1 : 16 / BITS;   // pairs per word (word rule)
+  uint32_t w[NT][2][2][RC::kStream ? NW : 1];
+  uint32_t rows[NT][2];
 #pragma unroll
   for (int v2 = 0; v2 < NT; ++v2) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const uint32_t row = kq + static_cast<uint32_t>((s0 + TPL * r + 2 * v2 + (e ^ sw)) * RK) + roff;
-      RC::load(w[v2][e][0], row, rsh);
-      RC::load(w[v2][e][1], row + RC::kHalfBytes, rsh);
+      rows[v2][e] = kq + static_cast<uint32_t>((s0 + TPL * r + 2 * v2 + (e ^ sw)) * RK) + roff;
+      if constexpr (RC::kStream) {
+        RC::load(w[v2][e][0], rows[v2][e], rsh);
+        RC::load(w[v2][e][1], rows[v2][e] + RC::kHalfBytes, rsh);
+      }
     }
   }
   float acc[NT][4];
@@ -909,13 +916,29 @@ __device__ __forceinline__ void rope_chunk_scores(uint32_t qrow_s, uint32_t wrow
     da.x *= sk; da.y *= sk; db.x *= sk; db.y *= sk;
     const float2 ma = h2f(lds32(ks + 2 * D + 2 * i));
     const float2 mb = h2f(lds32(ks + 2 * D + 2 * (i + H)));
+    if constexpr (!RC::kStream) {
+      if (kc % PPW == 0) {   // the words holding pairs kc .. kc + PPW - 1
+#pragma unroll
+        for (int v2 = 0; v2 < NT; ++v2) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            uint32_t x0 = lds32(rows[v2][e] + 4 * (kc / PPW));
+            uint32_t x1 = lds32(rows[v2][e] + RC::kHalfBytes + 4 * (kc / PPW));
+            if constexpr (RS * BITS < 32) { x0 >>= rsh; x1 >>= rsh; }
+            w[v2][e][0][0] = x0;
+            w[v2][e][1][0] = x1;
+          }
+        }
+      }
+    }
 #pragma unroll
     for (int v2 = 0; v2 < NT; ++v2) {
       uint32_t ah[4], al[4];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int j = s0 + TPL * r + 2 * v2 + (e ^ sw);   // the token's offset in its group
-        const float2 xc = h2f(RC::pair_h(w[v2][e][0], kc)), yc = h2f(RC::pair_h(w[v2][e][1], kc));
+        const int kk = RC::kStream ? kc : kc % PPW;        // the pair within the loaded word(s)
+        const float2 xc = h2f(RC::pair_h(w[v2][e][0], kk)), yc = h2f(RC::pair_h(w[v2][e][1], kk));
         const float x0 = fmaf(xc.x, da.x, ma.x), x1 = fmaf(xc.y, da.y, ma.y);
         const float y0 = fmaf(yc.x, db.x, mb.x), y1 = fmaf(yc.y, db.y, mb.y);
         const float4 rr = __ldg(otab + (i / 2) * (G + 1) + j);   // (cos, sin) / 2 of pairs i and i + 1
