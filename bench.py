@@ -402,11 +402,7 @@ def run_ours(args, rank, world, device):
         # flush launch when any of them freezes a group)
         runs = [b for b in range(w.batch) if b == 0 or T_now[r][b] != T_now[r][b - 1]]
         freezes = [state_at(w, T_now[r][b0] + 1)[1] > state_at(w, T_now[r][b0])[1] for b0 in runs]
-        if (w.bits not in (2, 4, 8) and w.head_dim != 128) or w.rope_base:
-            # the CUDA-core decode (bit-stream widths at head dim 64, pre-RoPE
-            # keys): per run, append (flush, write) + decode
-            launches = sum((2 if f else 1) + 1 for f in freezes)
-        elif not fused:   # kivi_append, one launch pair (flush, write) per run, then the decode
+        if not fused:   # kivi_append, one launch pair (flush, write) per run, then the decode
             launches = sum(2 if f else 1 for f in freezes) + -(-len(runs) // 64)
         else:
             launches = sum(1 + (1 if any(freezes[i:i + 64]) else 0) for i in range(0, len(runs), 64))

@@ -71,8 +71,8 @@ int validate(const kivi_params* p) {
   // the outlier corrections are built into the tensor-core decode at 2 to 4
   // bits with 32-token chunks
   if (p->outlier_permille > 0 && (p->bits < 2 || p->bits > 4 || p->group % 32 != 0)) return KIVI_EINVAL;
-  // pre-RoPE keys decode on CUDA cores (a group in one warp's shared memory,
-  // value rows whole 32-bit words), without outlier tables
+  // pre-RoPE keys: 32-token chunks (a key's rotation pairs sit in one lane's
+  // two regions; value rows whole 32-bit words), without outlier tables
   if (!(p->rope_base == 0.0 || (p->rope_base > 1.0 && p->rope_base <= 1e7))) return KIVI_EINVAL;
   if (p->rope_base != 0.0 && ((p->group != 32 && p->group != 64) || p->outlier_permille != 0)) return KIVI_EINVAL;
   return KIVI_OK;

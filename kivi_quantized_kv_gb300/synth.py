@@ -90,7 +90,8 @@ WORKLOADS = {
     # rotates each key at its position inside the decode
     "gqa8b_b4_prerope": Workload("gqa8b_b4_prerope", batch=4, h_q=32, h_kv=8, head_dim=128, tokens=32768, bits=4,
                                  group=32, residual=128, sinks=4, rope=False, rope_base=10000.0),
-    # head dim 64 at 3 bits: the CUDA-core decode of the bit-stream widths
+    # head dim 64 at 3 bits: a bit-stream width whose key quarters may start
+    # on a 16-bit boundary
     "mha_d64_b3": Workload("mha_d64_b3", batch=8, h_q=32, h_kv=32, head_dim=64, tokens=4096, bits=3,
                            group=32, residual=128, sinks=4),
 }

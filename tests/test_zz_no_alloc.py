@@ -47,8 +47,8 @@ def _filled_cache(cfg, T, seed):
 @pytest.mark.parametrize("shape", [
     dict(bits=4, group=32, residual=128, sinks=4, h_q=32, h_kv=8, head_dim=128, batch=4, max_tokens=3000),
     dict(bits=2, group=32, residual=64, sinks=1, h_q=8, h_kv=8, head_dim=64, batch=2, max_tokens=0, window=300),
-    # a bit-stream width at head dim 64: the CUDA-core decode, whose split
-    # count the fixed scratch clamps
+    # a bit-stream width at head dim 64 (unaligned key quarters), with a
+    # split count the fixed scratch clamps
     dict(bits=3, group=32, residual=64, sinks=4, h_q=8, h_kv=4, head_dim=64, batch=3, max_tokens=3000),
 ])
 @pytest.mark.parametrize("ragged", [False, True])
