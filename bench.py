@@ -796,8 +796,10 @@ def run_prefill(args, device):
 def run_e2e(args, caches, new_kv, w, device, stream):
     """The same step through the public API with host buffers: one
     kivi_append_decode_attn_host call per step (kivi_append on a device copy
-    + kivi_decode_attn_host with --unfused), which copies the step's pinned
-    host K/V and q in and the output back, all inside the timed region."""
+    + kivi_decode_attn_host with --unfused).  The step's K/V and q sit in
+    pinned host memory and the output goes back to pinned host memory: the
+    step reads the inputs over the host mapping and its merge writes the
+    output there, every step, inside the timed region."""
     import ctypes
     import torch
     from kivi_quantized_kv_gb300 import _abi
@@ -844,7 +846,8 @@ def run_e2e(args, caches, new_kv, w, device, stream):
     h2d = (2 * w.batch * w.h_kv + w.batch * w.h_q) * w.head_dim * 2
     d2h = w.batch * w.h_q * w.head_dim * 2
     return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "transfer": "the step reads the pinned host inputs and writes the output to pinned host memory over the host mapping"}
 
 
 # --------------------------------------------------------------- oracle arm

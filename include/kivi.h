@@ -275,20 +275,27 @@ int kivi_decode_attn(kivi_cache* cache, const void* q, void* out, void* cuda_str
 int kivi_append_decode_attn(kivi_cache* cache, const void* k_new, const void* v_new, const void* q, void* out,
                             void* cuda_stream);
 
-/* Same as kivi_append_decode_attn with host-resident k_new, v_new, q and out
- * (pinned host memory gives asynchronous copies): copies the inputs into the
- * arena's staging area, runs the step, copies the result back to out_host,
- * all on `stream`; the call returns once the work is queued (synchronise the
- * stream before reading out_host or reusing the input buffers).  Errors: as
- * kivi_append_decode_attn. */
+/* Same as kivi_append_decode_attn with host-resident k_new, v_new, q and out.
+ * When all four are pinned host memory mapped into the device's address
+ * space (cudaHostAlloc / cudaMallocHost / cudaHostRegister under unified
+ * addressing) and 16-byte aligned, the step reads the inputs over that
+ * mapping and writes its output straight to out_host (no copy engine
+ * involved; for bit-stream widths, outlier tables and pre-RoPE keys one extra
+ * launch first gathers the inputs into the arena's staging area); otherwise
+ * (pageable memory) the call copies the inputs into the staging area, runs
+ * the step and copies the result back to out_host.  Everything is queued on `stream`, in stream
+ * order.  Either way the call returns once the work is
+ * queued: synchronise the stream before reading out_host or reusing the input
+ * buffers.  Errors: as kivi_append_decode_attn. */
 int kivi_append_decode_attn_host(kivi_cache* cache, const void* k_host, const void* v_host, const void* q_host,
                                  void* out_host, void* cuda_stream);
 
-/* Same as kivi_decode_attn with host-resident q and out (pinned host memory
- * gives asynchronous copies): copies q into the arena's staging area, runs
- * the decode, copies the result back to out_host, all on `stream`.  The call
- * returns once the work is queued; synchronise the stream before reading
- * out_host.  Errors: as kivi_decode_attn. */
+/* Same as kivi_decode_attn with host-resident q and out: a pinned, mapped,
+ * 16-byte aligned q is read over the mapping and the output written straight
+ * to out_host; other memory is staged through the arena with copies on
+ * `stream` (as kivi_append_decode_attn_host).  The call returns once the work is
+ * queued; synchronise the stream before reading out_host.  Errors: as
+ * kivi_decode_attn. */
 int kivi_decode_attn_host(kivi_cache* cache, const void* q_host, void* out_host, void* cuda_stream);
 
 /* Causal attention of the n_queries newest tokens of every sequence over the

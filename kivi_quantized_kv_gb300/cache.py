@@ -172,8 +172,9 @@ class KiviCache:
 
     def append_decode_host(self, k_host: torch.Tensor, v_host: torch.Tensor, q_host: torch.Tensor,
                            out_host: torch.Tensor, stream=None) -> torch.Tensor:
-        """append_decode with host-resident tensors (pin them for asynchronous
-        copies); the copies and the step are queued on `stream`."""
+        """append_decode with host-resident tensors, queued on `stream`: pinned
+        tensors are read and written by the step over the host mapping;
+        pageable tensors are staged through the arena with copies."""
         c = self.cfg
         shapes = ((k_host, (c.batch, c.h_kv, 1, c.head_dim), "k_host"), (v_host, (c.batch, c.h_kv, 1, c.head_dim), "v_host"),
                   (q_host, (c.batch, c.h_q, c.head_dim), "q_host"), (out_host, (c.batch, c.h_q, c.head_dim), "out_host"))
@@ -187,8 +188,9 @@ class KiviCache:
         return out_host
 
     def decode_host(self, q_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> torch.Tensor:
-        """Host-resident q and out (pin them for asynchronous copies); the
-        copies and the decode are queued on `stream`."""
+        """Host-resident q and out, queued on `stream`: pinned tensors are read
+        and written by the decode over the host mapping; pageable tensors are
+        staged with copies."""
         c = self.cfg
         shape = (c.batch, c.h_q, c.head_dim)
         for t, what in ((q_host, "q_host"), (out_host, "out_host")):

@@ -10,13 +10,13 @@ namespace kivi {
 namespace mma {
 
 // the kernel of an instantiation
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false, bool HIO = false>
 constexpr auto kernel_of() {
-  if constexpr (RG) return decode_mma_ragged_kernel<D, BITS, CH, MQ, OUTL, ROPE>;
-  else return decode_mma_kernel<D, BITS, CH, MQ, false, OUTL, ROPE>;
+  if constexpr (RG) return decode_mma_ragged_kernel<D, BITS, CH, MQ, OUTL, ROPE, HIO>;
+  else return decode_mma_kernel<D, BITS, CH, MQ, false, OUTL, ROPE, HIO>;
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false, bool HIO = false>
 cudaError_t prepare() {
   // opt in to the largest dynamic shared memory once per instantiation
   static std::atomic<int> done{0};
@@ -27,18 +27,18 @@ cudaError_t prepare() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>());
+  e = cudaFuncGetAttributes(&fa, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE, HIO>());
   if (e != cudaSuccess) return e;
   // the opt-in limit covers static + dynamic shared memory
-  e = cudaFuncSetAttribute(kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE, HIO>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            optin - static_cast<int>(fa.sharedSizeBytes));
   if (e == cudaSuccess) done.store(1, std::memory_order_release);
   return e;
 }
 
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false, bool HIO = false>
 cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
-  cudaError_t e = prepare<D, BITS, CH, MQ, RG, OUTL, ROPE>();
+  cudaError_t e = prepare<D, BITS, CH, MQ, RG, OUTL, ROPE, HIO>();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the CTAs may start (and set up their
   // shared memory) while the previous kernel in the stream drains; the kernel
@@ -53,8 +53,8 @@ cudaError_t launch_one(const Args& a, const RunTableT<RG>& rt, dim3 grid, int th
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if constexpr (RG) e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>(), a, rt);
-  else e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE>(), a);
+  if constexpr (RG) e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE, HIO>(), a, rt);
+  else e = cudaLaunchKernelEx(&cfg, kernel_of<D, BITS, CH, MQ, RG, OUTL, ROPE, HIO>(), a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -71,14 +71,14 @@ int occupancy_one(int threads, int smem) {
 
 // one instantiation per (head dim, chunk of the group, several query tokens,
 // ragged)
-template <int BITS, bool MQ, bool RG>
+template <int BITS, bool MQ, bool RG, bool HIO = false>
 cudaError_t launch_mq(const Args& a, const RunTableT<RG>& rt, dim3 grid, int threads, int smem, cudaStream_t s) {
   const bool ch32 = (a.g.G % 32) == 0;
   if (a.g.d == 64)
-    return ch32 ? launch_one<64, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s)
-                : launch_one<64, BITS, 16, MQ, RG>(a, rt, grid, threads, smem, s);
-  return ch32 ? launch_one<128, BITS, 32, MQ, RG>(a, rt, grid, threads, smem, s)
-              : launch_one<128, BITS, 16, MQ, RG>(a, rt, grid, threads, smem, s);
+    return ch32 ? launch_one<64, BITS, 32, MQ, RG, false, false, HIO>(a, rt, grid, threads, smem, s)
+                : launch_one<64, BITS, 16, MQ, RG, false, false, HIO>(a, rt, grid, threads, smem, s);
+  return ch32 ? launch_one<128, BITS, 32, MQ, RG, false, false, HIO>(a, rt, grid, threads, smem, s)
+              : launch_one<128, BITS, 16, MQ, RG, false, false, HIO>(a, rt, grid, threads, smem, s);
 }
 
 // bit-stream widths: 32-token chunks only (a lane's 8 codes of a value row
@@ -99,6 +99,8 @@ cudaError_t launch_bits(const Args& a, dim3 grid, int threads, int smem, cudaStr
     return a.plan.q_rows > 1 ? launch_stream<BITS, true, false>(a, none, grid, threads, smem, s)
                              : launch_stream<BITS, false, false>(a, none, grid, threads, smem, s);
   } else {
+    // host-io instantiations: the word-rule widths, one query token
+    if (a.plan.host_io && a.plan.q_rows == 1) return launch_mq<BITS, false, false, true>(a, none, grid, threads, smem, s);
     return a.plan.q_rows > 1 ? launch_mq<BITS, true, false>(a, none, grid, threads, smem, s)
                              : launch_mq<BITS, false, false>(a, none, grid, threads, smem, s);
   }
@@ -109,6 +111,7 @@ template <int BITS>
 cudaError_t launch_bits_ragged(const Args& a, const RunTable& rt, dim3 grid, int threads, int smem,
                                cudaStream_t s) {
   if constexpr (stream_bits<BITS>()) return launch_stream<BITS, false, true>(a, rt, grid, threads, smem, s);
+  else if (a.plan.host_io) return launch_mq<BITS, false, true, true>(a, rt, grid, threads, smem, s);
   else return launch_mq<BITS, false, true>(a, rt, grid, threads, smem, s);
 }
 

@@ -284,6 +284,20 @@ __device__ __forceinline__ void mbar_arrive_if(bool pred, uint32_t bar) {
                :: "r"(bar), "r"(static_cast<uint32_t>(pred)) : "memory");
 }
 
+// A warp copies `bytes` (a multiple of 16) from global memory into shared
+// memory with plain 16-byte loads (the host-io instantiations: pinned host
+// memory mapped into the device, read over the chip-to-chip link); the caller
+// then completes the stage.  Out of line: it takes no registers from the loop.
+static __device__ __noinline__ void warp_copy16(uint8_t* dst, const void* src, int bytes) {
+  const int lane = threadIdx.x & 31;
+  const uint4* s = static_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  for (int i = lane; i < bytes / 16; i += 32) d[i] = s[i];
+}
+// Orders a lane's generic-proxy writes into a stage before the bulk copies
+// (async proxy) that later reuse it.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -970,7 +984,7 @@ using RunTableT = typename std::conditional<RG, RunTable, NoRuns>::type;
 // run table `rt` (the unit's run) instead of the launch's plan.  ROPE: keys
 // stored before the rotary embedding, turned at their positions in the score
 // products (see rope_chunk_scores).
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL, bool ROPE>
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL, bool ROPE, bool HIO>
 __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& rt) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   using WS = WarpSmem<D, CH>;
@@ -1182,7 +1196,13 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         const int uq = u_first + p_u;
         const int nh_q = unit_rows<MQ>(a, uq);
         sts32_if(leader, ring_s + 4 * p_st, 2 * p_u + 1);
-        if constexpr (MQ) {
+        if constexpr (HIO) {   // the rows from host memory, loaded by the warp
+          uint8_t* dsts = my_stages + static_cast<size_t>(p_st) * a.stage_bytes;
+          for (int hh = 0; hh < nh_q; ++hh) warp_copy16(dsts + hh * D * 2, a.q + q_row<MQ>(a, uq, hh) * D, 2 * D);
+          fence_proxy_async();
+          __syncwarp();
+          mbar_arrive_if(leader, bar);
+        } else if constexpr (MQ) {
           if (lane == 0) {   // one copy per query row (the rows of a pass need not be adjacent)
             bulk_arm(bar, static_cast<uint32_t>(nh_q) * D * 2);
             for (int hh = 0; hh < nh_q; ++hh)
@@ -1210,6 +1230,15 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         const TailChunk tk = tail_chunk(pos - p_nvis, f_sink(p_k), f_res(p_k), fresh);
         if (tk.n == 0) {
           issued = false;     // nothing to copy or to attend to
+        } else if (HIO && tk.fresh) {   // the appended token's rows from host memory
+          const int64_t row = unit_kv(u_first + p_u) * D;
+          uint8_t* dsts = my_stages + static_cast<size_t>(p_st) * a.stage_bytes;
+          warp_copy16(dsts, a.plan.k_fresh + row, 2 * D);
+          warp_copy16(dsts + 16 * D, a.plan.v_fresh + row, 2 * D);
+          sts32_if(leader, ring_s + 4 * p_st, 2 * p_rel);
+          fence_proxy_async();
+          __syncwarp();
+          mbar_arrive_if(leader, bar);
         } else if (lane == 0) {
           ring_w[p_st] = 2 * p_rel;
           if (tk.fresh) {     // the appended token's rows, straight from the inputs
@@ -1945,17 +1974,21 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
 }
 
 // Uniform launches: the plan is the launch's own (one kernel parameter).
-template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false>
+// HIO: q, out and the fresh token's rows are pinned host memory mapped into
+// the device (the host-buffer entry points): the warps load the query and
+// fresh rows with plain loads instead of bulk copies, and the merge writes
+// the output to the host.
+template <int D, int BITS, int CH, bool MQ, bool RG, bool OUTL = false, bool ROPE = false, bool HIO = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm) decode_mma_kernel(const Args a) {
   const NoRuns none{0};
-  decode_body<D, BITS, CH, MQ, false, OUTL, ROPE>(a, none);
+  decode_body<D, BITS, CH, MQ, false, OUTL, ROPE, HIO>(a, none);
 }
 
 // Ragged launches: the runs' plans travel as a grid constant.
-template <int D, int BITS, int CH, bool MQ, bool OUTL = false, bool ROPE = false>
+template <int D, int BITS, int CH, bool MQ, bool OUTL = false, bool ROPE = false, bool HIO = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeCtasPerSm)
     decode_mma_ragged_kernel(const Args a, const __grid_constant__ RunTable rt) {
-  decode_body<D, BITS, CH, MQ, true, OUTL, ROPE>(a, rt);
+  decode_body<D, BITS, CH, MQ, true, OUTL, ROPE, HIO>(a, rt);
 }
 
 }  // namespace mma

@@ -390,7 +390,7 @@ kivi::RunTable run_table(const kivi_cache& c, const std::vector<Run>& runs, size
 // group).
 cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const __half* k_fresh,
                        const __half* v_fresh, float* partials, int32_t stride, unsigned* counters,
-                       unsigned* error, cudaStream_t s) {
+                       unsigned* error, cudaStream_t s, bool host_io = false) {
   const Geo& g = c.g;
   const bool fused = k_fresh != nullptr;
   const std::vector<Run> runs = runs_of(c);
@@ -418,6 +418,7 @@ cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const 
       pl.v_fresh = v_fresh;
       pl.fresh_pos = r.T;
     }
+    pl.host_io = host_io ? 1 : 0;
     return attn_run(c, r, pl, q, out, partials, stride, counters, error, s);
   }
   for (size_t first = 0; first < runs.size(); first += kivi::kMaxRuns) {
@@ -436,12 +437,28 @@ cudaError_t decode_all(const kivi_cache& c, const __half* q, __half* out, const 
     kivi::DecodePlan pl = plan_for(c, runs[first].T, g.B);   // launch-wide fields: the grid
     pl.k_fresh = k_fresh;
     pl.v_fresh = v_fresh;
+    pl.host_io = host_io ? 1 : 0;
     const cudaError_t e = kivi::launch_decode_ragged(g, c.arena, q, out, pl, t, partials, stride, counters, error, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 unsigned* ws_counters(const kivi_cache& c) { return reinterpret_cast<unsigned*>(c.arena + c.g.ws_counters); }
+// The host-io decode instantiations exist for the word-rule widths without
+// outlier tables or pre-RoPE keys (the other caches gather through stage.cu).
+bool host_io_kernels(const Geo& g) { return kivi::word_rule(g.bits) && g.n_out == 0 && g.rope_l2b == 0.0; }
+// The device address of a pinned host buffer mapped into the device's address
+// space (cudaHostAlloc, cudaMallocHost or cudaHostRegister under unified
+// addressing), or null for any other pointer (pageable host memory included).
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();   // not a pointer CUDA knows: clear the error
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+  return at.devicePointer;
+}
 unsigned* ws_error(const kivi_cache& c) { return reinterpret_cast<unsigned*>(c.arena + c.g.ws_error); }
 
 }  // namespace
@@ -524,6 +541,33 @@ int kivi_append_decode_attn_host(kivi_cache* c, const void* k_host, const void* 
   void* dv = c->arena + g.ws_v;
   void* dq = c->arena + g.ws_q;
   void* dout = c->arena + g.ws_out;
+  // pinned host buffers mapped into the device's address space: one launch
+  // gathers the inputs into the staging area and the decode writes its
+  // output straight to out_host; other host memory: a copy per buffer
+  const void* mk = mapped_host(k_host);
+  const void* mv = mapped_host(v_host);
+  const void* mq = mapped_host(q_host);
+  void* mo = const_cast<void*>(mapped_host(out_host));
+  const bool mapped = mk && mv && mq && mo && aligned(mk, 16) && aligned(mv, 16) && aligned(mq, 16) &&
+                      aligned(mo, 16);
+  if (mapped && host_io_kernels(g)) {
+    // the decode's host-io instantiation reads q and the fresh rows itself
+    const cudaError_t e = decode_all(*c, static_cast<const __half*>(mq), static_cast<__half*>(mo),
+                                     static_cast<const __half*>(mk), static_cast<const __half*>(mv),
+                                     ws_partials(*c), g.split_stride, ws_counters(*c), ws_error(*c), s, true);
+    if (e != cudaSuccess) return cuda_status(e);
+    for (int64_t& t : c->T) t += 1;
+    return KIVI_OK;
+  }
+  if (mapped) {
+    const void* src[3] = {mk, mv, mq};
+    void* dst[3] = {dk, dv, dq};
+    const int64_t bytes[3] = {static_cast<int64_t>(kv_bytes), static_cast<int64_t>(kv_bytes),
+                              static_cast<int64_t>(q_bytes)};
+    const cudaError_t e = kivi::launch_stage(src, dst, bytes, 3, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return kivi_append_decode_attn(c, dk, dv, dq, mo, cuda_stream);
+  }
   if (cudaMemcpyAsync(dk, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(dv, v_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(dq, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -539,6 +583,19 @@ int kivi_decode_attn_host(kivi_cache* c, const void* q_host, void* out_host, voi
   const size_t bytes = static_cast<size_t>(c->g.B) * c->g.hq * c->g.d * 2;
   void* dq = c->arena + c->g.ws_q;
   void* dout = c->arena + c->g.ws_out;
+  const void* mq = mapped_host(q_host);
+  void* mo = const_cast<void*>(mapped_host(out_host));
+  if (mq && mo && aligned(mq, 16) && aligned(mo, 16) && host_io_kernels(c->g))
+    return cuda_status(decode_all(*c, static_cast<const __half*>(mq), static_cast<__half*>(mo), nullptr, nullptr,
+                                  ws_partials(*c), c->g.split_stride, ws_counters(*c), ws_error(*c), s, true));
+  if (mq && mo && aligned(mq, 16) && aligned(mo, 16)) {   // as kivi_append_decode_attn_host
+    const void* src[1] = {mq};
+    void* dst[1] = {dq};
+    const int64_t nb[1] = {static_cast<int64_t>(bytes)};
+    const cudaError_t e = kivi::launch_stage(src, dst, nb, 1, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return kivi_decode_attn(c, dq, mo, cuda_stream);
+  }
   cudaError_t e = cudaMemcpyAsync(dq, q_host, bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return KIVI_ECUDA;
   const int st = kivi_decode_attn(c, dq, dout, cuda_stream);

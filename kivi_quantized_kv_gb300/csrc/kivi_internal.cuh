@@ -111,6 +111,11 @@ cudaError_t launch_flush(const Geo& g, uint8_t* arena, const __half* k_new, cons
 // Writes new sink tokens [T_old, min(T_new, S)) and ring tokens
 // [ring_begin, T_new) of every unit from the new input (T_new = T_old +
 // n_new; rows of n_stride tokens).
+// Copies n (at most 3) buffers of bytes[i] (multiples of 16, 16-byte aligned)
+// from src[i] to dst[i] in one launch: the host-buffer entry points gather a
+// step's inputs from pinned, device-mapped host memory this way (stage.cu).
+cudaError_t launch_stage(const void* const* src, void* const* dst, const int64_t* bytes, int n,
+                         cudaStream_t stream);
 cudaError_t launch_write(const Geo& g, uint8_t* arena, const __half* k_new, const __half* v_new,
                          int64_t T_old, int64_t n_new, int64_t n_stride, int64_t ring_begin, cudaStream_t stream);
 
@@ -134,6 +139,11 @@ struct DecodePlan {
   int32_t nq;
   int32_t q_rows;         // query tokens per sequence in the q and out buffers (>= nq)
   int64_t q_pos0;
+  // 1: q, out, k_fresh and v_fresh are pinned host memory mapped into the
+  // device (the host-buffer entry points, word-rule widths without outlier
+  // tables or pre-RoPE keys): the host-io kernel instantiations read the
+  // query and fresh rows with plain loads and write the output to the host
+  int32_t host_io;
 };
 
 // Ragged launches: one decode launch over sequences of different lengths.

@@ -78,3 +78,34 @@ def random_stream(cfg: KiviConfig, T: int, seed: int, outliers: bool = True):
 def random_q(cfg: KiviConfig, seed: int):
     g = torch.Generator().manual_seed(seed + 99991)
     return torch.randn((cfg.batch, cfg.h_q, cfg.head_dim), generator=g).half()
+
+
+def dram_resident_cache(workload="gqa8b_b4"):
+    """A cache of a full-size workload (about 155 MB for gqa8b_b4: larger
+    than the 129 MB L2), filled from the seeded device-side stream, and its
+    decode queries."""
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
+    from kivi_quantized_kv_gb300.synth import KVStream, WORKLOADS, queries
+    w = WORKLOADS[workload]
+    dev = torch.device("cuda")
+    cache = KiviCache(KiviConfig.from_workload(w), device=dev)
+    stream = KVStream(w, device=dev)
+    t = 0
+    while t < w.tokens:
+        n = min(4096, w.tokens - t)
+        k, v = stream.next(n)
+        cache.append(k, v)
+        t += n
+    return cache, queries(w, device=dev)
+
+
+_FLUSH = {}
+
+
+def flush_l2():
+    """Writes 512 MB on the current stream, so the next launch finds none of
+    the cache in the 129 MB L2."""
+    buf = _FLUSH.get("buf")
+    if buf is None:
+        buf = _FLUSH["buf"] = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    buf.fill_(1)

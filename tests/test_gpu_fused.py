@@ -102,9 +102,12 @@ def test_fused_step_errors_leave_state_untouched():
     assert c.tokens == 3
 
 
-def test_fused_step_with_host_buffers_matches_device_buffers():
-    """kivi_append_decode_attn_host (pinned host K/V/q/out) leaves the same
-    cache bytes and output as the device-buffer step."""
+@pytest.mark.parametrize("pinned", [True, False])
+def test_fused_step_with_host_buffers_matches_device_buffers(pinned):
+    """kivi_append_decode_attn_host leaves the same cache bytes and output as
+    the device-buffer step: with pinned host K/V/q/out one launch gathers the
+    inputs over the host mapping and the step writes the output to out_host;
+    with pageable buffers the library copies them through the arena."""
     from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
     cfg = KiviConfig(bits=4, group=16, residual=32, sinks=2, h_q=8, h_kv=2, head_dim=128, batch=2, max_tokens=120)
     a, b = KiviCache(cfg), KiviCache(cfg)
@@ -113,10 +116,62 @@ def test_fused_step_with_host_buffers_matches_device_buffers():
         kt, vt = k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous()
         q = random_q(cfg, 7 * t)
         out_d = a.append_decode(kt.cuda(), vt.cuda(), q.cuda())
-        # pinned inputs held until the queued copies have run
+        # host inputs held until the queued work has run
+        if pinned:
+            k_h, v_h, q_h = kt.pin_memory(), vt.pin_memory(), q.pin_memory()
+            out_h = torch.empty_like(q).pin_memory()
+        else:
+            k_h, v_h, q_h, out_h = kt.clone(), vt.clone(), q.clone(), torch.empty_like(q)
+        b.append_decode_host(k_h, v_h, q_h, out_h)
+        torch.cuda.synchronize()
+        assert torch.equal(out_h, out_d.cpu())
+    assert torch.equal(a.cache_region(), b.cache_region())
+
+
+def test_fused_host_step_over_ragged_lengths_and_multiple_queries_per_head():
+    """Pinned host buffers through the ragged launch (sequences of different
+    lengths, GQA rep 4, one a group freeze): the same bytes and outputs as the
+    device-buffer step."""
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
+    cfg = KiviConfig(bits=2, group=32, residual=64, sinks=3, h_q=16, h_kv=4, head_dim=64, batch=3, max_tokens=400)
+    a, b = KiviCache(cfg), KiviCache(cfg)
+    k, v = random_stream(cfg, 300, seed=5)
+    counts = [300, 211, 95]
+    for c in (a, b):
+        c.append_ragged(k.cuda(), v.cuda(), counts)
+    k2, v2 = random_stream(cfg, 40, seed=6)
+    for t in range(40):
+        kt, vt = k2[:, :, t:t + 1].contiguous(), v2[:, :, t:t + 1].contiguous()
+        q = random_q(cfg, 11 * t)
+        out_d = a.append_decode(kt.cuda(), vt.cuda(), q.cuda())
         k_h, v_h, q_h = kt.pin_memory(), vt.pin_memory(), q.pin_memory()
         out_h = torch.empty_like(q).pin_memory()
         b.append_decode_host(k_h, v_h, q_h, out_h)
         torch.cuda.synchronize()
-        assert torch.equal(out_h, out_d.cpu())
+        assert torch.equal(out_h, out_d.cpu()), t
+    assert torch.equal(a.cache_region(), b.cache_region())
+
+
+@pytest.mark.parametrize("extra", [dict(bits=3), dict(bits=4, rope_base=10000.0), dict(bits=2, outlier_permille=20)])
+def test_fused_host_step_through_the_gather_launch(extra):
+    """Caches without a host-io decode instantiation (a bit-stream width,
+    pre-RoPE keys, outlier tables): pinned host buffers are gathered by one
+    launch into the staging area and the output written to out_host; the same
+    bytes and outputs as the device-buffer step."""
+    from kivi_quantized_kv_gb300 import KiviCache, KiviConfig
+    base = dict(group=32, residual=64, sinks=2, h_q=8, h_kv=2, head_dim=128, batch=2, max_tokens=300)
+    cfg = KiviConfig(**{**base, **extra})
+    a, b = KiviCache(cfg), KiviCache(cfg)
+    k, v = random_stream(cfg, 200, seed=31)
+    for c in (a, b):
+        c.append(k[:, :, :170].contiguous().cuda(), v[:, :, :170].contiguous().cuda())
+    for t in range(170, 200):
+        kt, vt = k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous()
+        q = random_q(cfg, 5 * t)
+        out_d = a.append_decode(kt.cuda(), vt.cuda(), q.cuda())
+        k_h, v_h, q_h = kt.pin_memory(), vt.pin_memory(), q.pin_memory()
+        out_h = torch.empty_like(q).pin_memory()
+        b.append_decode_host(k_h, v_h, q_h, out_h)
+        torch.cuda.synchronize()
+        assert torch.equal(out_h, out_d.cpu()), t
     assert torch.equal(a.cache_region(), b.cache_region())

@@ -161,15 +161,19 @@ def test_errors_leave_state_untouched():
     assert p.gpu.tokens == 40
 
 
-def test_host_buffer_entry_matches_device_entry():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_entry_matches_device_entry(pinned):
+    """kivi_decode_attn_host: a pinned q is gathered by one launch over the
+    host mapping and the output written to the pinned out; pageable buffers
+    are copied through the arena."""
     c = cfg(batch=2, h_q=8, h_kv=2, max_tokens=300)
     p = Pair(c)
     k, v = random_stream(c, 300, seed=10)
     p.append(k, v)
     q = random_q(c, 3)
     dev_out = p.gpu.decode(q.cuda()).cpu()
-    q_host = q.clone().pin_memory()
-    out_host = torch.empty_like(q).pin_memory()
+    q_host = q.clone().pin_memory() if pinned else q.clone()
+    out_host = torch.empty_like(q).pin_memory() if pinned else torch.empty_like(q)
     p.gpu.decode_host(q_host, out_host)
     torch.cuda.synchronize()
     assert torch.equal(dev_out, out_host)

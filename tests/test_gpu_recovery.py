@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, Pair, random_q, random_stream
+from gpu_util import TOL, Pair, random_q, random_stream, row_rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -93,30 +93,37 @@ def test_injected_launch_failures_leave_counts_and_allow_retry():
 
 def test_expired_copy_wait_sets_the_error_bit_and_the_next_call_is_exact():
     """Every decode wait for a copy is bounded.  With the limit set to 1 ns
-    (kivi_debug_set_wait_limit) the waits run out while the copies are still
-    on their way, although every copy does arrive: the warps that give up let
-    their copies land, the launch ends, and bit 0 of the error word is set.
-    The next call at the default limit matches the oracle and sets no bit."""
-    from kivi_quantized_kv_gb300 import KiviConfig, _abi
+    (kivi_debug_set_wait_limit) a wait gives up unless its copy has already
+    landed at the first look; every copy still arrives, the warps that give up
+    let their copies land, the launch ends, and bit 0 of the error word is
+    set.  The cache (gqa8b_b4, 155 MB) is larger than L2 and L2 is flushed
+    before each launch, so each warp's first group block comes from DRAM
+    while its first look is a few hundred nanoseconds after the copy's issue.
+    The next call at the default limit gives the output of a call made before
+    to within rounding (which warp claims which position, and so the order of
+    the fp32 sums, varies from call to call) and sets no bit; that output's
+    parity with the oracle is checked at this shape in test_gpu_workloads."""
+    from kivi_quantized_kv_gb300 import _abi
+    from gpu_util import dram_resident_cache, flush_l2
     L = _abi.lib()
-    cfg = KiviConfig(bits=4, group=32, residual=64, sinks=4, h_q=16, h_kv=4, head_dim=128, batch=4,
-                     max_tokens=3000)
-    p = Pair(cfg)
-    k, v = random_stream(cfg, 2500, seed=8)
-    p.append(k, v)
-    q = random_q(cfg, 5)
-    assert p.gpu.read_error() == 0
+    cache, q = dram_resident_cache()
+    flush_l2()
+    before = cache.decode(q).clone()
+    assert cache.read_error() == 0
     flags = 0
     try:
         assert L.kivi_debug_set_wait_limit(1) == 0
-        for _ in range(3):   # thousands of waits per launch; one running out is enough
-            p.gpu.decode(q.cuda())
-            flags |= p.gpu.read_error()
+        for _ in range(5):   # thousands of first looks per launch; one running out is enough
+            flush_l2()
+            cache.decode(q)
+            flags |= cache.read_error()
             if flags & 1:
                 break
     finally:
         assert L.kivi_debug_set_wait_limit(0) == 0
     assert flags & 1, flags
-    assert p.decode_err(q) <= TOL
-    assert p.gpu.read_error() == 0
-    assert p.bytes_equal()
+    flush_l2()
+    after = cache.decode(q)
+    torch.cuda.synchronize()
+    assert row_rel_err(after.float().cpu().numpy(), before.float().cpu().numpy()) <= 1e-3
+    assert cache.read_error() == 0

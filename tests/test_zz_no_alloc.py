@@ -87,22 +87,25 @@ def test_noalloc_matches_workspace_decode_twice(shape, ragged):
 def test_noalloc_timeouts_reach_the_caches_error_word():
     """The bounded copy waits of a no-allocation decode report into the
     cache's own error word (in the arena the caller owns), which
-    kivi_read_error reads: with the wait limit at 1 ns the waits run out while
-    the copies are still in flight, and the bit shows.  At the default limit
-    the next call is exact again."""
-    from kivi_quantized_kv_gb300 import KiviConfig, _abi
+    kivi_read_error reads: with the wait limit at 1 ns a wait whose copy has
+    not landed at the first look gives up, and the bit shows.  The cache
+    (gqa8b_b4, 155 MB) is larger than L2 and L2 is flushed before each call,
+    so first block copies come from DRAM.  At the default limit the next call
+    gives the output of a call made before, to within rounding."""
+    from kivi_quantized_kv_gb300 import _abi
+    from gpu_util import dram_resident_cache, flush_l2
     L = _abi.lib()
-    cfg = KiviConfig(bits=4, group=32, residual=128, sinks=4, h_q=32, h_kv=8, head_dim=128, batch=4,
-                     max_tokens=3000)
-    cache = _filled_cache(cfg, 2900, seed=5)
-    q = random_q(cfg, 3).cuda()
-    ref = cache.decode(q).float().cpu().numpy()
-    assert cache.read_error() == 0
+    cache, q = dram_resident_cache()
     o = torch.empty_like(q)
+    flush_l2()
+    assert L.kivi_decode_attn_noalloc(cache._h, _ptr(q), _ptr(o), _stream()) == _abi.KIVI_OK
+    before = o.clone()
+    assert cache.read_error() == 0
     flags = 0
     try:
         assert L.kivi_debug_set_wait_limit(1) == 0
-        for _ in range(3):
+        for _ in range(5):
+            flush_l2()
             assert L.kivi_decode_attn_noalloc(cache._h, _ptr(q), _ptr(o), _stream()) == _abi.KIVI_OK
             flags |= cache.read_error()
             if flags & 1:
@@ -110,9 +113,10 @@ def test_noalloc_timeouts_reach_the_caches_error_word():
     finally:
         assert L.kivi_debug_set_wait_limit(0) == 0
     assert flags & 1, flags
+    flush_l2()
     assert L.kivi_decode_attn_noalloc(cache._h, _ptr(q), _ptr(o), _stream()) == _abi.KIVI_OK
     torch.cuda.synchronize()
-    assert row_rel_err(o.float().cpu().numpy(), ref) <= TOL
+    assert row_rel_err(o.float().cpu().numpy(), before.float().cpu().numpy()) <= 1e-3
     assert cache.read_error() == 0
 
 
