@@ -1172,10 +1172,21 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
       if (!p_have) {
         if (p_left == 0) {   // claim the next kClaim positions of the range
           if (p_done) return;
-          const int rel = __shfl_sync(0xffffffffu, static_cast<int>(atom_add_shared_if(leader, next_s, kClaim)), 0);
+          // kClaim positions at a time while the range is far from done, one
+          // at a time over its last 2 nw positions (the CTA's warps then
+          // finish closer together); the leader reads the counter plainly
+          // to choose, so the choice may be a claim late, which is harmless
+          int packed = 0;
+          if (leader) {
+            const unsigned seen = *reinterpret_cast<volatile unsigned*>(&s_next);
+            const unsigned k = seen + 2u * static_cast<unsigned>(nw) < static_cast<unsigned>(range) ? kClaim : 1u;
+            packed = static_cast<int>(2u * atom_add_shared_if(true, next_s, k) + (k - 1u));
+          }
+          packed = __shfl_sync(0xffffffffu, packed, 0);
+          const int rel = packed >> 1;
           if (rel >= range) { p_done = true; return; }
           p_next = rel;
-          p_left = min(static_cast<int>(kClaim), range - rel);
+          p_left = min((packed & 1) + 1, range - rel);
         }
         p_rel = p_next++;
         --p_left;
