@@ -16,8 +16,9 @@
 // in chunks of 4 tokens, then the fp16 ring in chunks of 8).  The units'
 // positions, laid end to end, are cut into one equal contiguous range per CTA,
 // and the grid is one wave of resident CTAs.  Inside a CTA the warps claim
-// the range's positions two at a time from a shared counter, so a warp that
-// is held up (say, by combining a unit) simply takes fewer.
+// the range's positions two at a time from a shared counter (one at a time
+// near the range's end), so a warp that is held up (say, by combining a
+// unit) simply takes fewer, and the warps finish close together.
 //
 // Warps never wait for one another while they stream:
 //  * each warp runs its own copy pipeline: lane 0 claims a position, issues
@@ -46,6 +47,11 @@
 //    Σ_c q_c min_c (q·k̂_t = Σ_c (q_c Δ_c) code_tc + Σ_c q_c min_c exactly);
 //  * online softmax in log2 units, rescaled only when the running max grows
 //    by more than 2^8 (the stale max keeps every p <= 256);
+//  * fp16 range: a query row whose largest |q_c| exceeds 1 is stored scaled
+//    by 2^-e (so q_c Δ_c stays inside fp16 for every fp16 Δ_c; the scores
+//    take 2^e back), the values of a unit by 2^F (so small Δ_t keep P' out of
+//    the fp16 subnormals), and a chunk whose P' would pass 65504 raises the
+//    head's softmax reference by a power of two; all three are exact;
 //  * values: Oᵀ += Vᵀ P' with A = value codes (16 channels x 16 tokens: a
 //    channel's tokens are contiguous in the block) and B = p_t Δ_t 2^-k split
 //    into hi/lo fp16; P' moves from the score layout to the B layout through
@@ -54,6 +60,16 @@
 // Tails go through the same tensor-core path: the fp16 ring rows are A
 // operands as they are (values transposed by ldmatrix), and the fp32 sink
 // rows are narrowed to fp16 exactly (they were fp16 when appended).
+//
+// Pre-RoPE keys (the ROPE instantiations): q R(aθ) k̂ = (R(-a0 θ) q) (R(jθ) k̂)
+// with a0 the first position of a group or tail chunk and j < G; the query
+// rows are turned back per group, each dequantized key turned by its offset
+// from a table, and both split into hi/lo fp16 operands (rope_chunk_scores).
+//
+// Host io (the HIO instantiations, word-rule widths): q, out and the fresh
+// token's rows are pinned host memory mapped into the device; the warps load
+// the query and fresh rows with plain 16-byte loads where the device
+// instantiation issues bulk copies, and the merge writes the output there.
 //
 // Outlier tables (the OUTL instantiations; KV-cache quantization guide
 // (pigeon), "KVQuant adds": a small share of values kept in fp16 beside the
