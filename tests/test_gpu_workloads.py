@@ -70,12 +70,12 @@ def run_sampled(w, units, chunk=2048, layer=0):
 @pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa8b_b4", "gqa8b_b2", "swa_mistral", "mha7b_b3", "gqa8b_b3",
                                   "mha_d64_b3", "mha7b_o10", "mha7b_b3_o10", "gqa8b_b4_prerope"])
 def test_workload_full_size_sampled_units(name):
-    """Eight (sequence, kv head) units per workload, the first and the last
-    among them.  With 304 CTAs over at most 256 units, nearly every unit's
-    positions are cut between CTAs, so the sampled units go through the
-    cross-CTA merge."""
+    """Sixteen (sequence, kv head) units per workload (all of them when it has
+    fewer), the first and the last among them.  With 304 CTAs over at most
+    256 units, nearly every unit's positions are cut between CTAs, so the
+    sampled units go through the cross-CTA merge."""
     w = WORKLOADS[name]
-    units = sampled_units(w.batch, w.h_kv, 8, seed=len(name))
+    units = sampled_units(w.batch, w.h_kv, 16, seed=len(name))
     err = run_sampled(w, units)
     print(f"{name}: worst row error {err:.2e}")
 
