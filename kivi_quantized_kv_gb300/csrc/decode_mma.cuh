@@ -205,6 +205,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return done != 0;
 }
 
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -636,9 +642,15 @@ __device__ __forceinline__ void warp_epilogue(const Args& a, const float* slots,
 }
 
 // Epilogue of the CTA's last unit, run by every thread of the CTA.
+// `others_done`: every other CTA of the unit had published its record when a
+// warp of this CTA read the unit's counter (with acquire order), so this CTA
+// is the unit's last: it merges as soon as its own record is written, without
+// the release fence and the sign-in (the counter, at total - 1, is reset for
+// the next launch).  Otherwise it publishes, signs in, and the CTA that signs
+// in last merges.
 template <int D, bool MQ>
 __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, int slot_floats, int nw, int u,
-                                          int nh, int total, int cslot, unsigned* s_flag) {
+                                          int nh, int total, int cslot, unsigned* s_flag, bool others_done) {
   for (int i = threadIdx.x; i < nh * D; i += blockDim.x) {
     const int hh = i / D, ch = i % D;
     float M, L, O;
@@ -646,12 +658,16 @@ __device__ __forceinline__ void cta_epilogue(const Args& a, const float* slots, 
     publish<D>(a, q_row<MQ>(a, u, hh), ch, total, cslot, M, L, O);
   }
   if (total == 1) return;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *s_flag = (atomicAdd(a.counters + u, 1u) == static_cast<unsigned>(total - 1)) ? 1u : 0u;
-  __syncthreads();
-  if (!*s_flag) return;
-  __threadfence();
+  if (others_done) {
+    __syncthreads();   // this CTA's record is visible to all of its threads
+  } else {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_flag = (atomicAdd(a.counters + u, 1u) == static_cast<unsigned>(total - 1)) ? 1u : 0u;
+    __syncthreads();
+    if (!*s_flag) return;
+    __threadfence();
+  }
   for (int i = threadIdx.x; i < nh * D / 2; i += blockDim.x) merge_out<D, MQ>(a, u, i, total);
   if (threadIdx.x == 0) a.counters[u] = 0u;
 }
@@ -1098,7 +1114,7 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
   // a launch that follows in the stream may start its own set-up now; it
   // waits below for this grid to finish before it reads or writes memory
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) { s_arrive = 0u; s_done = 0u; s_next = 0u; }
+  if (threadIdx.x == 0) { s_arrive = 0u; s_done = 0u; s_next = 0u; s_flag = 0u; }
   if (lane == 0) {
     for (int s = 0; s < a.ns; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
@@ -1483,8 +1499,13 @@ __device__ __forceinline__ void decode_body(const Args& a, const RunTableT<RG>& 
         warp_epilogue<D, MQ>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, cu, &s_done);
       }
     } else {
+      // the CTA's last unit: each warp looks at the unit's counter as it
+      // arrives (the other CTAs' parts usually ended long before), so the
+      // load's latency hides behind the wait for the slowest warp
+      if (lane == 0 && total > 1 && ld_acquire_gpu(a.counters + u) == static_cast<unsigned>(total - 1))
+        atomicOr(&s_flag, 1u);
       __syncthreads();
-      cta_epilogue<D, MQ>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, &s_flag);
+      cta_epilogue<D, MQ>(a, slots, WS::kSlot / 4, nw, u, nh, total, cslot, &s_flag, s_flag != 0u);
     }
   };
 
