@@ -39,12 +39,13 @@ constexpr int kFlushThreads = 256;
 
 // Group grp of unit (bb, h): the body of both flush kernels.  Shared memory:
 // keys [G][d] fp16, values [G][d] fp16, key codes [G][d] u8, value codes
-// [G][d] u8; with outliers also the key and value flag bitmasks (G d / 32
-// words each), the selected flat indices of keys and values (n_out each) and
-// the round maxima (2 x 8 words).
+// [G][d] u8, the per-thread key (min, max) of its share of a channel (2 x
+// kFlushThreads floats); with outliers also the key and value flag bitmasks
+// (G d / 32 words each), the selected flat indices of keys and values (n_out
+// each) and the round maxima (2 x 8 words).
 size_t flush_smem(const Geo& g) {
   const size_t gd = static_cast<size_t>(g.G) * g.d;
-  size_t s = gd * (2 * sizeof(__half) + 2);
+  size_t s = gd * (2 * sizeof(__half) + 2) + 2 * kFlushThreads * sizeof(float);
   if (g.n_out > 0) s += 2 * (gd / 32) * 4 + 2 * static_cast<size_t>(g.n_out) * 4 + 16 * 4;
   return s;
 }
@@ -112,6 +113,8 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
   __half* vx = kx + G * d;
   uint8_t* kc = reinterpret_cast<uint8_t*>(vx + G * d);
   uint8_t* vc = kc + G * d;
+  float* kmn = reinterpret_cast<float*>(vc + G * d);   // [kFlushThreads]: a thread's share of a channel
+  float* kmx = kmn + kFlushThreads;
 
   uint8_t* unit = arena + (static_cast<int64_t>(bb) * g.hkv + h) * g.unit_bytes;
   const int64_t in_off = (static_cast<int64_t>(bb) * g.hkv + h) * n_stride * d;   // input row of (bb, h)
@@ -154,7 +157,7 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
 
   // outliers: flags (bit t d + c) of the key and value blocks
   const bool outl = g.n_out > 0;
-  uint32_t* kf = reinterpret_cast<uint32_t*>(vc + G * d);
+  uint32_t* kf = reinterpret_cast<uint32_t*>(kmx + kFlushThreads);
   uint32_t* vf = kf + G * d / 32;
   if (outl) {
     int* sel = reinterpret_cast<int*>(vf + G * d / 32);
@@ -163,21 +166,39 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
     select_outliers(vx, G, d, g.n_out, g.out_ent, vf, sel, red, blk + g.blk_vo);
   }
 
-  // keys: one (Δ, min) per channel over the group's tokens (its dense values)
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+  // keys: one (Δ, min) per channel over the group's tokens (its dense values).
+  // The block's threads split each channel's tokens into np parts (thread
+  // part * d + c takes channel c, tokens [part G / np, (part + 1) G / np)),
+  // whose minima and maxima meet in shared memory
+  const int np = static_cast<int>(blockDim.x) / d;   // 2 at d = 128, 4 at d = 64
+  const int kc_ch = static_cast<int>(threadIdx.x) % d, kpart = static_cast<int>(threadIdx.x) / d;
+  const bool kthread = kpart < np;
+  const int kt0 = kpart * G / np, kt1 = (kpart + 1) * G / np;
+  if (kthread) {
     float mn = INFINITY, mx = -INFINITY;
-    for (int t = 0; t < G; ++t) {
-      if (outl && flagged(kf, t * d + c)) continue;
-      const float v = __half2float(kx[t * d + c]);
+    for (int t = kt0; t < kt1; ++t) {
+      if (outl && flagged(kf, t * d + kc_ch)) continue;
+      const float v = __half2float(kx[t * d + kc_ch]);
       mn = fminf(mn, v);
       mx = fmaxf(mx, v);
+    }
+    kmn[threadIdx.x] = mn;
+    kmx[threadIdx.x] = mx;
+  }
+  __syncthreads();
+  if (kthread) {
+    const int c = kc_ch;
+    float mn = INFINITY, mx = -INFINITY;
+    for (int p2 = 0; p2 < np; ++p2) {
+      mn = fminf(mn, kmn[p2 * d + c]);
+      mx = fmaxf(mx, kmx[p2 * d + c]);
     }
     if (mn > mx) { mn = 0.0f; mx = 0.0f; }   // every value an outlier
     mn = __fadd_rn(mn, 0.0f);
     mx = __fadd_rn(mx, 0.0f);
     const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), top));
     const float dq = __half2float(d16);
-    for (int t = 0; t < G; ++t) {
+    for (int t = kt0; t < kt1; ++t) {
       int code = 0;
       if (dq != 0.0f && !(outl && flagged(kf, t * d + c))) {
         const float r = rintf(__fdiv_rn(__fsub_rn(__half2float(kx[t * d + c]), mn), dq));
@@ -185,8 +206,10 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
       }
       kc[t * d + c] = static_cast<uint8_t>(code);
     }
-    ks_out[c] = d16;
-    ks_out[d + c] = __float2half_rn(mn);
+    if (kpart == 0) {
+      ks_out[c] = d16;
+      ks_out[d + c] = __float2half_rn(mn);
+    }
   }
 
   // values: one (Δ, min) per token over the channels; one warp per token
