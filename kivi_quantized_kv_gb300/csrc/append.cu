@@ -13,7 +13,9 @@
 // round-to-nearest-even intrinsic (__fsub_rn, __fdiv_rn, __fadd_rn), so the
 // compiler cannot contract or reorder it; fp16 conversion is
 // __float2half_rn; "round" is rintf (half to even).  min and max are
-// canonicalised with + 0.0f so -0 and +0 give the same bytes.
+// canonicalised with + 0.0f so -0 and +0 give the same bytes.  A code is
+// rintf of the correctly rounded quotient (x - min) / Δ, computed through
+// the correctly rounded 1/Δ (code_of), which rounds to the same integer.
 //
 // Dense-and-sparse outliers (when the cache keeps them; pigeon guide, "KVQuant
 // adds"): before the quantizer, the n_out values of largest magnitude of the
@@ -103,6 +105,19 @@ __device__ __forceinline__ void select_outliers(const __half* x, int G, int d, i
 }
 
 __device__ __forceinline__ bool flagged(const uint32_t* f, int i) { return (f[i >> 5] >> (i & 31)) & 1u; }
+
+// rintf(__fdiv_rn(a, dq)) for 0 <= a <= max - min, dq the fp16-rounded
+// (max - min) / (2^b - 1) and rq = __frcp_rn(dq).  Rounding to nearest keeps
+// dq at least half of the unrounded step, so the exact quotient Q = a / dq
+// is below 512.  The product q = RN(a rq) lies within Q 2^-23 <= 2^-14 of Q
+// and the division's RN(Q) within 2^-16, so q and RN(Q) are less than 2^-13
+// apart and round to the same integer unless q lies within 2^-11 of a
+// half-integer; there the division itself is done.
+__device__ __forceinline__ float code_of(float a, float dq, float rq) {
+  float q = __fmul_rn(a, rq);
+  if (fabsf(q - floorf(q) - 0.5f) < 0x1p-11f) q = __fdiv_rn(a, dq);
+  return rintf(q);
+}
 
 __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ arena,
                                             const __half* __restrict__ k_new, const __half* __restrict__ v_new,
@@ -198,10 +213,11 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
     mx = __fadd_rn(mx, 0.0f);
     const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), top));
     const float dq = __half2float(d16);
+    const float rq = dq != 0.0f ? __frcp_rn(dq) : 0.0f;
     for (int t = kt0; t < kt1; ++t) {
       int code = 0;
       if (dq != 0.0f && !(outl && flagged(kf, t * d + c))) {
-        const float r = rintf(__fdiv_rn(__fsub_rn(__half2float(kx[t * d + c]), mn), dq));
+        const float r = code_of(__fsub_rn(__half2float(kx[t * d + c]), mn), dq, rq);
         code = static_cast<int>(fminf(fmaxf(r, 0.0f), top));
       }
       kc[t * d + c] = static_cast<uint8_t>(code);
@@ -232,10 +248,11 @@ __device__ __forceinline__ void flush_group(const Geo& g, uint8_t* __restrict__ 
     mx = __fadd_rn(mx, 0.0f);
     const __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), top));
     const float dq = __half2float(d16);
+    const float rq = dq != 0.0f ? __frcp_rn(dq) : 0.0f;
     for (int c = lane; c < d; c += 32) {
       int code = 0;
       if (dq != 0.0f && !(outl && flagged(vf, t * d + c))) {
-        const float r = rintf(__fdiv_rn(__fsub_rn(__half2float(vx[t * d + c]), mn), dq));
+        const float r = code_of(__fsub_rn(__half2float(vx[t * d + c]), mn), dq, rq);
         code = static_cast<int>(fminf(fmaxf(r, 0.0f), top));
       }
       vc[t * d + c] = static_cast<uint8_t>(code);
